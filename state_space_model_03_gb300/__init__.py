@@ -1,0 +1,17 @@
+"""GB300-native Mamba-1 selective-scan forward.
+
+``selective_scan_fn`` runs the hand-written sm_103a kernels of ``libssfwd.so``
+through its C ABI (``include/ssfwd.h``). There is no CPU fallback: the call
+raises if the CUDA library is missing or no GPU is present.
+"""
+
+__all__ = ["selective_scan_fn", "selective_scan_fn_host"]
+
+
+def __getattr__(name):
+    # Lazy: importing the package (e.g. for the input generator) does not load
+    # the CUDA library; the first use of the API does, and fails loudly.
+    if name in __all__:
+        from . import api
+        return getattr(api, name)
+    raise AttributeError(name)
