@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""Selective-scan forward bench: HBM GB/s, (b*d*l) elements/s and the fraction
+of the GB300 HBM roofline, on seeded synthetic Mamba-layer workloads.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one selective-scan forward over the whole workload (all of the
+path: softplus, exp, recurrence, C contraction, D skip, silu gate, last_state),
+inputs resident in HBM. Each step is preceded (outside its timed interval) by a
+write of 2x the L2 size so that no input is served from L2. Kernel time is
+measured with CUDA events on the launching stream; the reported time is the
+max over ranks. Under torchrun every rank runs the full workload on its own GPU
+(independent problems, no data-path collective: weak scaling).
+
+--impl reference times the fp64 CPU oracle (as it stands) on the host cores on
+bounded samples of the same workload, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from state_space_model_03_gb300 import workloads  # noqa: E402
+
+NAMES = ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")
+METRIC = "selective-scan fwd HBM GB/s (compulsory bytes / kernel time)"
+DEFAULT_WORKLOAD = "mamba130m_bf16"
+# FP32 lane-ops per (state, step) pair on the dominant path: exponent product,
+# dt*u*B product, state FMA, C contraction FMA (3 for fixed B/C, where the
+# state is carried as x / B).
+PAIR_FP32_OPS = {"variable": 4, "fixed": 3}
+
+
+def _env_int(k, d):
+    try:
+        return int(os.environ.get(k, d))
+    except ValueError:
+        return d
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "state_space_model_03_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources and this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != _kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+                power.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s, p in zip(sm, power) if p > 300.0] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(loaded),
+                "power_w_max": max(power) if power else None}
+
+
+def _oracle_rows_rate(w, x, rows, threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.selective_scan_rows(rows, **{k: x[k] for k in NAMES}, delta_softplus=x["delta_softplus"],
+                               threads=threads)
+    return time.perf_counter() - t0
+
+
+def _row_bytes(w):
+    """Compulsory bytes of one (batch, channel) row, for sampled CPU timing."""
+    return workloads.compulsory_bytes(w) / (w.batch * w.dim)
+
+
+def cpu_baseline(w, x, budget_s=15.0):
+    """Oracle timed on a bounded sample of rows (all host cores)."""
+    import numpy as np
+    threads = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    nrows = w.batch * w.dim
+    probe = [(int(r // w.dim), int(r % w.dim)) for r in rng.choice(nrows, size=min(nrows, threads), replace=False)]
+    dt = _oracle_rows_rate(w, x, probe, threads)
+    per_row = dt / len(probe) * min(threads, len(probe))  # seconds of one row on one core
+    want = int(min(nrows, max(threads, budget_s * threads / max(per_row, 1e-9))))
+    sel = rng.choice(nrows, size=want, replace=False)
+    rows = [(int(r // w.dim), int(r % w.dim)) for r in sel]
+    dt = _oracle_rows_rate(w, x, rows, threads)
+    gbs = len(rows) * _row_bytes(w) / dt / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "elems_per_s": len(rows) * w.seqlen / dt, "seconds": dt,
+            "sample": f"{len(rows)} of {nrows} (batch, channel) rows of {w.name}, full seqlen {w.seqlen}, "
+                      f"fp64 C oracle, {threads} host threads"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 CPU oracle as it stands, on host cores."""
+    if rank != 0:
+        return
+    import numpy as np
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w)
+    threads = os.cpu_count() or 1
+    nrows = w.batch * w.dim
+    rng = np.random.default_rng(1)
+    probe = [(int(r // w.dim), int(r % w.dim)) for r in rng.choice(nrows, size=min(nrows, threads), replace=False)]
+    per_row = _oracle_rows_rate(w, x, probe, threads) / len(probe) * min(threads, len(probe))
+    budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))  # seconds per step
+    R = int(min(nrows, max(1, budget * threads / max(per_row, 1e-9))))
+    order = rng.permutation(nrows)
+    step_rows = [[(int(order[(i * R + k) % nrows] // w.dim), int(order[(i * R + k) % nrows] % w.dim))
+                  for k in range(R)] for i in range(args.steps + args.warmup)]
+    for i in range(args.warmup):
+        _oracle_rows_rate(w, x, step_rows[i], threads)
+    times = [_oracle_rows_rate(w, x, step_rows[args.warmup + i], threads) for i in range(args.steps)]
+    t = sum(times)
+    gbs = args.steps * R * _row_bytes(w) / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, Mamba-layer shapes)",
+            "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen,
+                       "dstate": w.dstate, "groups": w.groups, "bc": w.bc, "io_dtype": w.dtype},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "kind": "oracle", "cores": threads,
+                             "sample": f"each step: {R} of {nrows} (batch, channel) rows of {w.name}, "
+                                       f"full seqlen, fp64 C oracle on {threads} host threads"},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from state_space_model_03_gb300 import api
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w)
+    lib = api.load_library()
+    d = {k: (None if x[k] is None else x[k].to(dev)) for k in NAMES}
+    nu = api.normalise(*(d[k] for k in NAMES))
+    out = torch.empty(w.batch, w.dim, w.seqlen, dtype=d["u"].dtype, device=dev)
+    last = (torch.empty(w.batch, w.dim, w.dstate, dtype=torch.float32, device=dev)
+            if w.return_last_state else None)
+    params = api.make_params(*nu, w.delta_softplus, out, last)
+    pref = ctypes.byref(params)
+    stream = torch.cuda.Stream(device=dev)
+    sptr = stream.cuda_stream
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def step():
+        st = lib.ss_fwd(pref, sptr)
+        if st != 0:
+            raise RuntimeError(api.status_string(st))
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            flush_buf.fill_(i & 0xFF)
+            step()
+    stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk, torch.cuda.stream(stream):
+        region0.record(stream)
+        for i in range(args.steps):
+            flush_buf.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        region1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    if api.device_error() != 0:
+        raise RuntimeError("device error word set during the bench")
+    kms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(kms) / len(kms)
+    region_ms = region0.elapsed_time(region1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms, region_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, region_ms = float(t[0]), float(t[1])
+    cb = workloads.compulsory_bytes(w)
+    gbs = world * cb / (ms * 1e-3) / 1e9
+    elems = world * w.elems / (ms * 1e-3)
+    peak, peak_src = _peaks()
+    clocks = clk.summary()
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    hx = {k: (None if x[k] is None else x[k].pin_memory()) for k in NAMES}
+    runner = api.HostRunner(**hx, delta_softplus=w.delta_softplus, return_last_state=w.return_last_state,
+                            device=dev)
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        runner.run(**hx)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(runner.stream)
+    for _ in range(e2e_steps):
+        runner.enqueue(**hx)
+    e1.record(runner.stream)
+    runner.stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    if rank != 0:
+        return
+    sm_mhz = clocks.get("sm_mhz") or 1900.0
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    pair_ops = PAIR_FP32_OPS[w.bc]
+    alu_floor_s = w.elems * w.dstate * pair_ops / (128.0 * nsm * sm_mhz * 1e6)
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {"fp32": "f32", "fp16": "f16", "bf16": "bf16"}[w.dtype],
+        "data": "synthetic (seeded, Mamba-layer shapes)",
+        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": w.dstate,
+                   "groups": w.groups, "bc": w.bc, "io_dtype": w.dtype, "z": w.has_z,
+                   "return_last_state": w.return_last_state, "parallelism": f"independent x{world}",
+                   "l2": f"flushed before every step ({2 * l2 >> 20} MiB write, outside the kernel interval)"},
+        "elems_per_s": elems,
+        "compulsory_bytes_per_step": cb,
+        "region_ms_per_step_incl_flush": region_ms,
+        "roofline": {"bound": "hbm", "achieved": cb / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": cb / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
+                     "traffic": _traffic(w.name)},
+        "alu_floor": {"fp32_lane_ops_per_pair": pair_ops, "pairs_per_step": w.elems * w.dstate,
+                      "fp32_lanes_per_sm_clk": 128, "sms": nsm, "sm_mhz": sm_mhz,
+                      "floor_ms": alu_floor_s * 1e3,
+                      "gbs_at_floor": cb / alu_floor_s / 1e9},
+        "e2e": {"value": world * cb / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
+                "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "kernel_hash": _kernel_hash(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = _env_int("RANK", 0), _env_int("WORLD_SIZE", 1), _env_int("LOCAL_RANK", 0)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

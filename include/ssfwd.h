@@ -1,0 +1,150 @@
+/*
+ * ssfwd.h - C ABI of libssfwd.so, the GB300 (sm_103a) Mamba-1 selective-scan
+ * forward.
+ *
+ * The operation is the forward pass of `selective_scan_fn(u, delta, A, B, C,
+ * D=None, z=None, delta_bias=None, delta_softplus=False,
+ * return_last_state=False)`, whose operands and shapes are those of the page
+ * "PaddleNLP Kernel 算子库：CUDA 与 Triton 双实现的高性能 NLP GPU 算子实战指南",
+ * section 4.1 "CUDA 算子 selective_scan". That page names the operator but
+ * prints no formula; the recurrence computed is the Mamba-1 selective scan
+ * with an Euler input term, per (batch b, channel d, state n, step t):
+ *
+ *     dt    = softplus(delta[b,d,t] + delta_bias[d])   (plain sum if !delta_softplus)
+ *     x[n]  = exp(dt * A[d,n]) * x[n] + dt * B[n,t] * u[b,d,t]   (x = 0 before t = 0)
+ *     y     = sum_n C[n,t] * x[n] + D[d] * u[b,d,t]
+ *     out   = y * silu(z[b,d,t])  if z is given, else y;  silu(v) = v / (1 + e^-v)
+ *     last_state[b,d,n] = x[n] after the last step
+ *
+ * B[n,t]/C[n,t] is B[d,n] for fixed B/C, or B[b, d / (dim/ngroups), n, t] for
+ * variable (grouped) B/C; the page's 3-D (batch, dstate, seqlen) form is
+ * ngroups = 1. The state is carried in fp32.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers in ss_fwd_params are DEVICE pointers owned by the
+ *     caller. The library allocates no memory, keeps no per-call global state,
+ *     never synchronises, and is safe to call from several host threads.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Work is enqueued on it; results are ready when it is.
+ *   - Validation happens before anything is enqueued: on any error status
+ *     nothing was launched and no memory was touched.
+ *   - Asynchronous device faults surface on the caller's next synchronisation
+ *     with the stream, as for any CUDA launch.
+ */
+#ifndef SSFWD_H_
+#define SSFWD_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SS_ABI_VERSION 1
+
+/* Element types. u, delta, z and out share `in_dtype`. */
+typedef enum ss_dtype { SS_F32 = 0, SS_F16 = 1, SS_BF16 = 2 } ss_dtype;
+
+/* B/C forms (section 4.1: fixed (dim, dstate), or varying over the sequence as
+ * (batch, groups, dstate, seqlen); (batch, dstate, seqlen) is groups = 1). */
+typedef enum ss_bc_mode { SS_BC_FIXED = 0, SS_BC_VARIABLE = 1 } ss_bc_mode;
+
+typedef enum ss_status {
+  SS_OK = 0,
+  SS_ERR_NULL = 1,         /* a required pointer is NULL                      */
+  SS_ERR_SHAPE = 2,        /* negative size, dim % ngroups != 0, ...          */
+  SS_ERR_DTYPE = 3,        /* unknown dtype or unsupported dtype combination  */
+  SS_ERR_STRIDE = 4,       /* seqlen (or state, for fixed B/C / A) stride != 1, or a negative stride */
+  SS_ERR_ALIGN = 5,        /* a pointer is not aligned to its element size    */
+  SS_ERR_ALIAS = 6,        /* out or last_state overlaps an input or each other */
+  SS_ERR_UNSUPPORTED = 7,  /* dstate > 64, or a feature this build lacks      */
+  SS_ERR_CUDA = 8,         /* a CUDA runtime/driver call failed               */
+  SS_ERR_INTERNAL = 9,     /* a device-side self-check tripped                */
+  SS_ERR_VERSION = 10      /* params->abi_version != SS_ABI_VERSION           */
+} ss_status;
+
+/*
+ * Parameters of one forward call. Strides are in ELEMENTS of the tensor's own
+ * type and may be any non-negative value (views are fine) except where a unit
+ * stride is required.
+ *
+ *   u, delta, z, out   (batch, dim, seqlen), stride[2] (seqlen) must be 1.
+ *                      dtype in_dtype. z may be NULL (no gating).
+ *   A                  (dim, dstate) fp32, A_stride = {dim, state}; state stride 1.
+ *   B, C  variable     (batch, ngroups, dstate, seqlen), dtype bc_dtype
+ *                      (in_dtype or SS_F32); stride = {batch, group, state, seqlen},
+ *                      seqlen stride 1.
+ *         fixed        (dim, dstate) fp32; stride[0] = dim stride, stride[1]
+ *                      must be 1, stride[2..3] ignored. ngroups is ignored.
+ *   D, delta_bias      (dim,) fp32, contiguous; NULL = absent (treated as 0).
+ *   out                written, in_dtype, rounded once to nearest-even.
+ *   last_state         (batch, dim, dstate) fp32 with last_state_stride =
+ *                      {batch, dim, state}, state stride 1; NULL = not returned.
+ *                      For seqlen == 0 it is filled with zeros.
+ *
+ * Sizes: batch, dim, seqlen >= 0; 1 <= dstate <= 64. batch*dim*seqlen == 0 is
+ * a no-op (except the zero fill of last_state when seqlen == 0).
+ */
+typedef struct ss_fwd_params {
+  int32_t abi_version;      /* must be SS_ABI_VERSION */
+  int32_t in_dtype;         /* ss_dtype */
+  int32_t bc_dtype;         /* ss_dtype */
+  int32_t bc_mode;          /* ss_bc_mode */
+  int32_t delta_softplus;   /* nonzero: dt = softplus(delta + delta_bias) */
+  int32_t reserved0;
+  int64_t batch, dim, seqlen, dstate, ngroups;
+  const void *u, *delta, *z, *B, *C;
+  const float *A, *D, *delta_bias;
+  void *out;
+  float *last_state;
+  int64_t u_stride[3], delta_stride[3], z_stride[3], out_stride[3];
+  int64_t B_stride[4], C_stride[4];
+  int64_t A_stride[2];
+  int64_t last_state_stride[3];
+} ss_fwd_params;
+
+/* SS_ABI_VERSION of the loaded library. */
+int ss_abi_version(void);
+
+/* Static, never-NULL description of a status code. */
+const char *ss_status_string(int status);
+
+/* Validate `p` without launching anything (no CUDA call is made). Returns the
+ * status ss_fwd would return before launching. */
+int ss_fwd_validate(const ss_fwd_params *p);
+
+/* The selective-scan forward on device buffers, enqueued on `stream`.
+ * Returns SS_OK once enqueued, or an error status with nothing enqueued
+ * (SS_ERR_CUDA if the launch itself failed). */
+int ss_fwd(const ss_fwd_params *p, void *stream);
+
+/*
+ * The same forward for HOST data, with the host<->device copies enqueued on
+ * the same stream: each non-NULL host input (`h_u`, `h_delta`, `h_z`, `h_B`,
+ * `h_C`, `h_A`, `h_D`, `h_delta_bias`) is copied into the matching device
+ * buffer of `p` (which must already exist and be laid out contiguously, as
+ * the strides in `p` must then describe), the kernel runs, and `out` (and
+ * `last_state` when `h_last_state` is non-NULL) are copied back into the host
+ * buffers. Host buffers should be pinned for the copies to be asynchronous.
+ * Nothing is synchronised: host outputs are valid once `stream` completes.
+ * Copy sizes are the contiguous sizes of each tensor. Returns as ss_fwd.
+ */
+int ss_fwd_host(const ss_fwd_params *p,
+                const void *h_u, const void *h_delta, const void *h_z,
+                const void *h_B, const void *h_C,
+                const float *h_A, const float *h_D, const float *h_delta_bias,
+                void *h_out, float *h_last_state, void *stream);
+
+/*
+ * Device-side error word of the library on the current device (nonzero after
+ * a kernel gave up on a bounded wait or tripped a self-check; 0 otherwise).
+ * Reading it synchronises with the device. `clear` nonzero resets it to 0.
+ * Returns SS_OK and writes the word into *out_word, or SS_ERR_CUDA.
+ */
+int ss_device_error(int32_t *out_word, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSFWD_H_ */

@@ -1,0 +1,276 @@
+"""Python binding of libssfwd.so (C ABI in include/ssfwd.h).
+
+Argument marshalling only: shapes, strides, dtypes and device pointers are
+read from torch tensors and handed to ``ss_fwd``; every step of the
+selective scan runs in the library's CUDA kernels. torch supplies device
+memory and the current stream. There is no CPU fallback: without the built
+library or a CUDA device the calls raise.
+
+``selective_scan_fn`` mirrors the signature and layout handling of the page
+"PaddleNLP Kernel 算子库：CUDA 与 Triton 双实现的高性能 NLP GPU 算子实战指南",
+section 4.1: tensors whose last stride is not 1 are made contiguous, a 3-D
+(batch, dstate, seqlen) B/C is treated as 4-D with one group, and the result
+is ``out`` or ``(out, last_state)``. Forward only (no autograd).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libssfwd.so")
+_lock = threading.Lock()
+_lib = None
+
+SS_F32, SS_F16, SS_BF16 = 0, 1, 2
+SS_BC_FIXED, SS_BC_VARIABLE = 0, 1
+SS_ABI_VERSION = 1
+_DT = {torch.float32: SS_F32, torch.float16: SS_F16, torch.bfloat16: SS_BF16}
+
+_i64x2, _i64x3, _i64x4 = ctypes.c_int64 * 2, ctypes.c_int64 * 3, ctypes.c_int64 * 4
+
+
+class SSFwdParams(ctypes.Structure):
+    """Mirror of ``ss_fwd_params``."""
+    _fields_ = [
+        ("abi_version", ctypes.c_int32), ("in_dtype", ctypes.c_int32), ("bc_dtype", ctypes.c_int32),
+        ("bc_mode", ctypes.c_int32), ("delta_softplus", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+        ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+        ("u", ctypes.c_void_p), ("delta", ctypes.c_void_p), ("z", ctypes.c_void_p),
+        ("B", ctypes.c_void_p), ("C", ctypes.c_void_p),
+        ("A", ctypes.c_void_p), ("D", ctypes.c_void_p), ("delta_bias", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("last_state", ctypes.c_void_p),
+        ("u_stride", _i64x3), ("delta_stride", _i64x3), ("z_stride", _i64x3), ("out_stride", _i64x3),
+        ("B_stride", _i64x4), ("C_stride", _i64x4), ("A_stride", _i64x2), ("last_state_stride", _i64x3),
+    ]
+
+
+class SSError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"ss_fwd failed: status {status} ({msg})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libssfwd.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"libssfwd.so is not built ({_LIB_PATH}); build it with "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.POINTER(SSFwdParams)
+            vp = ctypes.c_void_p
+            lib.ss_abi_version.restype = ctypes.c_int
+            lib.ss_status_string.argtypes = [ctypes.c_int]
+            lib.ss_status_string.restype = ctypes.c_char_p
+            lib.ss_fwd_validate.argtypes = [P]
+            lib.ss_fwd_validate.restype = ctypes.c_int
+            lib.ss_fwd.argtypes = [P, vp]
+            lib.ss_fwd.restype = ctypes.c_int
+            lib.ss_fwd_host.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.ss_fwd_host.restype = ctypes.c_int
+            lib.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
+            lib.ss_device_error.restype = ctypes.c_int
+            if lib.ss_abi_version() != SS_ABI_VERSION:
+                raise RuntimeError("libssfwd.so ABI version mismatch")
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().ss_status_string(status).decode()
+
+
+def _check(status: int):
+    if status != 0:
+        raise SSError(status, status_string(status))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _unit_last(t):
+    if t is not None and t.dim() > 0 and t.stride(-1) != 1:
+        return t.contiguous()
+    return t
+
+
+def normalise(u, delta, A, B, C, D=None, z=None, delta_bias=None):
+    """Layout handling of the page's selective_scan_fn: unit last stride (else
+    .contiguous()), 3-D B/C -> 4-D with one group. Returns the tensors."""
+    if A.is_complex():
+        raise NotImplementedError("complex A is not supported (real A only)")
+    u, delta, z, B, C, A = (_unit_last(t) for t in (u, delta, z, B, C, A))
+    if B.dim() == 3:
+        B = B.unsqueeze(1)
+    if C.dim() == 3:
+        C = C.unsqueeze(1)
+    if D is not None:
+        D = D.contiguous()
+    if delta_bias is not None:
+        delta_bias = delta_bias.contiguous()
+    return u, delta, A, B, C, D, z, delta_bias
+
+
+def make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last_state) -> SSFwdParams:
+    """Fill an ss_fwd_params from already-normalised tensors (see normalise)."""
+    if u.dim() != 3:
+        raise ValueError("u must be (batch, dim, seqlen)")
+    if u.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {u.dtype}")
+    for name, t in (("delta", delta), ("z", z)):
+        if t is not None and (t.dtype != u.dtype or t.shape != u.shape):
+            raise TypeError(f"{name} must match u in shape and dtype")
+    for name, t in (("A", A), ("D", D), ("delta_bias", delta_bias)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    batch, dim, seqlen = u.shape
+    if A.dim() != 2 or A.shape[0] != dim:
+        raise ValueError("A must be (dim, dstate)")
+    dstate = A.shape[1]
+    p = SSFwdParams()
+    p.abi_version = SS_ABI_VERSION
+    p.in_dtype = _DT[u.dtype]
+    if B.dim() == 2:
+        p.bc_mode, p.ngroups = SS_BC_FIXED, 1
+        if B.dtype != torch.float32 or C.dtype != torch.float32:
+            raise TypeError("fixed (dim, dstate) B/C must be float32")
+        if tuple(B.shape) != (dim, dstate) or tuple(C.shape) != (dim, dstate):
+            raise ValueError("fixed B/C must be (dim, dstate)")
+        p.B_stride[:] = [B.stride(0), B.stride(1), 0, 0]
+        p.C_stride[:] = [C.stride(0), C.stride(1), 0, 0]
+    elif B.dim() == 4:
+        p.bc_mode, p.ngroups = SS_BC_VARIABLE, B.shape[1]
+        if B.dtype not in (u.dtype, torch.float32) or C.dtype != B.dtype:
+            raise TypeError("variable B/C must share a dtype, equal to u's or float32")
+        want = (batch, B.shape[1], dstate, seqlen)
+        if tuple(B.shape) != want or tuple(C.shape) != want:
+            raise ValueError(f"variable B/C must be {want}")
+        p.B_stride[:] = list(B.stride())
+        p.C_stride[:] = list(C.stride())
+    else:
+        raise ValueError("B/C must be (dim, dstate), (batch, dstate, seqlen) or (batch, groups, dstate, seqlen)")
+    p.bc_dtype = _DT[B.dtype]
+    p.delta_softplus = int(bool(delta_softplus))
+    p.batch, p.dim, p.seqlen, p.dstate = batch, dim, seqlen, dstate
+    p.u, p.delta, p.z, p.B, p.C = _ptr(u), _ptr(delta), _ptr(z), _ptr(B), _ptr(C)
+    p.A, p.D, p.delta_bias = _ptr(A), _ptr(D), _ptr(delta_bias)
+    p.out, p.last_state = _ptr(out), _ptr(last_state)
+    p.u_stride[:] = list(u.stride())
+    p.delta_stride[:] = list(delta.stride())
+    p.z_stride[:] = list(z.stride()) if z is not None else [0, 0, 1]
+    p.out_stride[:] = list(out.stride())
+    p.A_stride[:] = list(A.stride())
+    p.last_state_stride[:] = list(last_state.stride()) if last_state is not None else [0, 0, 1]
+    return p
+
+
+def selective_scan_fn(u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                      delta_softplus=False, return_last_state=False):
+    """Selective-scan forward on CUDA tensors; runs on the current stream.
+
+    u, delta, z: (batch, dim, seqlen), fp32/fp16/bf16, one dtype.
+    A: (dim, dstate) fp32 (real). B, C: (dim, dstate) fp32 fixed, or
+    (batch, dstate, seqlen) / (batch, groups, dstate, seqlen) in u's dtype or
+    fp32. D, delta_bias: (dim,) fp32. Returns out (u's dtype), or
+    (out, last_state) with last_state (batch, dim, dstate) fp32.
+    """
+    if not u.is_cuda:
+        raise RuntimeError("selective_scan_fn needs CUDA tensors (there is no CPU path)")
+    lib = load_library()
+    u, delta, A, B, C, D, z, delta_bias = normalise(u, delta, A, B, C, D, z, delta_bias)
+    out = torch.empty(u.shape, dtype=u.dtype, device=u.device)
+    last = (torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
+            if return_last_state else None)
+    p = make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last)
+    stream = torch.cuda.current_stream(u.device).cuda_stream
+    with torch.cuda.device(u.device):
+        _check(lib.ss_fwd(ctypes.byref(p), stream))
+    return (out, last) if return_last_state else out
+
+
+class HostRunner:
+    """End-to-end runner for HOST tensors through ``ss_fwd_host``: each call
+    copies the (pinned) host inputs into device buffers owned by this object,
+    runs the kernel and copies ``out`` (and ``last_state``) back, all on one
+    stream; ``run`` returns once the stream has completed.
+
+    The device buffers are allocated once (torch) for the given shapes/dtypes;
+    host tensors passed to ``run`` must have exactly those shapes and dtypes
+    and be contiguous.
+    """
+
+    def __init__(self, u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                 delta_softplus=False, return_last_state=False, device="cuda"):
+        lib = load_library()
+        self._lib = lib
+        host = normalise(u, delta, A, B, C, D, z, delta_bias)
+        self._host_shapes = [None if t is None else (tuple(t.shape), t.dtype) for t in host]
+        dev = [None if t is None else torch.empty(t.shape, dtype=t.dtype, device=device) for t in host]
+        self.dev = dev
+        du = dev[0]
+        self.out = torch.empty(du.shape, dtype=du.dtype, device=device)
+        self.last = (torch.empty((du.shape[0], du.shape[1], dev[2].shape[1]), dtype=torch.float32, device=device)
+                     if return_last_state else None)
+        self.params = make_params(*dev, delta_softplus, self.out, self.last)
+        self.h_out = torch.empty(du.shape, dtype=du.dtype, pin_memory=True)
+        self.h_last = (torch.empty(self.last.shape, dtype=torch.float32, pin_memory=True)
+                       if return_last_state else None)
+        self.stream = torch.cuda.Stream(device=device)
+
+    @property
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.dev if t is not None)
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.h_out.numel() * self.h_out.element_size() + (
+            0 if self.h_last is None else self.h_last.numel() * 4)
+
+    def enqueue(self, u, delta, A, B, C, D=None, z=None, delta_bias=None):
+        host = normalise(u, delta, A, B, C, D, z, delta_bias)
+        for t, want in zip(host, self._host_shapes):
+            if (t is None) != (want is None) or (t is not None and (tuple(t.shape), t.dtype) != want):
+                raise ValueError("host tensors do not match the runner's shapes/dtypes")
+            if t is not None and (t.is_cuda or not t.is_contiguous()):
+                raise ValueError("host tensors must be contiguous CPU tensors")
+        hp = [None if t is None else t.data_ptr() for t in host]
+        # order of ss_fwd_host: u, delta, z, B, C, A, D, delta_bias
+        _check(self._lib.ss_fwd_host(
+            ctypes.byref(self.params), hp[0], hp[1], hp[6], hp[3], hp[4], hp[2], hp[5], hp[7],
+            self.h_out.data_ptr(), None if self.h_last is None else self.h_last.data_ptr(),
+            self.stream.cuda_stream))
+
+    def run(self, *args, **kwargs):
+        self.enqueue(*args, **kwargs)
+        self.stream.synchronize()
+        return (self.h_out, self.h_last) if self.h_last is not None else self.h_out
+
+
+def selective_scan_fn_host(u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                           delta_softplus=False, return_last_state=False):
+    """selective_scan_fn for CPU tensors: copies in, runs on the GPU, copies
+    out (through ss_fwd_host). Returns CPU tensors."""
+    r = HostRunner(u, delta, A, B, C, D, z, delta_bias, delta_softplus, return_last_state)
+    res = r.run(u.contiguous(), delta.contiguous(), A, B.contiguous(), C.contiguous(), D,
+                None if z is None else z.contiguous(), delta_bias)
+    if return_last_state:
+        return res[0].clone(), res[1].clone()
+    return res.clone()
+
+
+def device_error(clear: bool = False) -> int:
+    """The library's device error word on the current device (0 = none)."""
+    w = ctypes.c_int32(0)
+    _check(load_library().ss_device_error(ctypes.byref(w), int(bool(clear))))
+    return int(w.value)

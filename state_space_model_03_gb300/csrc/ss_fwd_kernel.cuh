@@ -1,0 +1,665 @@
+// Selective-scan forward kernels for sm_103a (GB300).
+//
+// Operation (operands of `selective_scan_fn`, page "PaddleNLP Kernel 算子库：
+// CUDA 与 Triton 双实现的高性能 NLP GPU 算子实战指南", section 4.1): per batch b,
+// channel d, state n and step t
+//   dt = softplus(delta + delta_bias); x_n = exp(dt A_n) x_n + dt B_n,t u_t;
+//   y = sum_n C_n,t x_n + D u_t; out = y silu(z_t); last_state = final x.
+//
+// Work decomposition (one CTA = one (batch, group, channel tile)):
+//   * 4 compute warps; each channel is owned by TN = NP/K adjacent lanes, each
+//     lane holding K of the channel's NP (padded) states in fp32 registers, so
+//     the recurrence runs sequentially in time with no scan overhead.
+//   * 1 producer warp streams 64-step (16-bit) or 32-step (fp32) chunks of u,
+//     delta, z with TMA (cp.async.bulk.tensor, 128-byte swizzle) into a
+//     2-stage mbarrier ring, and the (batch, group) B/C tile of the chunk,
+//     which it converts once per CTA into fp32 [t][n] so that every lane reads
+//     its K states of B and C with one 16-byte shared load.
+//   * Per-element work (softplus, dt*u, D skip, silu gate, rounding) is done
+//     once per element: within a 16-step sub-chunk, lane j of a channel takes
+//     steps [j*S/TN, (j+1)*S/TN), publishing (dt, dt, w, w) to shared memory
+//     before the recurrence and summing the TN partial y's after it.
+//   * exp(dt A) = exp2(dt * A log2e) with A pre-scaled; state pairs use packed
+//     fp32x2 multiply/FMA (half the issue slots of scalar FFMA).
+//   * Fixed B/C (dim, dstate): B and C are per-channel constants, so the state
+//     is carried as xi = x / B (x = B xi), which removes the dt*u*B product:
+//     xi = exp(dt A) xi + dt u, y = sum_n (C_n B_n) xi_n. Exact algebra; B = 0
+//     gives x = 0 as required.
+// Every mbarrier wait is bounded; on expiry the kernel records an error code
+// in the caller-supplied error word and leaves its loops.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+namespace ssk {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Error codes written into the error word (first one wins).
+constexpr int32_t kErrWaitFull = 1;
+constexpr int32_t kErrWaitEmpty = 2;
+constexpr int32_t kErrWaitReady = 3;
+// Bounded mbarrier wait: try_wait suspends up to a hardware time limit per
+// call; 1<<22 calls is far beyond any legitimate wait (microseconds).
+constexpr uint32_t kMaxWaitIters = 1u << 22;
+
+struct KParams {
+  int batch, dim, seqlen, dstate, ngroups, dpg, tiles_per_group, nchunks;
+  int has_z, has_D, has_bias, softplus, want_last;
+  int out_vec;  // out rows 16-byte aligned (base and strides): vector stores allowed
+  const void *u, *delta, *z, *B, *C;
+  const float *A, *D, *bias;
+  void *out;
+  float *last;
+  long long su[3], sd[3], sz[3], so[3], sB[4], sC[4], sA[2], sl[3];
+  int32_t *err;
+};
+
+// ----------------------------------------------------------------------------
+// PTX helpers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+               ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait; returns false (and records `code`) if the phase never completed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err, int32_t code) {
+  for (uint32_t i = 0; i < kMaxWaitIters; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  atomicCAS(err, 0, code);
+  return false;
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Packed fp32 pair (one 64-bit register pair): .x = lo, .y = hi.
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 pk(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 upk(f2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// softplus(v) = max(v, 0) + log1p(e), e = exp(-|v|) in (0, 1]. For e < 1/16
+// log1p is its Taylor series to e^6 (relative truncation error < 1e-8); above,
+// log2(1 + e) ln2 with 1 + e in [1.0625, 2].
+__device__ __forceinline__ float softplus_f(float v) {
+  float e = ex2(-fabsf(v) * kLog2e);
+  float series = e * fmaf(e, fmaf(e, fmaf(e, fmaf(e, fmaf(e, -1.f / 6.f, 0.2f), -0.25f), 1.f / 3.f), -0.5f), 1.f);
+  float logp = lg2(1.f + e) * kLn2;
+  return fmaxf(v, 0.f) + (e < 0.0625f ? series : logp);
+}
+// silu(z) = z / (1 + e^-z)
+__device__ __forceinline__ float silu_f(float z) {
+  return z * rcp(1.f + ex2(-z * kLog2e));
+}
+
+// 16-bit I/O: outputs are rounded to 8 or 11 significant bits, so dt and the
+// gate are evaluated with single MUFU approximations (relative error ~1e-4,
+// far inside the 16-bit tolerance): softplus(v) = log2(1 + 2^(v log2e)) ln2
+// (v itself above 15, where the two agree in fp32), and
+// silu(z) = z (1/2 + tanh(z/2)/2).
+__device__ __forceinline__ float softplus_fast(float v) {
+  return v > 15.f ? v : lg2(1.f + ex2(v * kLog2e)) * kLn2;
+}
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float silu_fast(float z) {
+  const float hz = 0.5f * z;
+  return fmaf(hz, tanh_approx(hz), hz);
+}
+template <typename T> __device__ __forceinline__ float softplus_t(float v) {
+  if constexpr (sizeof(T) == 4) return softplus_f(v); else return softplus_fast(v);
+}
+template <typename T> __device__ __forceinline__ float silu_t(float z) {
+  if constexpr (sizeof(T) == 4) return silu_f(z); else return silu_fast(z);
+}
+
+// Two floats from one 32-bit word holding two 16-bit values (lo, hi).
+template <typename T> __device__ __forceinline__ float2 unpack2(uint32_t w);
+template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
+  __half2 h;
+  memcpy(&h, &w, 4);
+  return __half22float2(h);
+}
+template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  uint32_t w;
+  memcpy(&w, &h, 4);
+  return w;
+}
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  uint32_t w;
+  memcpy(&w, &h, 4);
+  return w;
+}
+
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// Byte offset of (row, byte-in-row) inside a tile of 128-byte rows written by
+// TMA with 128-byte swizzle: the 16-byte chunk index is XORed with row % 8.
+__device__ __forceinline__ int swz(int row, int byte) {
+  return row * 128 + ((((byte >> 4) ^ row) & 7) << 4) + (byte & 15);
+}
+
+// N consecutive elements (row, col .. col+N-1) of a 128B-swizzled tile of T,
+// widened to fp32. Pieces of up to 16 bytes each lie inside one 16-byte chunk
+// (col * sizeof(T) is a multiple of the piece size), so each is one vector LDS.
+template <typename T, int N>
+__device__ __forceinline__ void lds_row(const unsigned char *tile, int row, int col, float (&v)[N]) {
+  constexpr int BYTES = N * (int)sizeof(T);
+  constexpr int PB = BYTES < 16 ? BYTES : 16;
+  constexpr int NW = PB / 4;
+  constexpr int PE = PB / (int)sizeof(T);
+  static_assert(PB >= 4 && BYTES % PB == 0, "row piece must be whole 32-bit words");
+#pragma unroll
+  for (int q = 0; q < N / PE; ++q) {
+    const unsigned char *ptr = tile + swz(row, (col + q * PE) * (int)sizeof(T));
+    uint32_t w[NW];
+    if constexpr (NW == 4) {
+      const uint4 r = *reinterpret_cast<const uint4 *>(ptr);
+      w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+    } else if constexpr (NW == 2) {
+      const uint2 r = *reinterpret_cast<const uint2 *>(ptr);
+      w[0] = r.x; w[1] = r.y;
+    } else {
+      w[0] = *reinterpret_cast<const uint32_t *>(ptr);
+    }
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      if constexpr (sizeof(T) == 4) {
+        v[q * PE + i] = __uint_as_float(w[i]);
+      } else {
+        const float2 f = unpack2<T>(w[i]);
+        v[q * PE + 2 * i] = f.x;
+        v[q * PE + 2 * i + 1] = f.y;
+      }
+    }
+  }
+}
+
+// Store N consecutive floats as T at dst: 16-byte (or smaller) vectors when
+// `vec` (dst aligned to the piece size) and all N are in range, else scalars
+// for the first `valid` elements.
+template <typename T, int N>
+__device__ __forceinline__ void stg_row(T *dst, const float (&v)[N], bool vec, int valid) {
+  constexpr int BYTES = N * (int)sizeof(T);
+  constexpr int PB = BYTES < 16 ? BYTES : 16;
+  constexpr int NW = PB / 4;
+  constexpr int PE = PB / (int)sizeof(T);
+  if (vec && valid >= N) {
+#pragma unroll
+    for (int q = 0; q < N / PE; ++q) {
+      uint32_t w[NW];
+#pragma unroll
+      for (int i = 0; i < NW; ++i) {
+        if constexpr (sizeof(T) == 4) w[i] = __float_as_uint(v[q * PE + i]);
+        else w[i] = pack2<T>(v[q * PE + 2 * i], v[q * PE + 2 * i + 1]);
+      }
+      T *ptr = dst + q * PE;
+      if constexpr (NW == 4) *reinterpret_cast<uint4 *>(ptr) = make_uint4(w[0], w[1], w[2], w[3]);
+      else if constexpr (NW == 2) *reinterpret_cast<uint2 *>(ptr) = make_uint2(w[0], w[1]);
+      else *reinterpret_cast<uint32_t *>(ptr) = w[0];
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < N; ++k)
+      if (k < valid) dst[k] = from_f<T>(v[k]);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Configuration
+// ----------------------------------------------------------------------------
+template <typename T, int NP, int K, bool FIXED, bool BCF32>
+struct Cfg {
+  using BCT = typename std::conditional<BCF32, float, T>::type;  // stored B/C type (variable B/C)
+  static constexpr int TN = NP / K;              // lanes per channel
+  static constexpr int WARPS = 4;                // compute warps
+  static constexpr int THREADS = 32 * (WARPS + 1);
+  static constexpr int CPW = 32 / TN;            // channels per warp
+  static constexpr int CH = CPW * WARPS;         // channels per CTA
+  static constexpr int L = 128 / (int)sizeof(T); // steps per chunk (one 128-byte row)
+  static constexpr int S = 16;                   // steps per sub-chunk
+  static constexpr int SPT = S / TN;             // per-element steps per lane per sub-chunk
+  static constexpr int STAGES = 2;
+  static constexpr int YPAD = S + 4;             // padded row of the partial-y buffer
+  static_assert(NP % K == 0 && TN >= 1 && TN <= 16 && S % TN == 0, "bad state split");
+  static_assert(K % 4 == 0, "K must be a multiple of 4 (16-byte B/C loads)");
+  // shared memory map (bytes); tiles are 1024-aligned for the 128B swizzle
+  static constexpr int TILE = CH * 128;                    // u / delta / z tile
+  static constexpr int BC_ROW = L * (int)sizeof(BCT);       // bytes of one raw B/C row
+  static constexpr int BCMAX = (NP * BC_ROW + 1023) / 1024 * 1024;  // raw B or C tile, 1024-aligned
+  static constexpr int OFF_U = 0;
+  static constexpr int OFF_DL = OFF_U + STAGES * TILE;
+  static constexpr int OFF_Z = OFF_DL + STAGES * TILE;
+  static constexpr int OFF_BR = OFF_Z + STAGES * TILE;
+  static constexpr int OFF_CR = OFF_BR + (FIXED ? 0 : STAGES * BCMAX);
+  static constexpr int OFF_B32 = OFF_CR + (FIXED ? 0 : STAGES * BCMAX);
+  static constexpr int OFF_C32 = OFF_B32 + (FIXED ? 0 : STAGES * L * NP * 4);
+  static constexpr int OFF_P = OFF_C32 + (FIXED ? 0 : STAGES * L * NP * 4);
+  static constexpr int P_WARP = S * CPW * 16;
+  static constexpr int OFF_Y = OFF_P + WARPS * P_WARP;
+  static constexpr int Y_WARP = CPW * TN * YPAD * 4;
+  static constexpr int OFF_BAR = OFF_Y + WARPS * Y_WARP;
+  static constexpr int SMEM = OFF_BAR + 3 * STAGES * 8;
+  static constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024
+  // CTAs per SM the shared memory allows (228 KB per SM, 1 KB reserved per CTA);
+  // passed to __launch_bounds__ so the register budget matches that occupancy.
+  static constexpr int MINB_RAW = 233472 / (SMEM_ALLOC + 1024);
+  static constexpr int MINB = MINB_RAW < 1 ? 1 : (MINB_RAW > 4 ? 4 : MINB_RAW);
+};
+
+// ----------------------------------------------------------------------------
+// The kernel
+// ----------------------------------------------------------------------------
+template <typename T, int NP, int K, bool FIXED, bool BCF32, bool USE_TMA>
+__global__ void __launch_bounds__(Cfg<T, NP, K, FIXED, BCF32>::THREADS, Cfg<T, NP, K, FIXED, BCF32>::MINB)
+ss_fwd_kernel(const __grid_constant__ KParams p,
+              const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
+              const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
+              const __grid_constant__ CUtensorMap tm_C) {
+  using CF = Cfg<T, NP, K, FIXED, BCF32>;
+  using BCT = typename CF::BCT;
+  constexpr int TN = CF::TN, CPW = CF::CPW, CH = CF::CH, L = CF::L, S = CF::S, SPT = CF::SPT;
+  constexpr int STAGES = CF::STAGES, WARPS = CF::WARPS;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-align the base by an offset from the __shared__ array itself, so the
+  // compiler keeps every derived access in the shared state space (LDS/STS).
+  unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t *bar_full = reinterpret_cast<uint64_t *>(smem + CF::OFF_BAR);
+  uint64_t *bar_ready = bar_full + STAGES;
+  uint64_t *bar_empty = bar_ready + STAGES;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x / p.tiles_per_group;
+  const int tile = blockIdx.x - g * p.tiles_per_group;
+  const int b = blockIdx.y;
+  const int d0 = g * p.dpg + tile * CH;  // first channel of the tile
+  const int nchunks = p.nchunks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_ready[s], 1);
+      mbar_init(&bar_empty[s], WARPS);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // ==========================================================================
+  // Producer warp
+  // ==========================================================================
+  if (warp == WARPS) {
+    constexpr int bcs = (int)sizeof(BCT);
+    constexpr int bc_row = CF::BC_ROW;
+    constexpr bool bc_swz = (bc_row == 128);
+    const int nrow_bc = p.dstate;
+    // issue chunk ci into stage ci % STAGES
+    auto issue = [&](int ci) -> void {
+      const int s = ci % STAGES;
+      const int t0 = ci * L;
+      unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
+      unsigned char *sd = smem + CF::OFF_DL + s * CF::TILE;
+      unsigned char *sz = smem + CF::OFF_Z + s * CF::TILE;
+      unsigned char *sbr = smem + CF::OFF_BR + s * CF::BCMAX;
+      unsigned char *scr = smem + CF::OFF_CR + s * CF::BCMAX;
+      if constexpr (USE_TMA) {
+        if (lane == 0) {
+          uint32_t bytes = (2 + (p.has_z ? 1 : 0)) * CF::TILE;
+          if (!FIXED) bytes += 2 * nrow_bc * bc_row;
+          mbar_arrive_expect_tx(&bar_full[s], bytes);
+          tma_load_3d(su, &tm_u, &bar_full[s], t0, d0, b);
+          tma_load_3d(sd, &tm_dl, &bar_full[s], t0, d0, b);
+          if (p.has_z) tma_load_3d(sz, &tm_z, &bar_full[s], t0, d0, b);
+          if (!FIXED) {
+            tma_load_4d(sbr, &tm_B, &bar_full[s], t0, 0, g, b);
+            tma_load_4d(scr, &tm_C, &bar_full[s], t0, 0, g, b);
+          }
+        }
+      } else {
+        // Generic path: plain loads into the same (swizzled) layouts.
+        const T *gu = static_cast<const T *>(p.u);
+        const T *gd = static_cast<const T *>(p.delta);
+        const T *gz = static_cast<const T *>(p.z);
+        for (int i = lane; i < CH * L; i += 32) {
+          const int r = i / L, t = i - r * L;
+          const int d = d0 + r, tt = t0 + t;
+          const bool ok = (d < p.dim) && (tt < p.seqlen);
+          const int off = swz(r, t * (int)sizeof(T));
+          T zero = from_f<T>(0.f);
+          *reinterpret_cast<T *>(su + off) = ok ? gu[b * p.su[0] + (long long)d * p.su[1] + tt] : zero;
+          *reinterpret_cast<T *>(sd + off) = ok ? gd[b * p.sd[0] + (long long)d * p.sd[1] + tt] : zero;
+          if (p.has_z)
+            *reinterpret_cast<T *>(sz + off) = ok ? gz[b * p.sz[0] + (long long)d * p.sz[1] + tt] : zero;
+        }
+        if (!FIXED) {
+          for (int i = lane; i < nrow_bc * L; i += 32) {
+            const int n = i / L, t = i - n * L;
+            const int tt = t0 + t;
+            const bool ok = tt < p.seqlen;
+            const int off = bc_swz ? swz(n, t * bcs) : n * bc_row + t * bcs;
+            const long long gb = b * p.sB[0] + g * p.sB[1] + n * p.sB[2] + tt;
+            const long long gc = b * p.sC[0] + g * p.sC[1] + n * p.sC[2] + tt;
+            *reinterpret_cast<BCT *>(sbr + off) = ok ? static_cast<const BCT *>(p.B)[gb] : from_f<BCT>(0.f);
+            *reinterpret_cast<BCT *>(scr + off) = ok ? static_cast<const BCT *>(p.C)[gc] : from_f<BCT>(0.f);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_full[s]);
+      }
+    };
+    // convert chunk ci's raw B/C (stage ci % STAGES) into fp32 [t][NP]
+    auto convert = [&](int ci) -> void {
+      const int s = ci % STAGES;
+      const unsigned char *sbr = smem + CF::OFF_BR + s * CF::BCMAX;
+      const unsigned char *scr = smem + CF::OFF_CR + s * CF::BCMAX;
+      float *b32 = reinterpret_cast<float *>(smem + CF::OFF_B32) + s * L * NP;
+      float *c32 = reinterpret_cast<float *>(smem + CF::OFF_C32) + s * L * NP;
+      for (int i = lane; i < NP * L; i += 32) {
+        const int n = i % NP, t = i / NP;
+        float vb = 0.f, vc = 0.f;
+        if (n < nrow_bc) {
+          const int off = bc_swz ? swz(n, t * bcs) : n * bc_row + t * bcs;
+          vb = to_f<BCT>(*reinterpret_cast<const BCT *>(sbr + off));
+          vc = to_f<BCT>(*reinterpret_cast<const BCT *>(scr + off));
+        }
+        b32[t * NP + n] = vb;
+        c32[t * NP + n] = vc;
+      }
+    };
+
+    bool ok = true;
+    int issued = 0;
+    for (; issued < STAGES - 1 && issued < nchunks; ++issued) issue(issued);
+    for (int ci = 0; ci < nchunks && ok; ++ci) {
+      const int s = ci % STAGES;
+      const uint32_t ph = (ci / STAGES) & 1;
+      if (!FIXED) {
+        ok = mbar_wait(&bar_full[s], ph, p.err, kErrWaitFull);
+        if (!ok) break;
+        convert(ci);
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive(&bar_ready[s]);
+      // next chunk goes into the stage released by chunk ci + 1 - STAGES
+      if (issued < nchunks) {
+        const int prev = issued - STAGES;
+        if (prev >= 0) {
+          ok = mbar_wait(&bar_empty[prev % STAGES], (prev / STAGES) & 1, p.err, kErrWaitEmpty);
+          if (!ok) break;
+        }
+        issue(issued);
+        ++issued;
+      }
+    }
+    if (!ok) {
+      // give copies already in flight a bounded chance to land before exiting
+      for (int ci = 0; ci < issued; ++ci)
+        (void)mbar_try_wait(&bar_full[ci % STAGES], (ci / STAGES) & 1);
+    }
+    return;
+  }
+
+  // ==========================================================================
+  // Compute warps
+  // ==========================================================================
+  const int cl = lane / TN;          // channel within warp
+  const int j = lane - cl * TN;      // state group within channel
+  const int c = warp * CPW + cl;     // channel within CTA
+  const int dloc = tile * CH + c;    // channel within group
+  const bool ch_ok = (dloc < p.dpg);
+  const int d = ch_ok ? d0 + c : d0;  // clamp for parameter loads
+  const int n0 = j * K;
+
+  float a2[K];
+  f2 cb2[K / 2];  // fixed B/C: C*B per state pair
+  float bfix[K];  // fixed B/C: B per state (for last_state)
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const int n = n0 + k;
+    a2[k] = (n < p.dstate) ? p.A[(long long)d * p.sA[0] + n] * kLog2e : 0.f;
+    if constexpr (FIXED) {
+      float bv = 0.f, cv = 0.f;
+      if (n < p.dstate) {
+        bv = static_cast<const float *>(p.B)[(long long)d * p.sB[0] + n];
+        cv = static_cast<const float *>(p.C)[(long long)d * p.sC[0] + n];
+      }
+      bfix[k] = bv;
+      if (k & 1) cb2[k / 2] = pk(upk(cb2[k / 2]).x, cv * bv);
+      else cb2[k / 2] = pk(cv * bv, 0.f);
+    }
+  }
+  f2 a2p[K / 2];
+#pragma unroll
+  for (int k = 0; k < K / 2; ++k) a2p[k] = pk(a2[2 * k], a2[2 * k + 1]);
+  const float Dd = p.has_D ? p.D[d] : 0.f;
+  const float bias = p.has_bias ? p.bias[d] : 0.f;
+  const int softplus = p.softplus;
+  const int has_z = p.has_z;
+
+  f2 x2[K / 2];
+#pragma unroll
+  for (int k = 0; k < K / 2; ++k) x2[k] = pk(0.f, 0.f);
+
+  float4 *sP = reinterpret_cast<float4 *>(smem + CF::OFF_P + warp * CF::P_WARP);  // [S][CPW]
+  float *sY = reinterpret_cast<float *>(smem + CF::OFF_Y + warp * CF::Y_WARP);    // [CPW][TN][YPAD]
+  T *gout = static_cast<T *>(p.out);
+  const long long orow = (long long)b * p.so[0] + (long long)d * p.so[1];
+  const bool out_vec = p.out_vec != 0;
+  const int seqlen = p.seqlen;
+
+  bool ok = true;
+  for (int ci = 0; ci < nchunks; ++ci) {
+    const int s = ci % STAGES;
+    const uint32_t ph = (ci / STAGES) & 1;
+    if (!mbar_wait(&bar_ready[s], ph, p.err, kErrWaitReady)) { ok = false; break; }
+    if (!mbar_wait(&bar_full[s], ph, p.err, kErrWaitFull)) { ok = false; break; }
+    const unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
+    const unsigned char *sd = smem + CF::OFF_DL + s * CF::TILE;
+    const unsigned char *sz = smem + CF::OFF_Z + s * CF::TILE;
+    const float *b32 = reinterpret_cast<const float *>(smem + CF::OFF_B32) + s * L * NP;
+    const float *c32 = reinterpret_cast<const float *>(smem + CF::OFF_C32) + s * L * NP;
+
+#pragma unroll 1
+    for (int sub = 0; sub < L / S; ++sub) {
+      const int tb = ci * L + sub * S;  // first step of the sub-chunk
+      const int col0 = sub * S + j * SPT;  // my per-element steps: col0 .. col0+SPT-1
+      // ---- per-element prep: (dt, dt, w, w) for my SPT steps ----
+      float uv[SPT], dv[SPT];
+      lds_row<T, SPT>(su, c, col0, uv);
+      lds_row<T, SPT>(sd, c, col0, dv);
+#pragma unroll
+      for (int k = 0; k < SPT; ++k) {
+        const float v = dv[k] + bias;
+        float dt = softplus ? softplus_t<T>(v) : v;
+        float w = dt * uv[k];
+        if (tb + j * SPT + k >= seqlen) { dt = 0.f; w = 0.f; }  // padded steps leave x unchanged
+        sP[(j * SPT + k) * CPW + cl] = make_float4(dt, dt, w, w);
+      }
+      __syncwarp();
+      // ---- recurrence over the S steps ----
+      float yv[4];
+#pragma unroll
+      for (int tl = 0; tl < S; ++tl) {
+        const float4 pw = sP[tl * CPW + cl];
+        const f2 dt2 = pk(pw.x, pw.y);
+        const f2 w2 = pk(pw.z, pw.w);
+        f2 y2 = pk(0.f, 0.f);
+        if constexpr (FIXED) {
+#pragma unroll
+          for (int k = 0; k < K / 2; ++k) {
+            const float2 e = upk(mul2(dt2, a2p[k]));
+            const f2 a = pk(ex2(e.x), ex2(e.y));
+            x2[k] = fma2(a, x2[k], w2);
+            y2 = fma2(cb2[k], x2[k], y2);
+          }
+        } else {
+          const int t = sub * S + tl;
+#pragma unroll
+          for (int k = 0; k < K / 2; k += 2) {
+            // B, C for states n0+2k .. n0+2k+3 (one 16-byte load each)
+            const float4 bq = *reinterpret_cast<const float4 *>(b32 + t * NP + n0 + 2 * k);
+            const float4 cq = *reinterpret_cast<const float4 *>(c32 + t * NP + n0 + 2 * k);
+            {
+              const float2 e = upk(mul2(dt2, a2p[k]));
+              const f2 a = pk(ex2(e.x), ex2(e.y));
+              x2[k] = fma2(a, x2[k], mul2(w2, pk(bq.x, bq.y)));
+              y2 = fma2(pk(cq.x, cq.y), x2[k], y2);
+            }
+            {
+              const float2 e = upk(mul2(dt2, a2p[k + 1]));
+              const f2 a = pk(ex2(e.x), ex2(e.y));
+              x2[k + 1] = fma2(a, x2[k + 1], mul2(w2, pk(bq.z, bq.w)));
+              y2 = fma2(pk(cq.z, cq.w), x2[k + 1], y2);
+            }
+          }
+        }
+        const float2 yy = upk(y2);
+        yv[tl & 3] = yy.x + yy.y;
+        if ((tl & 3) == 3)
+          *reinterpret_cast<float4 *>(sY + (cl * TN + j) * CF::YPAD + (tl - 3)) =
+              make_float4(yv[0], yv[1], yv[2], yv[3]);
+      }
+      __syncwarp();
+      // ---- per-element epilogue for my SPT steps ----
+      float y[SPT];
+#pragma unroll
+      for (int k = 0; k < SPT; ++k) y[k] = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < TN; ++jj) {
+        const float *row = sY + (cl * TN + jj) * CF::YPAD + j * SPT;
+        if constexpr (SPT % 4 == 0) {
+#pragma unroll
+          for (int q = 0; q < SPT / 4; ++q) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(row + 4 * q);
+            y[4 * q] += v4.x; y[4 * q + 1] += v4.y; y[4 * q + 2] += v4.z; y[4 * q + 3] += v4.w;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < SPT / 2; ++q) {
+            const float2 v2 = *reinterpret_cast<const float2 *>(row + 2 * q);
+            y[2 * q] += v2.x; y[2 * q + 1] += v2.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < SPT; ++k) y[k] = fmaf(Dd, uv[k], y[k]);
+      if (has_z) {
+        float zv[SPT];
+        lds_row<T, SPT>(sz, c, col0, zv);
+#pragma unroll
+        for (int k = 0; k < SPT; ++k) y[k] *= silu_t<T>(zv[k]);
+      }
+      if (ch_ok) {
+        const int t0 = tb + j * SPT;
+        if (t0 < seqlen) stg_row<T, SPT>(gout + orow + t0, y, out_vec, seqlen - t0);
+      }
+      __syncwarp();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar_empty[s]);
+  }
+  (void)ok;
+
+  if (p.want_last && ch_ok) {
+    float *lr = p.last + (long long)b * p.sl[0] + (long long)d * p.sl[1];
+#pragma unroll
+    for (int k = 0; k < K / 2; ++k) {
+      float2 xv = upk(x2[k]);
+      if constexpr (FIXED) { xv.x *= bfix[2 * k]; xv.y *= bfix[2 * k + 1]; }
+      const int n = n0 + 2 * k;
+      if (n < p.dstate) lr[n * p.sl[2]] = xv.x;
+      if (n + 1 < p.dstate) lr[(n + 1) * p.sl[2]] = xv.y;
+    }
+  }
+}
+
+}  // namespace ssk

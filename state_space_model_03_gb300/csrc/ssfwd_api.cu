@@ -1,0 +1,422 @@
+// C ABI of libssfwd.so: validation, TMA descriptors, dispatch and launch for
+// the selective-scan forward (declarations and contract in include/ssfwd.h).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "ss_dispatch.h"
+#include "ss_fwd_kernel.cuh"
+#include "ssfwd.h"
+
+namespace {
+
+// Device error word written by kernels that give up on a bounded wait. Host
+// code obtains its device address once per device (cudaGetSymbolAddress).
+__device__ int32_t g_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int32_t *g_err_ptr[kMaxDevices] = {};
+bool g_attr_done[kMaxDevices][3][5][2][2][2] = {};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode() {
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+int elem_size(int dt) { return dt == SS_F32 ? 4 : 2; }
+
+bool fault_injected(const char *what) {
+  // Host-side fault injection for tests: SSFWD_FAULT=<what> makes the named
+  // step report a CUDA failure before anything is enqueued.
+  const char *f = std::getenv("SSFWD_FAULT");
+  return f && std::strcmp(f, what) == 0;
+}
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi) in bytes; empty if lo == hi
+};
+
+Range span(const void *ptr, int esize, const int64_t *sizes, const int64_t *strides, int nd) {
+  if (!ptr) return {0, 0};
+  int64_t last = 0;
+  for (int i = 0; i < nd; ++i) {
+    if (sizes[i] == 0) return {0, 0};
+    last += (sizes[i] - 1) * strides[i];
+  }
+  uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
+  return {lo, lo + static_cast<uintptr_t>((last + 1) * esize)};
+}
+
+bool overlap(Range a, Range b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned(const void *p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int validate(const ss_fwd_params *p) {
+  if (!p) return SS_ERR_NULL;
+  if (p->abi_version != SS_ABI_VERSION) return SS_ERR_VERSION;
+  if (p->in_dtype < SS_F32 || p->in_dtype > SS_BF16) return SS_ERR_DTYPE;
+  if (p->bc_dtype < SS_F32 || p->bc_dtype > SS_BF16) return SS_ERR_DTYPE;
+  if (p->bc_mode != SS_BC_FIXED && p->bc_mode != SS_BC_VARIABLE) return SS_ERR_SHAPE;
+  const bool fixed = p->bc_mode == SS_BC_FIXED;
+  if (fixed && p->bc_dtype != SS_F32) return SS_ERR_DTYPE;
+  if (!fixed && p->bc_dtype != p->in_dtype && p->bc_dtype != SS_F32) return SS_ERR_DTYPE;
+  if (p->batch < 0 || p->dim < 0 || p->seqlen < 0) return SS_ERR_SHAPE;
+  if (p->dstate < 1) return SS_ERR_SHAPE;
+  if (p->dstate > 64) return SS_ERR_UNSUPPORTED;
+  if (!fixed && (p->ngroups < 1 || (p->dim > 0 && p->dim % p->ngroups != 0))) return SS_ERR_SHAPE;
+  if (p->batch > 65535 || p->dim > (1 << 30) || p->seqlen > (int64_t(1) << 31) - 1024) return SS_ERR_UNSUPPORTED;
+  if (p->batch * p->dim == 0) return SS_OK;
+  if (p->last_state && p->last_state_stride[2] != 1) return SS_ERR_STRIDE;
+  for (int i = 0; i < 3; ++i)
+    if (p->last_state && p->last_state_stride[i] < 0) return SS_ERR_STRIDE;
+  if (p->seqlen == 0) return SS_OK;
+  if (!p->u || !p->delta || !p->A || !p->B || !p->C || !p->out) return SS_ERR_NULL;
+  const int64_t *st3[4] = {p->u_stride, p->delta_stride, p->z ? p->z_stride : p->u_stride, p->out_stride};
+  for (auto s : st3) {
+    if (s[2] != 1) return SS_ERR_STRIDE;
+    if (s[0] < 0 || s[1] < 0) return SS_ERR_STRIDE;
+  }
+  if (p->A_stride[1] != 1 || p->A_stride[0] < 0) return SS_ERR_STRIDE;
+  if (fixed) {
+    if (p->B_stride[1] != 1 || p->C_stride[1] != 1 || p->B_stride[0] < 0 || p->C_stride[0] < 0) return SS_ERR_STRIDE;
+  } else {
+    for (int i = 0; i < 4; ++i)
+      if (p->B_stride[i] < 0 || p->C_stride[i] < 0) return SS_ERR_STRIDE;
+    if (p->B_stride[3] != 1 || p->C_stride[3] != 1) return SS_ERR_STRIDE;
+  }
+  const int es = elem_size(p->in_dtype), bs = elem_size(p->bc_dtype);
+  if (!aligned(p->u, es) || !aligned(p->delta, es) || !aligned(p->out, es) || (p->z && !aligned(p->z, es)))
+    return SS_ERR_ALIGN;
+  if (!aligned(p->B, bs) || !aligned(p->C, bs) || !aligned(p->A, 4)) return SS_ERR_ALIGN;
+  if ((p->D && !aligned(p->D, 4)) || (p->delta_bias && !aligned(p->delta_bias, 4)) ||
+      (p->last_state && !aligned(p->last_state, 4)))
+    return SS_ERR_ALIGN;
+  // outputs must not overlap inputs or each other
+  const int64_t sz3[3] = {p->batch, p->dim, p->seqlen};
+  Range out = span(p->out, es, sz3, p->out_stride, 3);
+  const int64_t szl[3] = {p->batch, p->dim, p->dstate};
+  Range last = p->last_state ? span(p->last_state, 4, szl, p->last_state_stride, 3) : Range{0, 0};
+  Range ins[8];
+  int ni = 0;
+  ins[ni++] = span(p->u, es, sz3, p->u_stride, 3);
+  ins[ni++] = span(p->delta, es, sz3, p->delta_stride, 3);
+  if (p->z) ins[ni++] = span(p->z, es, sz3, p->z_stride, 3);
+  const int64_t sza[2] = {p->dim, p->dstate};
+  ins[ni++] = span(p->A, 4, sza, p->A_stride, 2);
+  if (fixed) {
+    ins[ni++] = span(p->B, 4, sza, p->B_stride, 2);
+    ins[ni++] = span(p->C, 4, sza, p->C_stride, 2);
+  } else {
+    const int64_t szb[4] = {p->batch, p->ngroups, p->dstate, p->seqlen};
+    ins[ni++] = span(p->B, bs, szb, p->B_stride, 4);
+    ins[ni++] = span(p->C, bs, szb, p->C_stride, 4);
+  }
+  const int64_t one[1] = {p->dim}, unit[1] = {1};
+  if (p->D) ins[ni++] = span(p->D, 4, one, unit, 1);
+  if (p->delta_bias) ins[ni++] = span(p->delta_bias, 4, one, unit, 1);
+  for (int i = 0; i < ni; ++i)
+    if (overlap(out, ins[i]) || overlap(last, ins[i])) return SS_ERR_ALIAS;
+  if (overlap(out, last)) return SS_ERR_ALIAS;
+  return SS_OK;
+}
+
+int padded_states(int64_t n) {
+  if (n <= 4) return 4;
+  if (n <= 8) return 8;
+  if (n <= 16) return 16;
+  if (n <= 32) return 32;
+  return 64;
+}
+
+int np_index(int np) { return np == 4 ? 0 : np == 8 ? 1 : np == 16 ? 2 : np == 32 ? 3 : 4; }
+
+ssk::KernelInfo lookup(int dt, int np, bool fixed, bool bc_f32, bool tma) {
+  switch (dt) {
+    case SS_F32: return ssk::lookup_f32(np, fixed, bc_f32, tma);
+    case SS_F16: return ssk::lookup_f16(np, fixed, bc_f32, tma);
+    default: return ssk::lookup_bf16(np, fixed, bc_f32, tma);
+  }
+}
+
+// Stride as used by a TMA descriptor: a dimension of extent 1 may carry any
+// stride, so give it a legal one.
+uint64_t tma_stride(int64_t extent, int64_t stride_elems, int esize, uint64_t fallback) {
+  if (extent <= 1) return fallback;
+  return static_cast<uint64_t>(stride_elems) * esize;
+}
+
+bool tma_ok_stride(uint64_t s) { return s % 16 == 0 && s > 0 && s < (uint64_t(1) << 40); }
+
+// 3-D (seqlen, dim, batch) descriptor for u / delta / z: box {L, CH, 1}.
+bool make_map3(CUtensorMap *m, const void *base, int es, const ss_fwd_params *p, const int64_t *st, int L, int CH) {
+  if (!aligned(base, 16)) return false;
+  const uint64_t row = static_cast<uint64_t>(p->seqlen) * es;
+  const uint64_t s1 = tma_stride(p->dim, st[1], es, (row + 15) / 16 * 16);
+  const uint64_t s2 = tma_stride(p->batch, st[0], es, s1 * static_cast<uint64_t>(p->dim));
+  if (!tma_ok_stride(s1) || !tma_ok_stride(s2)) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->seqlen), static_cast<cuuint64_t>(p->dim),
+                        static_cast<cuuint64_t>(p->batch)};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(L), static_cast<cuuint32_t>(CH), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+                        const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 4-D (seqlen, dstate, groups, batch) descriptor for variable B / C: box {L, dstate, 1, 1}.
+bool make_map4(CUtensorMap *m, const void *base, int bs, const ss_fwd_params *p, const int64_t *st, int L) {
+  if (!aligned(base, 16)) return false;
+  const uint64_t row = static_cast<uint64_t>(p->seqlen) * bs;
+  const uint64_t s1 = tma_stride(p->dstate, st[2], bs, (row + 15) / 16 * 16);
+  const uint64_t s2 = tma_stride(p->ngroups, st[1], bs, s1 * static_cast<uint64_t>(p->dstate));
+  const uint64_t s3 = tma_stride(p->batch, st[0], bs, s2 * static_cast<uint64_t>(p->ngroups));
+  if (!tma_ok_stride(s1) || !tma_ok_stride(s2) || !tma_ok_stride(s3)) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(p->seqlen), static_cast<cuuint64_t>(p->dstate),
+                        static_cast<cuuint64_t>(p->ngroups), static_cast<cuuint64_t>(p->batch)};
+  cuuint64_t strides[3] = {s1, s2, s3};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(L), static_cast<cuuint32_t>(p->dstate), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const bool swz = (L * bs == 128);
+  CUresult r = g_encode(m, bs == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                        const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int32_t *error_word_ptr(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_err_ptr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int32_t *>(ptr);
+  }
+  return g_err_ptr[dev];
+}
+
+__global__ void zero_last_state(float *last, int64_t batch, int64_t dim, int64_t dstate, int64_t s0, int64_t s1,
+                                int64_t s2) {
+  const int64_t total = batch * dim * dstate;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = i % dstate, r = i / dstate, d = r % dim, b = r / dim;
+    last[b * s0 + d * s1 + n * s2] = 0.f;
+  }
+}
+
+int launch(const ss_fwd_params *p, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+  if (p->batch * p->dim == 0) return SS_OK;
+  if (p->seqlen == 0) {
+    if (!p->last_state) return SS_OK;
+    if (fault_injected("launch")) return SS_ERR_CUDA;
+    const int64_t total = p->batch * p->dim * p->dstate;
+    const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 4096));
+    zero_last_state<<<blocks, 256, 0, stream>>>(p->last_state, p->batch, p->dim, p->dstate, p->last_state_stride[0],
+                                                p->last_state_stride[1], p->last_state_stride[2]);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  }
+  int32_t *err = error_word_ptr(dev);
+  if (!err) return SS_ERR_CUDA;
+  std::call_once(g_encode_once, load_encode);
+
+  const bool fixed = p->bc_mode == SS_BC_FIXED;
+  const int np = padded_states(p->dstate);
+  const int es = elem_size(p->in_dtype), bs = elem_size(p->bc_dtype);
+  const bool bc_f32 = p->bc_dtype == SS_F32;
+  ssk::KernelInfo ki = lookup(p->in_dtype, np, fixed, bc_f32, true);
+  if (!ki.fn) return SS_ERR_UNSUPPORTED;
+
+  ssk::KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.batch = static_cast<int>(p->batch);
+  kp.dim = static_cast<int>(p->dim);
+  kp.seqlen = static_cast<int>(p->seqlen);
+  kp.dstate = static_cast<int>(p->dstate);
+  kp.ngroups = fixed ? 1 : static_cast<int>(p->ngroups);
+  kp.dpg = kp.dim / kp.ngroups;
+  kp.tiles_per_group = (kp.dpg + ki.ch - 1) / ki.ch;
+  kp.nchunks = static_cast<int>((p->seqlen + ki.L - 1) / ki.L);
+  kp.has_z = p->z != nullptr;
+  kp.has_D = p->D != nullptr;
+  kp.has_bias = p->delta_bias != nullptr;
+  kp.softplus = p->delta_softplus != 0;
+  kp.want_last = p->last_state != nullptr;
+  kp.out_vec = aligned(p->out, 16) && (p->batch <= 1 || (p->out_stride[0] * es) % 16 == 0) &&
+               (p->dim <= 1 || (p->out_stride[1] * es) % 16 == 0);
+  kp.u = p->u; kp.delta = p->delta; kp.z = p->z; kp.B = p->B; kp.C = p->C;
+  kp.A = p->A; kp.D = p->D; kp.bias = p->delta_bias;
+  kp.out = p->out; kp.last = p->last_state;
+  for (int i = 0; i < 3; ++i) {
+    kp.su[i] = p->u_stride[i]; kp.sd[i] = p->delta_stride[i]; kp.sz[i] = p->z_stride[i];
+    kp.so[i] = p->out_stride[i]; kp.sl[i] = p->last_state_stride[i];
+  }
+  for (int i = 0; i < 4; ++i) { kp.sB[i] = p->B_stride[i]; kp.sC[i] = p->C_stride[i]; }
+  kp.sA[0] = p->A_stride[0]; kp.sA[1] = p->A_stride[1];
+  kp.err = err;
+
+  // TMA when every streamed tensor has a legal descriptor; else the generic
+  // (plain-load) producer with the same compute path.
+  CUtensorMap tm[5];
+  std::memset(tm, 0, sizeof(tm));
+  bool tma = g_encode != nullptr && !std::getenv("SSFWD_NO_TMA");
+  if (tma) tma = make_map3(&tm[0], p->u, es, p, p->u_stride, ki.L, ki.ch);
+  if (tma) tma = make_map3(&tm[1], p->delta, es, p, p->delta_stride, ki.L, ki.ch);
+  if (tma && p->z) tma = make_map3(&tm[2], p->z, es, p, p->z_stride, ki.L, ki.ch);
+  if (tma && !fixed) tma = make_map4(&tm[3], p->B, bs, p, p->B_stride, ki.L);
+  if (tma && !fixed) tma = make_map4(&tm[4], p->C, bs, p, p->C_stride, ki.L);
+  if (!tma) ki = lookup(p->in_dtype, np, fixed, bc_f32, false);
+  if (!ki.fn) return SS_ERR_UNSUPPORTED;
+
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    bool &done = g_attr_done[dev][p->in_dtype][np_index(np)][fixed][bc_f32 && !fixed][tma];
+    if (!done) {
+      if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) != cudaSuccess)
+        return SS_ERR_CUDA;
+      done = true;
+    }
+  }
+  if (fault_injected("launch")) return SS_ERR_CUDA;
+  dim3 grid(static_cast<unsigned>(kp.tiles_per_group * kp.ngroups), static_cast<unsigned>(kp.batch));
+  if (std::getenv("SSFWD_DEBUG"))  // opt-in launch report on stderr
+    std::fprintf(stderr, "ssfwd: %s np=%d fixed=%d bc_f32=%d ch=%d L=%d grid=%ux%u threads=%d smem=%d encode=%d\n",
+                 tma ? "tma" : "generic", np, (int)fixed, (int)bc_f32, ki.ch, ki.L, grid.x, grid.y, ki.threads,
+                 ki.smem, g_encode != nullptr);
+  void *args[6] = {&kp, &tm[0], &tm[1], &tm[2], &tm[3], &tm[4]};
+  cudaError_t e = cudaLaunchKernel(ki.fn, grid, dim3(ki.threads), args, static_cast<size_t>(ki.smem), stream);
+  return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+// The host-staged entry point copies whole tensors, so the device buffers must
+// be laid out contiguously (a dimension of extent 1 may carry any stride).
+bool contiguous(const int64_t *sizes, const int64_t *strides, int nd) {
+  int64_t expect = 1;
+  for (int i = nd - 1; i >= 0; --i) {
+    if (sizes[i] > 1 && strides[i] != expect) return false;
+    expect *= sizes[i];
+  }
+  return true;
+}
+
+bool host_layout_ok(const ss_fwd_params *p) {
+  const int64_t sz3[3] = {p->batch, p->dim, p->seqlen};
+  if (!contiguous(sz3, p->u_stride, 3) || !contiguous(sz3, p->delta_stride, 3) || !contiguous(sz3, p->out_stride, 3))
+    return false;
+  if (p->z && !contiguous(sz3, p->z_stride, 3)) return false;
+  const int64_t sza[2] = {p->dim, p->dstate};
+  if (!contiguous(sza, p->A_stride, 2)) return false;
+  if (p->bc_mode == SS_BC_FIXED) {
+    if (!contiguous(sza, p->B_stride, 2) || !contiguous(sza, p->C_stride, 2)) return false;
+  } else {
+    const int64_t szb[4] = {p->batch, p->ngroups, p->dstate, p->seqlen};
+    if (!contiguous(szb, p->B_stride, 4) || !contiguous(szb, p->C_stride, 4)) return false;
+  }
+  const int64_t szl[3] = {p->batch, p->dim, p->dstate};
+  if (p->last_state && !contiguous(szl, p->last_state_stride, 3)) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ss_abi_version(void) { return SS_ABI_VERSION; }
+
+const char *ss_status_string(int s) {
+  switch (s) {
+    case SS_OK: return "ok";
+    case SS_ERR_NULL: return "a required pointer is NULL";
+    case SS_ERR_SHAPE: return "invalid shape (negative size, dstate < 1, or dim not divisible by ngroups)";
+    case SS_ERR_DTYPE: return "unsupported dtype or dtype combination";
+    case SS_ERR_STRIDE: return "unsupported stride (the seqlen/state stride must be 1; strides must be >= 0)";
+    case SS_ERR_ALIGN: return "pointer not aligned to its element size";
+    case SS_ERR_ALIAS: return "an output overlaps an input or the other output";
+    case SS_ERR_UNSUPPORTED: return "unsupported size (dstate > 64, batch > 65535, or too large)";
+    case SS_ERR_CUDA: return "a CUDA call failed";
+    case SS_ERR_INTERNAL: return "a device-side self-check failed";
+    case SS_ERR_VERSION: return "ABI version mismatch";
+    default: return "unknown status";
+  }
+}
+
+int ss_fwd_validate(const ss_fwd_params *p) { return validate(p); }
+
+int ss_fwd(const ss_fwd_params *p, void *stream) {
+  int st = validate(p);
+  if (st != SS_OK) return st;
+  return launch(p, static_cast<cudaStream_t>(stream));
+}
+
+int ss_fwd_host(const ss_fwd_params *p, const void *h_u, const void *h_delta, const void *h_z, const void *h_B,
+                const void *h_C, const float *h_A, const float *h_D, const float *h_delta_bias, void *h_out,
+                float *h_last_state, void *stream) {
+  int st = validate(p);
+  if (st != SS_OK) return st;
+  if (!host_layout_ok(p)) return SS_ERR_STRIDE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t es = elem_size(p->in_dtype), bs = elem_size(p->bc_dtype);
+  const size_t n3 = static_cast<size_t>(p->batch * p->dim * p->seqlen);
+  const size_t nbc = p->bc_mode == SS_BC_FIXED ? static_cast<size_t>(p->dim * p->dstate)
+                                               : static_cast<size_t>(p->batch * p->ngroups * p->dstate * p->seqlen);
+  struct Copy {
+    void *dst;
+    const void *src;
+    size_t bytes;
+  } in[8] = {{const_cast<void *>(p->u), h_u, n3 * es},
+             {const_cast<void *>(p->delta), h_delta, n3 * es},
+             {const_cast<void *>(p->z), h_z, n3 * es},
+             {const_cast<void *>(p->B), h_B, nbc * bs},
+             {const_cast<void *>(p->C), h_C, nbc * bs},
+             {const_cast<float *>(p->A), h_A, static_cast<size_t>(p->dim * p->dstate) * 4},
+             {const_cast<float *>(p->D), h_D, static_cast<size_t>(p->dim) * 4},
+             {const_cast<float *>(p->delta_bias), h_delta_bias, static_cast<size_t>(p->dim) * 4}};
+  if (fault_injected("h2d")) return SS_ERR_CUDA;
+  for (auto &c : in) {
+    if (!c.src || c.bytes == 0) continue;
+    if (!c.dst) return SS_ERR_NULL;
+    if (cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return SS_ERR_CUDA;
+  }
+  st = launch(p, s);
+  if (st != SS_OK) return st;
+  if (h_out && n3 && cudaMemcpyAsync(h_out, p->out, n3 * es, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SS_ERR_CUDA;
+  if (h_last_state && p->last_state) {
+    const size_t nl = static_cast<size_t>(p->batch * p->dim * p->dstate) * 4;
+    if (nl && cudaMemcpyAsync(h_last_state, p->last_state, nl, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return SS_ERR_CUDA;
+  }
+  return SS_OK;
+}
+
+int ss_device_error(int32_t *out_word, int clear) {
+  if (!out_word) return SS_ERR_NULL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+  int32_t *ptr = error_word_ptr(dev);
+  if (!ptr) return SS_ERR_CUDA;
+  if (cudaMemcpy(out_word, ptr, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return SS_ERR_CUDA;
+  if (clear && cudaMemset(ptr, 0, sizeof(int32_t)) != cudaSuccess) return SS_ERR_CUDA;
+  return SS_OK;
+}
+
+}  // extern "C"

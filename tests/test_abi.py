@@ -1,0 +1,157 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+include/ssfwd.h declares, and its validation returns the documented status
+for each malformed call without launching anything (ss_fwd_validate makes no
+CUDA call, and ss_fwd returns before its first CUDA call on these inputs)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from state_space_model_03_gb300 import api
+from state_space_model_03_gb300 import build as ssbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssfwd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ssbuild.build()
+    return api.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ss_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert set(names) == {"ss_abi_version", "ss_status_string", "ss_fwd_validate", "ss_fwd",
+                          "ss_fwd_host", "ss_device_error"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_abi_version_and_strings(lib):
+    assert lib.ss_abi_version() == api.SS_ABI_VERSION
+    for s in range(0, 11):
+        assert api.status_string(s) and api.status_string(s) != "unknown status"
+    assert api.status_string(99) == "unknown status"
+
+
+def _good():
+    """A valid variable-B/C bf16 problem with fake (never dereferenced) device
+    addresses, laid out contiguously and 16-byte aligned."""
+    b, d, l, n, g = 2, 64, 128, 16, 2
+    p = api.SSFwdParams()
+    p.abi_version = api.SS_ABI_VERSION
+    p.in_dtype = p.bc_dtype = api.SS_BF16
+    p.bc_mode = api.SS_BC_VARIABLE
+    p.delta_softplus = 1
+    p.batch, p.dim, p.seqlen, p.dstate, p.ngroups = b, d, l, n, g
+    base = 1 << 40
+    sz3 = b * d * l * 2
+    addrs = {}
+    cur = base
+    for k, nbytes in (("u", sz3), ("delta", sz3), ("z", sz3), ("B", b * g * n * l * 2), ("C", b * g * n * l * 2),
+                      ("A", d * n * 4), ("D", d * 4), ("delta_bias", d * 4), ("out", sz3), ("last_state", b * d * n * 4)):
+        addrs[k] = cur
+        cur += (nbytes + 255) // 256 * 256
+    for k, v in addrs.items():
+        setattr(p, k, v)
+    for k in ("u_stride", "delta_stride", "z_stride", "out_stride"):
+        getattr(p, k)[:] = [d * l, l, 1]
+    p.B_stride[:] = [g * n * l, n * l, l, 1]
+    p.C_stride[:] = [g * n * l, n * l, l, 1]
+    p.A_stride[:] = [n, 1]
+    p.last_state_stride[:] = [d * n, n, 1]
+    return p
+
+
+def _val(lib, p):
+    return lib.ss_fwd_validate(ctypes.byref(p)) if p is not None else lib.ss_fwd_validate(None)
+
+
+def test_valid_params_pass(lib):
+    assert _val(lib, _good()) == 0
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda p: setattr(p, "abi_version", 0), 10),
+    (lambda p: setattr(p, "u", None), 1),
+    (lambda p: setattr(p, "out", None), 1),
+    (lambda p: setattr(p, "B", None), 1),
+    (lambda p: setattr(p, "in_dtype", 7), 3),
+    (lambda p: setattr(p, "bc_dtype", api.SS_F16), 3),        # bf16 inputs, fp16 B/C
+    (lambda p: setattr(p, "ngroups", 3), 2),                  # 64 % 3 != 0
+    (lambda p: setattr(p, "ngroups", 0), 2),
+    (lambda p: setattr(p, "dstate", 0), 2),
+    (lambda p: setattr(p, "dstate", 65), 7),
+    (lambda p: setattr(p, "seqlen", -1), 2),
+    (lambda p: setattr(p, "batch", 70000), 7),
+    (lambda p: p.u_stride.__setitem__(2, 2), 4),
+    (lambda p: p.out_stride.__setitem__(2, 2), 4),
+    (lambda p: p.B_stride.__setitem__(3, 2), 4),
+    (lambda p: p.A_stride.__setitem__(1, 2), 4),
+    (lambda p: p.delta_stride.__setitem__(0, -5), 4),
+    (lambda p: p.last_state_stride.__setitem__(2, 3), 4),
+    (lambda p: setattr(p, "u", p.u + 1), 5),                  # bf16 needs 2-byte alignment
+    (lambda p: setattr(p, "A", p.A + 2), 5),
+    (lambda p: setattr(p, "out", p.u), 6),                    # out aliases u
+    (lambda p: setattr(p, "out", p.z + 64), 6),               # partial overlap with z
+    (lambda p: setattr(p, "last_state", p.A), 6),
+    (lambda p: setattr(p, "last_state", p.out + 128), 6),
+])
+def test_invalid_params_rejected(lib, mutate, status):
+    p = _good()
+    mutate(p)
+    assert _val(lib, p) == status
+    # ss_fwd validates first and returns the same status with nothing launched
+    assert lib.ss_fwd(ctypes.byref(p), None) == status
+
+
+def test_null_params(lib):
+    assert _val(lib, None) == 1
+    assert lib.ss_fwd(None, None) == 1
+
+
+def test_fixed_bc_rules(lib):
+    p = _good()
+    p.bc_mode = api.SS_BC_FIXED
+    p.bc_dtype = api.SS_F32
+    p.B_stride[:] = [16, 1, 0, 0]
+    p.C_stride[:] = [16, 1, 0, 0]
+    p.ngroups = 3  # ignored for fixed B/C
+    assert _val(lib, p) == 0
+    p.bc_dtype = api.SS_BF16
+    assert _val(lib, p) == 3
+    p.bc_dtype = api.SS_F32
+    p.B_stride[1] = 2
+    assert _val(lib, p) == 4
+
+
+def test_empty_problems_validate(lib):
+    p = _good()
+    p.batch = 0
+    assert _val(lib, p) == 0
+    p = _good()
+    p.seqlen = 0
+    p.u = p.delta = p.out = None  # nothing is read or written but last_state
+    assert _val(lib, p) == 0
+
+
+def test_python_wrapper_refuses_cpu_tensors():
+    import torch
+    u = torch.zeros(1, 4, 8)
+    with pytest.raises(RuntimeError):
+        api.selective_scan_fn(u, u, torch.zeros(4, 4), torch.zeros(1, 4, 8), torch.zeros(1, 4, 8))
+
+
+def test_complex_A_not_implemented():
+    import torch
+    u = torch.zeros(1, 4, 8)
+    with pytest.raises(NotImplementedError):
+        api.normalise(u, u, torch.zeros(4, 4, dtype=torch.complex64), torch.zeros(1, 4, 8), torch.zeros(1, 4, 8))
