@@ -7,18 +7,19 @@
 //   y = sum_n C_n,t x_n + D u_t; out = y silu(z_t); last_state = final x.
 //
 // Work decomposition (one CTA = one (batch, group, channel tile)):
-//   * 4 compute warps; each channel is owned by TN = NP/K adjacent lanes, each
-//     lane holding K of the channel's NP (padded) states in fp32 registers, so
-//     the recurrence runs sequentially in time with no scan overhead.
+//   * Scan warps run only the recurrence: each channel is owned by TN = NP/K
+//     adjacent lanes, each lane holding K of the channel's NP (padded) states
+//     in fp32 registers, so time runs sequentially with no scan overhead.
 //   * 1 producer warp streams 64-step (16-bit) or 32-step (fp32) chunks of u,
 //     delta, z with TMA (cp.async.bulk.tensor, 128-byte swizzle) into a
-//     2-stage mbarrier ring, and the (batch, group) B/C tile of the chunk,
-//     which it converts once per CTA into fp32 [t][n] so that every lane reads
-//     its K states of B and C with one 16-byte shared load.
-//   * Per-element work (softplus, dt*u, D skip, silu gate, rounding) is done
-//     once per element: within a 16-step sub-chunk, lane j of a channel takes
-//     steps [j*S/TN, (j+1)*S/TN), publishing (dt, dt, w, w) to shared memory
-//     before the recurrence and summing the TN partial y's after it.
+//     2-stage mbarrier ring, with the (batch, group) B/C tile of the chunk.
+//   * 2 element warps do the per-element work once per element, one 16-step
+//     sub-chunk ahead of the scan (softplus, dt*u, and the conversion of the
+//     sub-chunk's B/C to fp32 [t][n], so that a scan lane reads its K states
+//     of B and C with one 16-byte load) and one sub-chunk behind it (sum of
+//     the TN partial y's, D skip, silu gate, rounding, 16-byte stores). The
+//     three roles hand over through double-buffered shared slots guarded by
+//     mbarriers, so per-element latency overlaps the recurrence.
 //   * exp(dt A) = exp2(dt * A log2e) with A pre-scaled; state pairs use packed
 //     fp32x2 multiply/FMA (half the issue slots of scalar FFMA).
 //   * Fixed B/C (dim, dstate): B and C are per-channel constants, so the state
@@ -300,35 +301,39 @@ __device__ __forceinline__ void stg_row(T *dst, const float (&v)[N], bool vec, i
 template <typename T, int NP, int K, bool FIXED, bool BCF32>
 struct Cfg {
   using BCT = typename std::conditional<BCF32, float, T>::type;  // stored B/C type (variable B/C)
-  static constexpr int TN = NP / K;              // lanes per channel
-  static constexpr int WARPS = 4;                // compute warps
-  static constexpr int THREADS = 32 * (WARPS + 1);
-  static constexpr int CPW = 32 / TN;            // channels per warp
-  static constexpr int CH = CPW * WARPS;         // channels per CTA
+  static constexpr int TN = NP / K;              // scan lanes per channel
+  static constexpr int CH = 32;                  // channels per CTA
+  static constexpr int CPW = 32 / TN;            // channels per scan warp
+  static constexpr int WS = CH / CPW;            // scan warps (= TN)
+  static constexpr int WE = 2;                   // element warps
+  static constexpr int THREADS = 32 * (WS + WE + 1);
+  static constexpr int PRODUCER = WS + WE;       // warp index of the producer
   static constexpr int L = 128 / (int)sizeof(T); // steps per chunk (one 128-byte row)
   static constexpr int S = 16;                   // steps per sub-chunk
-  static constexpr int SPT = S / TN;             // per-element steps per lane per sub-chunk
+  static constexpr int SUBS = L / S;             // sub-chunks per chunk
+  static constexpr int EPT = 8;                  // element-warp steps per lane per sub-chunk
   static constexpr int STAGES = 2;
-  static constexpr int YPAD = S + 4;             // padded row of the partial-y buffer
-  static_assert(NP % K == 0 && TN >= 1 && TN <= 16 && S % TN == 0, "bad state split");
+  static_assert(NP % K == 0 && TN >= 1 && TN <= 8, "bad state split");
   static_assert(K % 4 == 0, "K must be a multiple of 4 (16-byte B/C loads)");
-  // shared memory map (bytes); tiles are 1024-aligned for the 128B swizzle
-  static constexpr int TILE = CH * 128;                    // u / delta / z tile
-  static constexpr int BC_ROW = L * (int)sizeof(BCT);       // bytes of one raw B/C row
-  static constexpr int BCMAX = (NP * BC_ROW + 1023) / 1024 * 1024;  // raw B or C tile, 1024-aligned
+  static_assert(CH * S == WE * 32 * EPT, "element warps cover the sub-chunk exactly");
+  // shared memory map (bytes); TMA tiles are 1024-aligned for the 128B swizzle
+  static constexpr int TILE = CH * 128;                          // u / delta / z tile
+  static constexpr int BC_ROW = L * (int)sizeof(BCT);             // bytes of one raw B/C row
+  static constexpr int BCMAX = (NP * BC_ROW + 1023) / 1024 * 1024;  // raw B or C tile
   static constexpr int OFF_U = 0;
   static constexpr int OFF_DL = OFF_U + STAGES * TILE;
   static constexpr int OFF_Z = OFF_DL + STAGES * TILE;
   static constexpr int OFF_BR = OFF_Z + STAGES * TILE;
   static constexpr int OFF_CR = OFF_BR + (FIXED ? 0 : STAGES * BCMAX);
-  static constexpr int OFF_B32 = OFF_CR + (FIXED ? 0 : STAGES * BCMAX);
-  static constexpr int OFF_C32 = OFF_B32 + (FIXED ? 0 : STAGES * L * NP * 4);
-  static constexpr int OFF_P = OFF_C32 + (FIXED ? 0 : STAGES * L * NP * 4);
-  static constexpr int P_WARP = S * CPW * 16;
-  static constexpr int OFF_Y = OFF_P + WARPS * P_WARP;
-  static constexpr int Y_WARP = CPW * TN * YPAD * 4;
-  static constexpr int OFF_BAR = OFF_Y + WARPS * Y_WARP;
-  static constexpr int SMEM = OFF_BAR + 3 * STAGES * 8;
+  static constexpr int OFF_P = OFF_CR + (FIXED ? 0 : STAGES * BCMAX);
+  static constexpr int P_SLOT = S * CH * 16;                      // (dt, dt, w, w) [S][CH]
+  static constexpr int OFF_BC = OFF_P + 2 * P_SLOT;
+  static constexpr int BC_SLOT = FIXED ? 0 : 2 * S * NP * 4;       // fp32 B then C, [S][NP] each
+  static constexpr int OFF_Y = OFF_BC + 2 * BC_SLOT;
+  static constexpr int Y_SLOT = S * CH * TN * 4;                  // partial y [S][CH*TN]
+  static constexpr int OFF_BAR = OFF_Y + 2 * Y_SLOT;
+  static constexpr int NBAR = 2 * STAGES + 8;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024
   // CTAs per SM the shared memory allows (228 KB per SM, 1 KB reserved per CTA);
   // passed to __launch_bounds__ so the register budget matches that occupancy.
@@ -347,15 +352,18 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
               const __grid_constant__ CUtensorMap tm_C) {
   using CF = Cfg<T, NP, K, FIXED, BCF32>;
   using BCT = typename CF::BCT;
-  constexpr int TN = CF::TN, CPW = CF::CPW, CH = CF::CH, L = CF::L, S = CF::S, SPT = CF::SPT;
-  constexpr int STAGES = CF::STAGES, WARPS = CF::WARPS;
+  constexpr int TN = CF::TN, CPW = CF::CPW, CH = CF::CH, L = CF::L, S = CF::S, SUBS = CF::SUBS;
+  constexpr int STAGES = CF::STAGES, WS = CF::WS, WE = CF::WE, EPT = CF::EPT;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-align the base by an offset from the __shared__ array itself, so the
   // compiler keeps every derived access in the shared state space (LDS/STS).
   unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t *bar_full = reinterpret_cast<uint64_t *>(smem + CF::OFF_BAR);
-  uint64_t *bar_ready = bar_full + STAGES;
-  uint64_t *bar_empty = bar_ready + STAGES;
+  uint64_t *bar_full = reinterpret_cast<uint64_t *>(smem + CF::OFF_BAR);  // [STAGES] TMA landed
+  uint64_t *bar_empty = bar_full + STAGES;   // [STAGES] element warps done with the stage
+  uint64_t *bar_pfull = bar_empty + STAGES;  // [2] P/BC slot written (element warps)
+  uint64_t *bar_pempty = bar_pfull + 2;      // [2] P/BC slot consumed (scan warps)
+  uint64_t *bar_yfull = bar_pempty + 2;      // [2] Y slot written (scan warps)
+  uint64_t *bar_yempty = bar_yfull + 2;      // [2] Y slot consumed (element warps)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.x / p.tiles_per_group;
@@ -363,26 +371,32 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   const int b = blockIdx.y;
   const int d0 = g * p.dpg + tile * CH;  // first channel of the tile
   const int nchunks = p.nchunks;
+  const int nsub = nchunks * SUBS;
+  const int seqlen = p.seqlen;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_ready[s], 1);
-      mbar_init(&bar_empty[s], WARPS);
+      mbar_init(&bar_empty[s], WE);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_pfull[s], WE);
+      mbar_init(&bar_pempty[s], WS);
+      mbar_init(&bar_yfull[s], WS);
+      mbar_init(&bar_yempty[s], WE);
     }
     fence_barrier_init();
   }
   __syncthreads();
 
   // ==========================================================================
-  // Producer warp
+  // Producer warp: TMA (or plain loads) of chunk ci into stage ci % STAGES
   // ==========================================================================
-  if (warp == WARPS) {
+  if (warp == CF::PRODUCER) {
     constexpr int bcs = (int)sizeof(BCT);
     constexpr int bc_row = CF::BC_ROW;
     constexpr bool bc_swz = (bc_row == 128);
     const int nrow_bc = p.dstate;
-    // issue chunk ci into stage ci % STAGES
     auto issue = [&](int ci) -> void {
       const int s = ci % STAGES;
       const int t0 = ci * L;
@@ -412,9 +426,9 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         for (int i = lane; i < CH * L; i += 32) {
           const int r = i / L, t = i - r * L;
           const int d = d0 + r, tt = t0 + t;
-          const bool ok = (d < p.dim) && (tt < p.seqlen);
+          const bool ok = (d < p.dim) && (tt < seqlen);
           const int off = swz(r, t * (int)sizeof(T));
-          T zero = from_f<T>(0.f);
+          const T zero = from_f<T>(0.f);
           *reinterpret_cast<T *>(su + off) = ok ? gu[b * p.su[0] + (long long)d * p.su[1] + tt] : zero;
           *reinterpret_cast<T *>(sd + off) = ok ? gd[b * p.sd[0] + (long long)d * p.sd[1] + tt] : zero;
           if (p.has_z)
@@ -424,7 +438,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
           for (int i = lane; i < nrow_bc * L; i += 32) {
             const int n = i / L, t = i - n * L;
             const int tt = t0 + t;
-            const bool ok = tt < p.seqlen;
+            const bool ok = tt < seqlen;
             const int off = bc_swz ? swz(n, t * bcs) : n * bc_row + t * bcs;
             const long long gb = b * p.sB[0] + g * p.sB[1] + n * p.sB[2] + tt;
             const long long gc = b * p.sC[0] + g * p.sC[1] + n * p.sC[2] + tt;
@@ -436,60 +450,154 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         if (lane == 0) mbar_arrive(&bar_full[s]);
       }
     };
-    // convert chunk ci's raw B/C (stage ci % STAGES) into fp32 [t][NP]
-    auto convert = [&](int ci) -> void {
-      const int s = ci % STAGES;
-      const unsigned char *sbr = smem + CF::OFF_BR + s * CF::BCMAX;
-      const unsigned char *scr = smem + CF::OFF_CR + s * CF::BCMAX;
-      float *b32 = reinterpret_cast<float *>(smem + CF::OFF_B32) + s * L * NP;
-      float *c32 = reinterpret_cast<float *>(smem + CF::OFF_C32) + s * L * NP;
-      for (int i = lane; i < NP * L; i += 32) {
-        const int n = i % NP, t = i / NP;
-        float vb = 0.f, vc = 0.f;
-        if (n < nrow_bc) {
-          const int off = bc_swz ? swz(n, t * bcs) : n * bc_row + t * bcs;
-          vb = to_f<BCT>(*reinterpret_cast<const BCT *>(sbr + off));
-          vc = to_f<BCT>(*reinterpret_cast<const BCT *>(scr + off));
-        }
-        b32[t * NP + n] = vb;
-        c32[t * NP + n] = vc;
-      }
-    };
-
-    bool ok = true;
     int issued = 0;
-    for (; issued < STAGES - 1 && issued < nchunks; ++issued) issue(issued);
-    for (int ci = 0; ci < nchunks && ok; ++ci) {
-      const int s = ci % STAGES;
-      const uint32_t ph = (ci / STAGES) & 1;
-      if (!FIXED) {
-        ok = mbar_wait(&bar_full[s], ph, p.err, kErrWaitFull);
-        if (!ok) break;
-        convert(ci);
-        __syncwarp();
+    bool ok = true;
+    for (; issued < nchunks; ++issued) {
+      const int prev = issued - STAGES;  // chunk that last used this stage
+      if (prev >= 0 && !mbar_wait(&bar_empty[prev % STAGES], (prev / STAGES) & 1, p.err, kErrWaitEmpty)) {
+        ok = false;
+        break;
       }
-      if (lane == 0) mbar_arrive(&bar_ready[s]);
-      // next chunk goes into the stage released by chunk ci + 1 - STAGES
-      if (issued < nchunks) {
-        const int prev = issued - STAGES;
-        if (prev >= 0) {
-          ok = mbar_wait(&bar_empty[prev % STAGES], (prev / STAGES) & 1, p.err, kErrWaitEmpty);
-          if (!ok) break;
-        }
-        issue(issued);
-        ++issued;
-      }
+      issue(issued);
     }
     if (!ok) {
       // give copies already in flight a bounded chance to land before exiting
-      for (int ci = 0; ci < issued; ++ci)
-        (void)mbar_try_wait(&bar_full[ci % STAGES], (ci / STAGES) & 1);
+      for (int ci = (issued > STAGES ? issued - STAGES : 0); ci < issued; ++ci)
+        (void)mbar_wait(&bar_full[ci % STAGES], (ci / STAGES) & 1, p.err, kErrWaitFull);
     }
     return;
   }
 
   // ==========================================================================
-  // Compute warps
+  // Element warps: per-element prep and epilogue, B/C conversion
+  // ==========================================================================
+  if (warp >= WS) {
+    const int le = (warp - WS) * 32 + lane;  // 0 .. WE*32-1
+    const int c = le >> 1;                   // channel within CTA
+    const int h = le & 1;                    // which half (EPT steps) of the sub-chunk
+    const int dloc = tile * CH + c;
+    const bool ch_ok = dloc < p.dpg;
+    const int d = ch_ok ? d0 + c : d0;
+    const float Dd = p.has_D ? p.D[d] : 0.f;
+    const float bias = p.has_bias ? p.bias[d] : 0.f;
+    const int softplus = p.softplus, has_z = p.has_z;
+    T *gout = static_cast<T *>(p.out);
+    const long long orow = (long long)b * p.so[0] + (long long)d * p.so[1];
+    const bool out_vec = p.out_vec != 0;
+    const int nrow_bc = p.dstate;
+    constexpr int bcs = (int)sizeof(BCT);
+    constexpr int bc_row = CF::BC_ROW;
+    constexpr bool bc_swz = (bc_row == 128);
+
+    // prep of sub-chunk q: (dt, dt, w, w) and fp32 B/C into slot q & 1
+    auto prep = [&](int q) -> bool {
+      const int ci = q / SUBS, sub = q - ci * SUBS, s = ci % STAGES;
+      if (!mbar_wait(&bar_full[s], (ci / STAGES) & 1, p.err, kErrWaitFull)) return false;
+      if (q >= 2 && !mbar_wait(&bar_pempty[q & 1], ((q - 2) >> 1) & 1, p.err, kErrWaitEmpty)) return false;
+      const unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
+      const unsigned char *sd = smem + CF::OFF_DL + s * CF::TILE;
+      float4 *P = reinterpret_cast<float4 *>(smem + CF::OFF_P + (q & 1) * CF::P_SLOT);
+      const int col0 = sub * S + h * EPT;
+      const int t0 = ci * L + col0;
+      float uv[EPT], dv[EPT];
+      lds_row<T, EPT>(su, c, col0, uv);
+      lds_row<T, EPT>(sd, c, col0, dv);
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) {
+        const float v = dv[k] + bias;
+        float dt = softplus ? softplus_t<T>(v) : v;
+        float w = dt * uv[k];
+        if (t0 + k >= seqlen) { dt = 0.f; w = 0.f; }  // padded steps leave x unchanged
+        P[(h * EPT + k) * CH + c] = make_float4(dt, dt, w, w);
+      }
+      if constexpr (!FIXED) {
+        const unsigned char *sbr = smem + CF::OFF_BR + s * CF::BCMAX;
+        const unsigned char *scr = smem + CF::OFF_CR + s * CF::BCMAX;
+        float *bc = reinterpret_cast<float *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
+        // items: (tensor, state n, half) -> EPT consecutive steps of one row
+        for (int it = le; it < 4 * NP; it += WE * 32) {
+          const int hh = it & 1, n = (it >> 1) % NP, tensor = (it >> 1) / NP;
+          float v[EPT];
+          if (n < nrow_bc) {
+            const unsigned char *raw = tensor ? scr : sbr;
+            const int col = sub * S + hh * EPT;
+            if constexpr (bc_swz) {
+              lds_row<BCT, EPT>(raw, n, col, v);
+            } else {
+#pragma unroll
+              for (int k = 0; k < EPT; ++k)
+                v[k] = to_f<BCT>(*reinterpret_cast<const BCT *>(raw + n * bc_row + (col + k) * bcs));
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < EPT; ++k) v[k] = 0.f;
+          }
+          float *dst = bc + tensor * S * NP + (hh * EPT) * NP + n;
+#pragma unroll
+          for (int k = 0; k < EPT; ++k) dst[k * NP] = v[k];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_pfull[q & 1]);
+      return true;
+    };
+    // epilogue of sub-chunk q: sum partial y, D skip, gate, round, store
+    auto epilogue = [&](int q) -> bool {
+      const int ci = q / SUBS, sub = q - ci * SUBS, s = ci % STAGES;
+      if (!mbar_wait(&bar_yfull[q & 1], (q >> 1) & 1, p.err, kErrWaitReady)) return false;
+      const float *Y = reinterpret_cast<const float *>(smem + CF::OFF_Y + (q & 1) * CF::Y_SLOT);
+      float y[EPT];
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) {
+        const float *row = Y + (h * EPT + k) * (CH * TN) + c * TN;
+        float acc = 0.f;
+        if constexpr (TN % 4 == 0) {
+#pragma unroll
+          for (int jj = 0; jj < TN; jj += 4) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(row + jj);
+            acc += (v4.x + v4.y) + (v4.z + v4.w);
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < TN; ++jj) acc += row[jj];
+        }
+        y[k] = acc;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_yempty[q & 1]);
+      const unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
+      const unsigned char *sz = smem + CF::OFF_Z + s * CF::TILE;
+      const int col0 = sub * S + h * EPT;
+      float uv[EPT];
+      lds_row<T, EPT>(su, c, col0, uv);
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) y[k] = fmaf(Dd, uv[k], y[k]);
+      if (has_z) {
+        float zv[EPT];
+        lds_row<T, EPT>(sz, c, col0, zv);
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) y[k] *= silu_t<T>(zv[k]);
+      }
+      const int t0 = ci * L + col0;
+      if (ch_ok && t0 < seqlen) stg_row<T, EPT>(gout + orow + t0, y, out_vec, seqlen - t0);
+      if (sub == SUBS - 1) {  // last use of this stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_empty[s]);
+      }
+      return true;
+    };
+
+    if (nsub > 0 && prep(0)) {
+      for (int q = 1; q <= nsub; ++q) {
+        if (q < nsub && !prep(q)) break;
+        if (!epilogue(q - 1)) break;
+      }
+    }
+    return;
+  }
+
+  // ==========================================================================
+  // Scan warps: the recurrence, K states per lane, TN lanes per channel
   // ==========================================================================
   const int cl = lane / TN;          // channel within warp
   const int j = lane - cl * TN;      // state group within channel
@@ -520,134 +628,60 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   f2 a2p[K / 2];
 #pragma unroll
   for (int k = 0; k < K / 2; ++k) a2p[k] = pk(a2[2 * k], a2[2 * k + 1]);
-  const float Dd = p.has_D ? p.D[d] : 0.f;
-  const float bias = p.has_bias ? p.bias[d] : 0.f;
-  const int softplus = p.softplus;
-  const int has_z = p.has_z;
-
   f2 x2[K / 2];
 #pragma unroll
   for (int k = 0; k < K / 2; ++k) x2[k] = pk(0.f, 0.f);
 
-  float4 *sP = reinterpret_cast<float4 *>(smem + CF::OFF_P + warp * CF::P_WARP);  // [S][CPW]
-  float *sY = reinterpret_cast<float *>(smem + CF::OFF_Y + warp * CF::Y_WARP);    // [CPW][TN][YPAD]
-  T *gout = static_cast<T *>(p.out);
-  const long long orow = (long long)b * p.so[0] + (long long)d * p.so[1];
-  const bool out_vec = p.out_vec != 0;
-  const int seqlen = p.seqlen;
-
-  bool ok = true;
-  for (int ci = 0; ci < nchunks; ++ci) {
-    const int s = ci % STAGES;
-    const uint32_t ph = (ci / STAGES) & 1;
-    if (!mbar_wait(&bar_ready[s], ph, p.err, kErrWaitReady)) { ok = false; break; }
-    if (!mbar_wait(&bar_full[s], ph, p.err, kErrWaitFull)) { ok = false; break; }
-    const unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
-    const unsigned char *sd = smem + CF::OFF_DL + s * CF::TILE;
-    const unsigned char *sz = smem + CF::OFF_Z + s * CF::TILE;
-    const float *b32 = reinterpret_cast<const float *>(smem + CF::OFF_B32) + s * L * NP;
-    const float *c32 = reinterpret_cast<const float *>(smem + CF::OFF_C32) + s * L * NP;
-
-#pragma unroll 1
-    for (int sub = 0; sub < L / S; ++sub) {
-      const int tb = ci * L + sub * S;  // first step of the sub-chunk
-      const int col0 = sub * S + j * SPT;  // my per-element steps: col0 .. col0+SPT-1
-      // ---- per-element prep: (dt, dt, w, w) for my SPT steps ----
-      float uv[SPT], dv[SPT];
-      lds_row<T, SPT>(su, c, col0, uv);
-      lds_row<T, SPT>(sd, c, col0, dv);
+  for (int q = 0; q < nsub; ++q) {
+    if (!mbar_wait(&bar_pfull[q & 1], (q >> 1) & 1, p.err, kErrWaitReady)) break;
+    if (q >= 2 && !mbar_wait(&bar_yempty[q & 1], ((q - 2) >> 1) & 1, p.err, kErrWaitEmpty)) break;
+    const float4 *P = reinterpret_cast<const float4 *>(smem + CF::OFF_P + (q & 1) * CF::P_SLOT);
+    const float *b32 = reinterpret_cast<const float *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
+    const float *c32 = b32 + S * NP;
+    float *Y = reinterpret_cast<float *>(smem + CF::OFF_Y + (q & 1) * CF::Y_SLOT);
 #pragma unroll
-      for (int k = 0; k < SPT; ++k) {
-        const float v = dv[k] + bias;
-        float dt = softplus ? softplus_t<T>(v) : v;
-        float w = dt * uv[k];
-        if (tb + j * SPT + k >= seqlen) { dt = 0.f; w = 0.f; }  // padded steps leave x unchanged
-        sP[(j * SPT + k) * CPW + cl] = make_float4(dt, dt, w, w);
-      }
-      __syncwarp();
-      // ---- recurrence over the S steps ----
-      float yv[4];
+    for (int tl = 0; tl < S; ++tl) {
+      const float4 pw = P[tl * CH + c];
+      const f2 dt2 = pk(pw.x, pw.y);
+      const f2 w2 = pk(pw.z, pw.w);
+      f2 y2 = pk(0.f, 0.f);
+      if constexpr (FIXED) {
 #pragma unroll
-      for (int tl = 0; tl < S; ++tl) {
-        const float4 pw = sP[tl * CPW + cl];
-        const f2 dt2 = pk(pw.x, pw.y);
-        const f2 w2 = pk(pw.z, pw.w);
-        f2 y2 = pk(0.f, 0.f);
-        if constexpr (FIXED) {
+        for (int k = 0; k < K / 2; ++k) {
+          const float2 e = upk(mul2(dt2, a2p[k]));
+          const f2 a = pk(ex2(e.x), ex2(e.y));
+          x2[k] = fma2(a, x2[k], w2);
+          y2 = fma2(cb2[k], x2[k], y2);
+        }
+      } else {
 #pragma unroll
-          for (int k = 0; k < K / 2; ++k) {
+        for (int k = 0; k < K / 2; k += 2) {
+          // B, C for states n0+2k .. n0+2k+3 (one 16-byte load each)
+          const float4 bq = *reinterpret_cast<const float4 *>(b32 + tl * NP + n0 + 2 * k);
+          const float4 cq = *reinterpret_cast<const float4 *>(c32 + tl * NP + n0 + 2 * k);
+          {
             const float2 e = upk(mul2(dt2, a2p[k]));
             const f2 a = pk(ex2(e.x), ex2(e.y));
-            x2[k] = fma2(a, x2[k], w2);
-            y2 = fma2(cb2[k], x2[k], y2);
+            x2[k] = fma2(a, x2[k], mul2(w2, pk(bq.x, bq.y)));
+            y2 = fma2(pk(cq.x, cq.y), x2[k], y2);
           }
-        } else {
-          const int t = sub * S + tl;
-#pragma unroll
-          for (int k = 0; k < K / 2; k += 2) {
-            // B, C for states n0+2k .. n0+2k+3 (one 16-byte load each)
-            const float4 bq = *reinterpret_cast<const float4 *>(b32 + t * NP + n0 + 2 * k);
-            const float4 cq = *reinterpret_cast<const float4 *>(c32 + t * NP + n0 + 2 * k);
-            {
-              const float2 e = upk(mul2(dt2, a2p[k]));
-              const f2 a = pk(ex2(e.x), ex2(e.y));
-              x2[k] = fma2(a, x2[k], mul2(w2, pk(bq.x, bq.y)));
-              y2 = fma2(pk(cq.x, cq.y), x2[k], y2);
-            }
-            {
-              const float2 e = upk(mul2(dt2, a2p[k + 1]));
-              const f2 a = pk(ex2(e.x), ex2(e.y));
-              x2[k + 1] = fma2(a, x2[k + 1], mul2(w2, pk(bq.z, bq.w)));
-              y2 = fma2(pk(cq.z, cq.w), x2[k + 1], y2);
-            }
-          }
-        }
-        const float2 yy = upk(y2);
-        yv[tl & 3] = yy.x + yy.y;
-        if ((tl & 3) == 3)
-          *reinterpret_cast<float4 *>(sY + (cl * TN + j) * CF::YPAD + (tl - 3)) =
-              make_float4(yv[0], yv[1], yv[2], yv[3]);
-      }
-      __syncwarp();
-      // ---- per-element epilogue for my SPT steps ----
-      float y[SPT];
-#pragma unroll
-      for (int k = 0; k < SPT; ++k) y[k] = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < TN; ++jj) {
-        const float *row = sY + (cl * TN + jj) * CF::YPAD + j * SPT;
-        if constexpr (SPT % 4 == 0) {
-#pragma unroll
-          for (int q = 0; q < SPT / 4; ++q) {
-            const float4 v4 = *reinterpret_cast<const float4 *>(row + 4 * q);
-            y[4 * q] += v4.x; y[4 * q + 1] += v4.y; y[4 * q + 2] += v4.z; y[4 * q + 3] += v4.w;
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < SPT / 2; ++q) {
-            const float2 v2 = *reinterpret_cast<const float2 *>(row + 2 * q);
-            y[2 * q] += v2.x; y[2 * q + 1] += v2.y;
+          {
+            const float2 e = upk(mul2(dt2, a2p[k + 1]));
+            const f2 a = pk(ex2(e.x), ex2(e.y));
+            x2[k + 1] = fma2(a, x2[k + 1], mul2(w2, pk(bq.z, bq.w)));
+            y2 = fma2(pk(cq.z, cq.w), x2[k + 1], y2);
           }
         }
       }
-#pragma unroll
-      for (int k = 0; k < SPT; ++k) y[k] = fmaf(Dd, uv[k], y[k]);
-      if (has_z) {
-        float zv[SPT];
-        lds_row<T, SPT>(sz, c, col0, zv);
-#pragma unroll
-        for (int k = 0; k < SPT; ++k) y[k] *= silu_t<T>(zv[k]);
-      }
-      if (ch_ok) {
-        const int t0 = tb + j * SPT;
-        if (t0 < seqlen) stg_row<T, SPT>(gout + orow + t0, y, out_vec, seqlen - t0);
-      }
-      __syncwarp();
+      const float2 yy = upk(y2);
+      Y[tl * (CH * TN) + c * TN + j] = yy.x + yy.y;  // step-major: one 128-byte row per warp
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bar_empty[s]);
+    if (lane == 0) {
+      mbar_arrive(&bar_pempty[q & 1]);
+      mbar_arrive(&bar_yfull[q & 1]);
+    }
   }
-  (void)ok;
 
   if (p.want_last && ch_ok) {
     float *lr = p.last + (long long)b * p.sl[0] + (long long)d * p.sl[1];
