@@ -14,9 +14,10 @@
 //     delta, z with TMA (cp.async.bulk.tensor, 128-byte swizzle) into a
 //     2-stage mbarrier ring, with the (batch, group) B/C tile of the chunk.
 //   * 2 element warps do the per-element work once per element, one 16-step
-//     sub-chunk ahead of the scan (softplus, dt*u, and the conversion of the
-//     sub-chunk's B/C to fp32 [t][n], so that a scan lane reads its K states
-//     of B and C with one 16-byte load) and one sub-chunk behind it (sum of
+//     sub-chunk ahead of the scan (softplus, dt*u, and the sub-chunk's B/C
+//     laid out per step so that a scan lane reads its K states of B and C with
+//     one 16-byte load: 16-bit B/C stay 16-bit, packed as state pairs, and are
+//     widened exactly in registers; fp32 B/C are transposed to [t][n]) and one sub-chunk behind it (sum of
 //     the TN partial y's, D skip, silu gate, rounding, 16-byte stores). The
 //     three roles hand over through double-buffered shared slots guarded by
 //     mbarriers, so per-element latency overlaps the recurrence.
@@ -326,9 +327,13 @@ struct Cfg {
   static constexpr int OFF_BR = OFF_Z + STAGES * TILE;
   static constexpr int OFF_CR = OFF_BR + (FIXED ? 0 : STAGES * BCMAX);
   static constexpr int OFF_P = OFF_CR + (FIXED ? 0 : STAGES * BCMAX);
-  static constexpr int P_SLOT = S * CH * 16;                      // (dt, dt, w, w) [S][CH]
+  static constexpr int P_SLOT = S * CH * 8;                       // (dt, w) [S][CH]
   static constexpr int OFF_BC = OFF_P + 2 * P_SLOT;
-  static constexpr int BC_SLOT = FIXED ? 0 : 2 * S * NP * 4;       // fp32 B then C, [S][NP] each
+  // B/C of one sub-chunk: fp32 B then C [S][NP] each when stored fp32; else the
+  // stored 16-bit values packed per step as, for each state group of K,
+  // K/2 words of (B_n, B_n+1) followed by K/2 words of (C_n, C_n+1).
+  static constexpr bool BCPACK = !BCF32;
+  static constexpr int BC_SLOT = FIXED ? 0 : (BCPACK ? S * NP * 4 : 2 * S * NP * 4);
   static constexpr int OFF_Y = OFF_BC + 2 * BC_SLOT;
   static constexpr int Y_SLOT = S * CH * TN * 4;                  // partial y [S][CH*TN]
   static constexpr int OFF_BAR = OFF_Y + 2 * Y_SLOT;
@@ -496,7 +501,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       if (q >= 2 && !mbar_wait(&bar_pempty[q & 1], ((q - 2) >> 1) & 1, p.err, kErrWaitEmpty)) return false;
       const unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
       const unsigned char *sd = smem + CF::OFF_DL + s * CF::TILE;
-      float4 *P = reinterpret_cast<float4 *>(smem + CF::OFF_P + (q & 1) * CF::P_SLOT);
+      float2 *P = reinterpret_cast<float2 *>(smem + CF::OFF_P + (q & 1) * CF::P_SLOT);
       const int col0 = sub * S + h * EPT;
       const int t0 = ci * L + col0;
       float uv[EPT], dv[EPT];
@@ -508,9 +513,35 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         float dt = softplus ? softplus_t<T>(v) : v;
         float w = dt * uv[k];
         if (t0 + k >= seqlen) { dt = 0.f; w = 0.f; }  // padded steps leave x unchanged
-        P[(h * EPT + k) * CH + c] = make_float4(dt, dt, w, w);
+        P[(h * EPT + k) * CH + c] = make_float2(dt, w);
       }
-      if constexpr (!FIXED) {
+      if constexpr (!FIXED && CF::BCPACK) {
+        // 16-bit B/C: pack rows (n, n+1) of the raw [n][t] tile into per-step
+        // words (B_n | B_n+1 << 16) and (C_n | C_n+1 << 16); no rounding.
+        static_assert(CF::BC_ROW == 128, "16-bit B/C rows are one swizzled 128-byte line");
+        const unsigned char *sbr = smem + CF::OFF_BR + s * CF::BCMAX;
+        const unsigned char *scr = smem + CF::OFF_CR + s * CF::BCMAX;
+        uint32_t *bcw = reinterpret_cast<uint32_t *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
+        // items: (tensor, state pair m, half) -> EPT steps of rows 2m and 2m+1
+        for (int it = le; it < 2 * NP; it += WE * 32) {
+          const int hh = it & 1, m = (it >> 1) % (NP / 2), tensor = (it >> 1) / (NP / 2);
+          const unsigned char *raw = tensor ? scr : sbr;
+          const int col = sub * S + hh * EPT;  // EPT 16-bit values = one 16-byte chunk
+          const int n = 2 * m;
+          uint4 r0 = make_uint4(0, 0, 0, 0), r1 = make_uint4(0, 0, 0, 0);
+          if (n < nrow_bc) r0 = *reinterpret_cast<const uint4 *>(raw + swz(n, col * 2));
+          if (n + 1 < nrow_bc) r1 = *reinterpret_cast<const uint4 *>(raw + swz(n + 1, col * 2));
+          const uint32_t a[4] = {r0.x, r0.y, r0.z, r0.w}, bb[4] = {r1.x, r1.y, r1.z, r1.w};
+          const int grp = n / K, wi = (n % K) / 2 + (tensor ? K / 2 : 0);
+          uint32_t *dst = bcw + (hh * EPT) * NP + grp * K + wi;
+#pragma unroll
+          for (int k = 0; k < EPT / 2; ++k) {
+            dst[(2 * k) * NP] = __byte_perm(a[k], bb[k], 0x5410);      // step 2k: low halves
+            dst[(2 * k + 1) * NP] = __byte_perm(a[k], bb[k], 0x7632);  // step 2k+1: high halves
+          }
+        }
+      }
+      if constexpr (!FIXED && !CF::BCPACK) {
         const unsigned char *sbr = smem + CF::OFF_BR + s * CF::BCMAX;
         const unsigned char *scr = smem + CF::OFF_CR + s * CF::BCMAX;
         float *bc = reinterpret_cast<float *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
@@ -635,15 +666,16 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   for (int q = 0; q < nsub; ++q) {
     if (!mbar_wait(&bar_pfull[q & 1], (q >> 1) & 1, p.err, kErrWaitReady)) break;
     if (q >= 2 && !mbar_wait(&bar_yempty[q & 1], ((q - 2) >> 1) & 1, p.err, kErrWaitEmpty)) break;
-    const float4 *P = reinterpret_cast<const float4 *>(smem + CF::OFF_P + (q & 1) * CF::P_SLOT);
+    const float2 *P = reinterpret_cast<const float2 *>(smem + CF::OFF_P + (q & 1) * CF::P_SLOT);
     const float *b32 = reinterpret_cast<const float *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
     const float *c32 = b32 + S * NP;
+    const uint32_t *bcw = reinterpret_cast<const uint32_t *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
     float *Y = reinterpret_cast<float *>(smem + CF::OFF_Y + (q & 1) * CF::Y_SLOT);
 #pragma unroll
     for (int tl = 0; tl < S; ++tl) {
-      const float4 pw = P[tl * CH + c];
-      const f2 dt2 = pk(pw.x, pw.y);
-      const f2 w2 = pk(pw.z, pw.w);
+      const float2 pw = P[tl * CH + c];
+      const f2 dt2 = pk(pw.x, pw.x);
+      const f2 w2 = pk(pw.y, pw.y);
       f2 y2 = pk(0.f, 0.f);
       if constexpr (FIXED) {
 #pragma unroll
@@ -652,6 +684,23 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
           const f2 a = pk(ex2(e.x), ex2(e.y));
           x2[k] = fma2(a, x2[k], w2);
           y2 = fma2(cb2[k], x2[k], y2);
+        }
+      } else if constexpr (CF::BCPACK) {
+        // K/2 words of B pairs then K/2 words of C pairs (16-byte loads)
+        uint32_t wv[K];
+#pragma unroll
+        for (int q4 = 0; q4 < K / 4; ++q4) {
+          const uint4 r = *reinterpret_cast<const uint4 *>(bcw + tl * NP + n0 + 4 * q4);
+          wv[4 * q4] = r.x; wv[4 * q4 + 1] = r.y; wv[4 * q4 + 2] = r.z; wv[4 * q4 + 3] = r.w;
+        }
+#pragma unroll
+        for (int k = 0; k < K / 2; ++k) {
+          const float2 bf = unpack2<T>(wv[k]);
+          const float2 cf = unpack2<T>(wv[K / 2 + k]);
+          const float2 e = upk(mul2(dt2, a2p[k]));
+          const f2 a = pk(ex2(e.x), ex2(e.y));
+          x2[k] = fma2(a, x2[k], mul2(w2, pk(bf.x, bf.y)));
+          y2 = fma2(pk(cf.x, cf.y), x2[k], y2);
         }
       } else {
 #pragma unroll
