@@ -83,7 +83,7 @@ def _traffic(workload):
 
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+    Q = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
@@ -116,22 +116,24 @@ class ClockSampler:
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, mx, reasons, power = [], None, set(), []
+        sm, mx, reasons, power, util = [], None, set(), [], []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 8:
                 continue
             try:
-                sm.append(float(f[0]))
-                mx = float(f[1])
-                power.append(float(f[2]))
+                sm_v, mx_v, p_v, u_v = float(f[0]), float(f[1]), float(f[2]), float(f[3])
             except ValueError:
                 continue
+            sm.append(sm_v)
+            mx = mx_v
+            power.append(p_v)
+            util.append(u_v)
             for n, v in zip(names, f[4:8]):
                 if v.lower() == "active":
                     reasons.add(n)
-        loaded = [s for s, p in zip(sm, power) if p > 300.0] or sm
+        loaded = [s for s, u in zip(sm, util) if u >= 50.0] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": mx,
                 "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(loaded),
                 "power_w_max": max(power) if power else None}
@@ -220,6 +222,8 @@ def run_ours(args, rank, world, local_rank):
     last = (torch.empty(w.batch, w.dim, w.dstate, dtype=torch.float32, device=dev)
             if w.return_last_state else None)
     params = api.make_params(*nu, w.delta_softplus, out, last)
+    workspace = api.attach_workspace(params, dev)  # segment summaries when the sequence is split
+    launches_per_step = 2 if workspace is not None else 1
     pref = ctypes.byref(params)
     stream = torch.cuda.Stream(device=dev)
     sptr = stream.cuda_stream
@@ -307,6 +311,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": w.dstate,
                    "groups": w.groups, "bc": w.bc, "io_dtype": w.dtype, "z": w.has_z,
                    "return_last_state": w.return_last_state, "parallelism": f"independent x{world}",
+                   "sequence_segmented": workspace is not None,
                    "l2": f"flushed before every step ({2 * l2 >> 20} MiB write, outside the kernel interval)"},
         "elems_per_s": elems,
         "compulsory_bytes_per_step": cb,
@@ -321,7 +326,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": world * cb / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
                 "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "kernel_hash": _kernel_hash(),
     }

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define SS_ABI_VERSION 1
+#define SS_ABI_VERSION 2
 
 /* Element types. u, delta, z and out share `in_dtype`. */
 typedef enum ss_dtype { SS_F32 = 0, SS_F16 = 1, SS_BF16 = 2 } ss_dtype;
@@ -101,6 +101,14 @@ typedef struct ss_fwd_params {
   int64_t B_stride[4], C_stride[4];
   int64_t A_stride[2];
   int64_t last_state_stride[3];
+  /* Optional device workspace (caller-owned, 16-byte aligned, not
+   * overlapping any tensor). When the (batch, group, channel-tile) work units
+   * cannot fill the GPU (few channels, long sequences), the forward splits the
+   * sequence into segments and keeps per-segment state summaries here; size it
+   * with ss_fwd_workspace_size. NULL / too small: the single-pass path runs
+   * instead (same results up to fp32 rounding, fewer CTAs). */
+  void *workspace;
+  int64_t workspace_bytes;
 } ss_fwd_params;
 
 /* SS_ABI_VERSION of the loaded library. */
@@ -112,6 +120,11 @@ const char *ss_status_string(int status);
 /* Validate `p` without launching anything (no CUDA call is made). Returns the
  * status ss_fwd would return before launching. */
 int ss_fwd_validate(const ss_fwd_params *p);
+
+/* Bytes of `workspace` the fastest schedule of `p` uses on the current device
+ * (0 if it uses none). Validates `p` like ss_fwd; makes a device-attribute
+ * query (no allocation, no launch). */
+int ss_fwd_workspace_size(const ss_fwd_params *p, int64_t *bytes);
 
 /* The selective-scan forward on device buffers, enqueued on `stream`.
  * Returns SS_OK once enqueued, or an error status with nothing enqueued

@@ -26,7 +26,7 @@ _lib = None
 
 SS_F32, SS_F16, SS_BF16 = 0, 1, 2
 SS_BC_FIXED, SS_BC_VARIABLE = 0, 1
-SS_ABI_VERSION = 1
+SS_ABI_VERSION = 2
 _DT = {torch.float32: SS_F32, torch.float16: SS_F16, torch.bfloat16: SS_BF16}
 
 _i64x2, _i64x3, _i64x4 = ctypes.c_int64 * 2, ctypes.c_int64 * 3, ctypes.c_int64 * 4
@@ -45,6 +45,7 @@ class SSFwdParams(ctypes.Structure):
         ("out", ctypes.c_void_p), ("last_state", ctypes.c_void_p),
         ("u_stride", _i64x3), ("delta_stride", _i64x3), ("z_stride", _i64x3), ("out_stride", _i64x3),
         ("B_stride", _i64x4), ("C_stride", _i64x4), ("A_stride", _i64x2), ("last_state_stride", _i64x3),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64),
     ]
 
 
@@ -76,6 +77,8 @@ def load_library():
             lib.ss_fwd_validate.restype = ctypes.c_int
             lib.ss_fwd.argtypes = [P, vp]
             lib.ss_fwd.restype = ctypes.c_int
+            lib.ss_fwd_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
+            lib.ss_fwd_workspace_size.restype = ctypes.c_int
             lib.ss_fwd_host.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.ss_fwd_host.restype = ctypes.c_int
             lib.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
@@ -175,6 +178,20 @@ def make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last_s
     return p
 
 
+def attach_workspace(p: SSFwdParams, device) -> "torch.Tensor | None":
+    """Allocate (torch, on `device`) and attach the workspace the fastest
+    schedule of p asks for; returns the tensor to keep alive, or None."""
+    lib = load_library()
+    n = ctypes.c_int64(0)
+    with torch.cuda.device(device):
+        _check(lib.ss_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)))
+    if n.value <= 0:
+        return None
+    ws = torch.empty(int(n.value), dtype=torch.uint8, device=device)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), int(n.value)
+    return ws
+
+
 def selective_scan_fn(u, delta, A, B, C, D=None, z=None, delta_bias=None,
                       delta_softplus=False, return_last_state=False):
     """Selective-scan forward on CUDA tensors; runs on the current stream.
@@ -193,9 +210,12 @@ def selective_scan_fn(u, delta, A, B, C, D=None, z=None, delta_bias=None,
     last = (torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
             if return_last_state else None)
     p = make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last)
+    ws = attach_workspace(p, u.device)  # noqa: F841 (kept alive until the launch is enqueued)
     stream = torch.cuda.current_stream(u.device).cuda_stream
     with torch.cuda.device(u.device):
         _check(lib.ss_fwd(ctypes.byref(p), stream))
+    if ws is not None:
+        ws.record_stream(torch.cuda.current_stream(u.device))
     return (out, last) if return_last_state else out
 
 
@@ -223,6 +243,7 @@ class HostRunner:
         self.last = (torch.empty((du.shape[0], du.shape[1], dev[2].shape[1]), dtype=torch.float32, device=device)
                      if return_last_state else None)
         self.params = make_params(*dev, delta_softplus, self.out, self.last)
+        self.workspace = attach_workspace(self.params, self.out.device)
         self.h_out = torch.empty(du.shape, dtype=du.dtype, pin_memory=True)
         self.h_last = (torch.empty(self.last.shape, dtype=torch.float32, pin_memory=True)
                        if return_last_state else None)

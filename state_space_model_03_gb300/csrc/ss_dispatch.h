@@ -12,9 +12,10 @@ struct KernelInfo {
 };
 
 // np in {4, 8, 16, 32, 64}; bc_f32: variable B/C stored as fp32 (else in the
-// input dtype). Returns fn == nullptr if not instantiated.
-KernelInfo lookup_f32(int np, bool fixed, bool bc_f32, bool tma);
-KernelInfo lookup_f16(int np, bool fixed, bool bc_f32, bool tma);
-KernelInfo lookup_bf16(int np, bool fixed, bool bc_f32, bool tma);
+// input dtype); summary: the segment-summary pass instead of the forward.
+// Returns fn == nullptr if not instantiated.
+KernelInfo lookup_f32(int np, bool fixed, bool bc_f32, bool tma, bool summary);
+KernelInfo lookup_f16(int np, bool fixed, bool bc_f32, bool tma, bool summary);
+KernelInfo lookup_bf16(int np, bool fixed, bool bc_f32, bool tma, bool summary);
 
 }  // namespace ssk

@@ -53,9 +53,15 @@ constexpr int32_t kErrWaitReady = 3;
 constexpr uint32_t kMaxWaitIters = 1u << 22;
 
 struct KParams {
-  int batch, dim, seqlen, dstate, ngroups, dpg, tiles_per_group, nchunks;
+  int batch, dim, seqlen, dstate, ngroups, dpg, tiles_per_group;
   int has_z, has_D, has_bias, softplus, want_last;
   int out_vec;  // out rows 16-byte aligned (base and strides): vector stores allowed
+  // Sequence segmentation (blockIdx.z = segment): steps [seg*seg_len, ...).
+  // ws holds, for segments 0..nseg-2, the end state reached from a zero state
+  // (NP floats per (batch, channel, segment)) followed by the segment's step
+  // sums (one float per (batch, channel, segment)).
+  int seg_len, nseg;
+  float *ws;
   const void *u, *delta, *z, *B, *C;
   const float *A, *D, *bias;
   void *out;
@@ -349,7 +355,9 @@ struct Cfg {
 // ----------------------------------------------------------------------------
 // The kernel
 // ----------------------------------------------------------------------------
-template <typename T, int NP, int K, bool FIXED, bool BCF32, bool USE_TMA>
+// SUMMARY = true: the segment-summary pass (end state from a zero state and
+// the sum of dt over the segment, written to p.ws; no outputs).
+template <typename T, int NP, int K, bool FIXED, bool BCF32, bool USE_TMA, bool SUMMARY>
 __global__ void __launch_bounds__(Cfg<T, NP, K, FIXED, BCF32>::THREADS, Cfg<T, NP, K, FIXED, BCF32>::MINB)
 ss_fwd_kernel(const __grid_constant__ KParams p,
               const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
@@ -375,9 +383,13 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   const int tile = blockIdx.x - g * p.tiles_per_group;
   const int b = blockIdx.y;
   const int d0 = g * p.dpg + tile * CH;  // first channel of the tile
-  const int nchunks = p.nchunks;
+  const int seg = blockIdx.z;
+  const int tseg0 = seg * p.seg_len;                        // first step of this segment
+  const int tseg1 = min(p.seqlen, tseg0 + p.seg_len);       // one past its last step
+  const int nchunks = (tseg1 - tseg0 + L - 1) / L;
   const int nsub = nchunks * SUBS;
   const int seqlen = p.seqlen;
+  const int nsum = p.nseg - 1;  // segments with a summary
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -404,7 +416,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     const int nrow_bc = p.dstate;
     auto issue = [&](int ci) -> void {
       const int s = ci % STAGES;
-      const int t0 = ci * L;
+      const int t0 = tseg0 + ci * L;
       unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
       unsigned char *sd = smem + CF::OFF_DL + s * CF::TILE;
       unsigned char *sz = smem + CF::OFF_Z + s * CF::TILE;
@@ -412,12 +424,13 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       unsigned char *scr = smem + CF::OFF_CR + s * CF::BCMAX;
       if constexpr (USE_TMA) {
         if (lane == 0) {
-          uint32_t bytes = (2 + (p.has_z ? 1 : 0)) * CF::TILE;
+          const bool ldz = p.has_z && !SUMMARY;
+          uint32_t bytes = (2 + (ldz ? 1 : 0)) * CF::TILE;
           if (!FIXED) bytes += 2 * nrow_bc * bc_row;
           mbar_arrive_expect_tx(&bar_full[s], bytes);
           tma_load_3d(su, &tm_u, &bar_full[s], t0, d0, b);
           tma_load_3d(sd, &tm_dl, &bar_full[s], t0, d0, b);
-          if (p.has_z) tma_load_3d(sz, &tm_z, &bar_full[s], t0, d0, b);
+          if (ldz) tma_load_3d(sz, &tm_z, &bar_full[s], t0, d0, b);
           if (!FIXED) {
             tma_load_4d(sbr, &tm_B, &bar_full[s], t0, 0, g, b);
             tma_load_4d(scr, &tm_C, &bar_full[s], t0, 0, g, b);
@@ -436,7 +449,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
           const T zero = from_f<T>(0.f);
           *reinterpret_cast<T *>(su + off) = ok ? gu[b * p.su[0] + (long long)d * p.su[1] + tt] : zero;
           *reinterpret_cast<T *>(sd + off) = ok ? gd[b * p.sd[0] + (long long)d * p.sd[1] + tt] : zero;
-          if (p.has_z)
+          if (p.has_z && !SUMMARY)
             *reinterpret_cast<T *>(sz + off) = ok ? gz[b * p.sz[0] + (long long)d * p.sz[1] + tt] : zero;
         }
         if (!FIXED) {
@@ -494,7 +507,8 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     constexpr int bc_row = CF::BC_ROW;
     constexpr bool bc_swz = (bc_row == 128);
 
-    // prep of sub-chunk q: (dt, dt, w, w) and fp32 B/C into slot q & 1
+    float lam = 0.f;  // SUMMARY: sum of dt over my steps of the segment
+    // prep of sub-chunk q: (dt, w) and the sub-chunk's B/C into slot q & 1
     auto prep = [&](int q) -> bool {
       const int ci = q / SUBS, sub = q - ci * SUBS, s = ci % STAGES;
       if (!mbar_wait(&bar_full[s], (ci / STAGES) & 1, p.err, kErrWaitFull)) return false;
@@ -503,7 +517,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       const unsigned char *sd = smem + CF::OFF_DL + s * CF::TILE;
       float2 *P = reinterpret_cast<float2 *>(smem + CF::OFF_P + (q & 1) * CF::P_SLOT);
       const int col0 = sub * S + h * EPT;
-      const int t0 = ci * L + col0;
+      const int t0 = tseg0 + ci * L + col0;
       float uv[EPT], dv[EPT];
       lds_row<T, EPT>(su, c, col0, uv);
       lds_row<T, EPT>(sd, c, col0, dv);
@@ -512,7 +526,8 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         const float v = dv[k] + bias;
         float dt = softplus ? softplus_t<T>(v) : v;
         float w = dt * uv[k];
-        if (t0 + k >= seqlen) { dt = 0.f; w = 0.f; }  // padded steps leave x unchanged
+        if (t0 + k >= tseg1) { dt = 0.f; w = 0.f; }  // padded steps leave x unchanged
+        if constexpr (SUMMARY) lam += dt;
         P[(h * EPT + k) * CH + c] = make_float2(dt, w);
       }
       if constexpr (!FIXED && CF::BCPACK) {
@@ -609,8 +624,8 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
 #pragma unroll
         for (int k = 0; k < EPT; ++k) y[k] *= silu_t<T>(zv[k]);
       }
-      const int t0 = ci * L + col0;
-      if (ch_ok && t0 < seqlen) stg_row<T, EPT>(gout + orow + t0, y, out_vec, seqlen - t0);
+      const int t0 = tseg0 + ci * L + col0;
+      if (ch_ok && t0 < tseg1) stg_row<T, EPT>(gout + orow + t0, y, out_vec, tseg1 - t0);
       if (sub == SUBS - 1) {  // last use of this stage
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_empty[s]);
@@ -618,7 +633,20 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       return true;
     };
 
-    if (nsub > 0 && prep(0)) {
+    if constexpr (SUMMARY) {
+      bool ok = true;
+      for (int q = 0; q < nsub && ok; ++q) {
+        ok = prep(q);
+        if (ok && (q % SUBS) == SUBS - 1) {  // last use of this stage
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_empty[(q / SUBS) % STAGES]);
+        }
+      }
+      // two lanes per channel: combine their step sums
+      lam += __shfl_xor_sync(0xffffffffu, lam, 1);
+      if (ok && h == 0 && ch_ok)
+        p.ws[(long long)nsum * NP * p.batch * p.dim + ((long long)b * p.dim + d) * nsum + seg] = lam;
+    } else if (nsub > 0 && prep(0)) {
       for (int q = 1; q <= nsub; ++q) {
         if (q < nsub && !prep(q)) break;
         if (!epilogue(q - 1)) break;
@@ -662,10 +690,28 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   f2 x2[K / 2];
 #pragma unroll
   for (int k = 0; k < K / 2; ++k) x2[k] = pk(0.f, 0.f);
+  const long long row_bd = (long long)b * p.dim + d;
+  if (!SUMMARY && seg > 0) {
+    // carry-in: fold the summaries of segments 0..seg-1 (state after segment
+    // k from state x: exp(A * sum dt) x + end state from zero)
+    const float *wsx = p.ws + row_bd * nsum * NP;
+    const float *wsl = p.ws + (long long)nsum * NP * p.batch * p.dim + row_bd * nsum;
+    for (int kseg = 0; kseg < seg; ++kseg) {
+      const float lk = wsl[kseg];
+      const f2 l2 = pk(lk, lk);
+#pragma unroll
+      for (int k = 0; k < K / 2; ++k) {
+        const float2 e = upk(mul2(l2, a2p[k]));
+        const f2 dec = pk(ex2(e.x), ex2(e.y));
+        const float2 xe = *reinterpret_cast<const float2 *>(wsx + kseg * NP + n0 + 2 * k);
+        x2[k] = fma2(dec, x2[k], pk(xe.x, xe.y));
+      }
+    }
+  }
 
   for (int q = 0; q < nsub; ++q) {
     if (!mbar_wait(&bar_pfull[q & 1], (q >> 1) & 1, p.err, kErrWaitReady)) break;
-    if (q >= 2 && !mbar_wait(&bar_yempty[q & 1], ((q - 2) >> 1) & 1, p.err, kErrWaitEmpty)) break;
+    if (!SUMMARY && q >= 2 && !mbar_wait(&bar_yempty[q & 1], ((q - 2) >> 1) & 1, p.err, kErrWaitEmpty)) break;
     const float2 *P = reinterpret_cast<const float2 *>(smem + CF::OFF_P + (q & 1) * CF::P_SLOT);
     const float *b32 = reinterpret_cast<const float *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
     const float *c32 = b32 + S * NP;
@@ -683,7 +729,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
           const float2 e = upk(mul2(dt2, a2p[k]));
           const f2 a = pk(ex2(e.x), ex2(e.y));
           x2[k] = fma2(a, x2[k], w2);
-          y2 = fma2(cb2[k], x2[k], y2);
+          if constexpr (!SUMMARY) y2 = fma2(cb2[k], x2[k], y2);
         }
       } else if constexpr (CF::BCPACK) {
         // K/2 words of B pairs then K/2 words of C pairs (16-byte loads)
@@ -700,7 +746,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
           const float2 e = upk(mul2(dt2, a2p[k]));
           const f2 a = pk(ex2(e.x), ex2(e.y));
           x2[k] = fma2(a, x2[k], mul2(w2, pk(bf.x, bf.y)));
-          y2 = fma2(pk(cf.x, cf.y), x2[k], y2);
+          if constexpr (!SUMMARY) y2 = fma2(pk(cf.x, cf.y), x2[k], y2);
         }
       } else {
 #pragma unroll
@@ -712,27 +758,40 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
             const float2 e = upk(mul2(dt2, a2p[k]));
             const f2 a = pk(ex2(e.x), ex2(e.y));
             x2[k] = fma2(a, x2[k], mul2(w2, pk(bq.x, bq.y)));
-            y2 = fma2(pk(cq.x, cq.y), x2[k], y2);
+            if constexpr (!SUMMARY) y2 = fma2(pk(cq.x, cq.y), x2[k], y2);
           }
           {
             const float2 e = upk(mul2(dt2, a2p[k + 1]));
             const f2 a = pk(ex2(e.x), ex2(e.y));
             x2[k + 1] = fma2(a, x2[k + 1], mul2(w2, pk(bq.z, bq.w)));
-            y2 = fma2(pk(cq.z, cq.w), x2[k + 1], y2);
+            if constexpr (!SUMMARY) y2 = fma2(pk(cq.z, cq.w), x2[k + 1], y2);
           }
         }
       }
-      const float2 yy = upk(y2);
-      Y[tl * (CH * TN) + c * TN + j] = yy.x + yy.y;  // step-major: one 128-byte row per warp
+      if constexpr (!SUMMARY) {
+        const float2 yy = upk(y2);
+        Y[tl * (CH * TN) + c * TN + j] = yy.x + yy.y;  // step-major: one 128-byte row per warp
+      }
     }
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&bar_pempty[q & 1]);
-      mbar_arrive(&bar_yfull[q & 1]);
+      if constexpr (!SUMMARY) mbar_arrive(&bar_yfull[q & 1]);
     }
   }
 
-  if (p.want_last && ch_ok) {
+  if constexpr (SUMMARY) {
+    // end state of this segment from a zero state (x, or x / B for fixed B/C)
+    if (ch_ok) {
+      float *wsx = p.ws + (row_bd * nsum + seg) * NP;
+#pragma unroll
+      for (int k = 0; k < K / 2; ++k)
+        *reinterpret_cast<float2 *>(wsx + n0 + 2 * k) = upk(x2[k]);
+    }
+    return;
+  }
+
+  if (p.want_last && ch_ok && seg == p.nseg - 1) {
     float *lr = p.last + (long long)b * p.sl[0] + (long long)d * p.sl[1];
 #pragma unroll
     for (int k = 0; k < K / 2; ++k) {

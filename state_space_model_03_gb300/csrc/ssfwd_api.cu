@@ -24,7 +24,7 @@ __device__ int32_t g_error_word;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int32_t *g_err_ptr[kMaxDevices] = {};
-bool g_attr_done[kMaxDevices][3][5][2][2][2] = {};
+bool g_attr_done[kMaxDevices][3][5][2][2][2][2] = {};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -132,6 +132,14 @@ int validate(const ss_fwd_params *p) {
   for (int i = 0; i < ni; ++i)
     if (overlap(out, ins[i]) || overlap(last, ins[i])) return SS_ERR_ALIAS;
   if (overlap(out, last)) return SS_ERR_ALIAS;
+  if (p->workspace_bytes < 0) return SS_ERR_SHAPE;
+  if (p->workspace && p->workspace_bytes > 0) {
+    const Range ws{reinterpret_cast<uintptr_t>(p->workspace),
+                   reinterpret_cast<uintptr_t>(p->workspace) + static_cast<uintptr_t>(p->workspace_bytes)};
+    for (int i = 0; i < ni; ++i)
+      if (overlap(ws, ins[i])) return SS_ERR_ALIAS;
+    if (overlap(ws, out) || overlap(ws, last)) return SS_ERR_ALIAS;
+  }
   return SS_OK;
 }
 
@@ -145,11 +153,11 @@ int padded_states(int64_t n) {
 
 int np_index(int np) { return np == 4 ? 0 : np == 8 ? 1 : np == 16 ? 2 : np == 32 ? 3 : 4; }
 
-ssk::KernelInfo lookup(int dt, int np, bool fixed, bool bc_f32, bool tma) {
+ssk::KernelInfo lookup(int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary) {
   switch (dt) {
-    case SS_F32: return ssk::lookup_f32(np, fixed, bc_f32, tma);
-    case SS_F16: return ssk::lookup_f16(np, fixed, bc_f32, tma);
-    default: return ssk::lookup_bf16(np, fixed, bc_f32, tma);
+    case SS_F32: return ssk::lookup_f32(np, fixed, bc_f32, tma, summary);
+    case SS_F16: return ssk::lookup_f16(np, fixed, bc_f32, tma, summary);
+    default: return ssk::lookup_bf16(np, fixed, bc_f32, tma, summary);
   }
 }
 
@@ -222,7 +230,79 @@ __global__ void zero_last_state(float *last, int64_t batch, int64_t dim, int64_t
   }
 }
 
-int launch(const ss_fwd_params *p, cudaStream_t stream) {
+int num_sms(int dev) {
+  static int cache[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  if (!cache[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+// Sequence segmentation: when the (batch, group, channel-tile) CTAs cannot
+// fill the GPU, the sequence is cut into segments processed by separate CTAs.
+// A summary pass records, for every segment but the last, the state it reaches
+// from zero and the sum of its steps; the forward pass folds the summaries of
+// the preceding segments into its starting state.
+constexpr int64_t kSegMinSteps = 2048;  // shortest segment worth a summary pass
+constexpr int kMaxSegments = 64;
+
+struct SegPlan {
+  int nseg = 1;
+  int seg_len = 0;
+  int64_t ws_bytes = 0;
+};
+
+SegPlan plan_segments(const ss_fwd_params *p, int np, int L, int ch, int nsm) {
+  SegPlan sp;
+  sp.seg_len = static_cast<int>(p->seqlen);
+  const int64_t groups = p->bc_mode == SS_BC_FIXED ? 1 : p->ngroups;
+  const int64_t dpg = p->dim / groups;
+  const int64_t base = (dpg + ch - 1) / ch * groups * p->batch;
+  if (nsm <= 0 || base >= 2 * nsm || p->seqlen < 2 * kSegMinSteps) return sp;
+  int64_t want = (3 * nsm + base - 1) / base;
+  want = std::min<int64_t>(want, p->seqlen / kSegMinSteps);
+  want = std::min<int64_t>(want, kMaxSegments);
+  if (want < 2) return sp;
+  int64_t len = (p->seqlen + want - 1) / want;
+  len = (len + L - 1) / L * L;
+  sp.nseg = static_cast<int>((p->seqlen + len - 1) / len);
+  sp.seg_len = static_cast<int>(len);
+  if (sp.nseg < 2) { sp.nseg = 1; sp.seg_len = static_cast<int>(p->seqlen); return sp; }
+  sp.ws_bytes = p->batch * p->dim * (sp.nseg - 1) * (np + 1) * int64_t(sizeof(float));
+  return sp;
+}
+
+bool set_smem_attr(int dev, const ssk::KernelInfo &ki, int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  bool &done = g_attr_done[dev][dt][np_index(np)][fixed][bc_f32 && !fixed][tma][summary];
+  if (!done) {
+    if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) != cudaSuccess)
+      return false;
+    done = true;
+  }
+  return true;
+}
+
+// Bytes of workspace the fastest path wants for p (0 if it needs none).
+int workspace_bytes(const ss_fwd_params *p, int64_t *bytes) {
+  *bytes = 0;
+  if (p->batch * p->dim == 0 || p->seqlen == 0) return SS_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+  const bool fixed = p->bc_mode == SS_BC_FIXED;
+  const int np = padded_states(p->dstate);
+  ssk::KernelInfo ki = lookup(p->in_dtype, np, fixed, p->bc_dtype == SS_F32, true, false);
+  if (!ki.fn) return SS_ERR_UNSUPPORTED;
+  *bytes = plan_segments(p, np, ki.L, ki.ch, num_sms(dev)).ws_bytes;
+  return SS_OK;
+}
+
+// Enqueue the forward. ws/ws_bytes: workspace for sequence segmentation
+// (device memory, may be NULL/0: the single-pass path is used then).
+int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_bytes) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
   if (p->batch * p->dim == 0) return SS_OK;
@@ -243,7 +323,7 @@ int launch(const ss_fwd_params *p, cudaStream_t stream) {
   const int np = padded_states(p->dstate);
   const int es = elem_size(p->in_dtype), bs = elem_size(p->bc_dtype);
   const bool bc_f32 = p->bc_dtype == SS_F32;
-  ssk::KernelInfo ki = lookup(p->in_dtype, np, fixed, bc_f32, true);
+  ssk::KernelInfo ki = lookup(p->in_dtype, np, fixed, bc_f32, true, false);
   if (!ki.fn) return SS_ERR_UNSUPPORTED;
 
   ssk::KParams kp;
@@ -255,7 +335,6 @@ int launch(const ss_fwd_params *p, cudaStream_t stream) {
   kp.ngroups = fixed ? 1 : static_cast<int>(p->ngroups);
   kp.dpg = kp.dim / kp.ngroups;
   kp.tiles_per_group = (kp.dpg + ki.ch - 1) / ki.ch;
-  kp.nchunks = static_cast<int>((p->seqlen + ki.L - 1) / ki.L);
   kp.has_z = p->z != nullptr;
   kp.has_D = p->D != nullptr;
   kp.has_bias = p->delta_bias != nullptr;
@@ -274,6 +353,15 @@ int launch(const ss_fwd_params *p, cudaStream_t stream) {
   kp.sA[0] = p->A_stride[0]; kp.sA[1] = p->A_stride[1];
   kp.err = err;
 
+  SegPlan sp = plan_segments(p, np, ki.L, ki.ch, num_sms(dev));
+  if (sp.nseg > 1 && (!ws || ws_bytes < sp.ws_bytes || !aligned(ws, 16) || std::getenv("SSFWD_NO_SEGMENTS"))) {
+    sp.nseg = 1;  // no (or too small a) workspace: single pass over the whole sequence
+    sp.seg_len = kp.seqlen;
+  }
+  kp.nseg = sp.nseg;
+  kp.seg_len = sp.seg_len;
+  kp.ws = sp.nseg > 1 ? static_cast<float *>(ws) : nullptr;
+
   // TMA when every streamed tensor has a legal descriptor; else the generic
   // (plain-load) producer with the same compute path.
   CUtensorMap tm[5];
@@ -284,26 +372,30 @@ int launch(const ss_fwd_params *p, cudaStream_t stream) {
   if (tma && p->z) tma = make_map3(&tm[2], p->z, es, p, p->z_stride, ki.L, ki.ch);
   if (tma && !fixed) tma = make_map4(&tm[3], p->B, bs, p, p->B_stride, ki.L);
   if (tma && !fixed) tma = make_map4(&tm[4], p->C, bs, p, p->C_stride, ki.L);
-  if (!tma) ki = lookup(p->in_dtype, np, fixed, bc_f32, false);
+  if (!tma) ki = lookup(p->in_dtype, np, fixed, bc_f32, false, false);
   if (!ki.fn) return SS_ERR_UNSUPPORTED;
-
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    bool &done = g_attr_done[dev][p->in_dtype][np_index(np)][fixed][bc_f32 && !fixed][tma];
-    if (!done) {
-      if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) != cudaSuccess)
-        return SS_ERR_CUDA;
-      done = true;
-    }
+  if (!set_smem_attr(dev, ki, p->in_dtype, np, fixed, bc_f32, tma, false)) return SS_ERR_CUDA;
+  ssk::KernelInfo ks{};
+  if (sp.nseg > 1) {
+    ks = lookup(p->in_dtype, np, fixed, bc_f32, tma, true);
+    if (!ks.fn) return SS_ERR_UNSUPPORTED;
+    if (!set_smem_attr(dev, ks, p->in_dtype, np, fixed, bc_f32, tma, true)) return SS_ERR_CUDA;
   }
   if (fault_injected("launch")) return SS_ERR_CUDA;
-  dim3 grid(static_cast<unsigned>(kp.tiles_per_group * kp.ngroups), static_cast<unsigned>(kp.batch));
+  const unsigned gx = static_cast<unsigned>(kp.tiles_per_group * kp.ngroups), gy = static_cast<unsigned>(kp.batch);
   if (std::getenv("SSFWD_DEBUG"))  // opt-in launch report on stderr
-    std::fprintf(stderr, "ssfwd: %s np=%d fixed=%d bc_f32=%d ch=%d L=%d grid=%ux%u threads=%d smem=%d encode=%d\n",
-                 tma ? "tma" : "generic", np, (int)fixed, (int)bc_f32, ki.ch, ki.L, grid.x, grid.y, ki.threads,
-                 ki.smem, g_encode != nullptr);
+    std::fprintf(stderr,
+                 "ssfwd: %s np=%d fixed=%d bc_f32=%d ch=%d L=%d grid=%ux%ux%d seg_len=%d threads=%d smem=%d\n",
+                 tma ? "tma" : "generic", np, (int)fixed, (int)bc_f32, ki.ch, ki.L, gx, gy, sp.nseg, sp.seg_len,
+                 ki.threads, ki.smem);
   void *args[6] = {&kp, &tm[0], &tm[1], &tm[2], &tm[3], &tm[4]};
-  cudaError_t e = cudaLaunchKernel(ki.fn, grid, dim3(ki.threads), args, static_cast<size_t>(ki.smem), stream);
+  if (sp.nseg > 1) {
+    cudaError_t e = cudaLaunchKernel(ks.fn, dim3(gx, gy, sp.nseg - 1), dim3(ks.threads), args,
+                                     static_cast<size_t>(ks.smem), stream);
+    if (e != cudaSuccess) return SS_ERR_CUDA;
+  }
+  cudaError_t e = cudaLaunchKernel(ki.fn, dim3(gx, gy, sp.nseg), dim3(ki.threads), args,
+                                   static_cast<size_t>(ki.smem), stream);
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
@@ -361,10 +453,18 @@ const char *ss_status_string(int s) {
 
 int ss_fwd_validate(const ss_fwd_params *p) { return validate(p); }
 
+int ss_fwd_workspace_size(const ss_fwd_params *p, int64_t *bytes) {
+  if (!bytes) return SS_ERR_NULL;
+  *bytes = 0;
+  int st = validate(p);
+  if (st != SS_OK) return st;
+  return workspace_bytes(p, bytes);
+}
+
 int ss_fwd(const ss_fwd_params *p, void *stream) {
   int st = validate(p);
   if (st != SS_OK) return st;
-  return launch(p, static_cast<cudaStream_t>(stream));
+  return launch(p, static_cast<cudaStream_t>(stream), p->workspace, p->workspace_bytes);
 }
 
 int ss_fwd_host(const ss_fwd_params *p, const void *h_u, const void *h_delta, const void *h_z, const void *h_B,
@@ -396,7 +496,7 @@ int ss_fwd_host(const ss_fwd_params *p, const void *h_u, const void *h_delta, co
     if (!c.dst) return SS_ERR_NULL;
     if (cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return SS_ERR_CUDA;
   }
-  st = launch(p, s);
+  st = launch(p, s, p->workspace, p->workspace_bytes);
   if (st != SS_OK) return st;
   if (h_out && n3 && cudaMemcpyAsync(h_out, p->out, n3 * es, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return SS_ERR_CUDA;

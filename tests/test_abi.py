@@ -30,7 +30,7 @@ def _declared_functions():
 def test_exports_every_declared_symbol(lib):
     names = _declared_functions()
     assert set(names) == {"ss_abi_version", "ss_status_string", "ss_fwd_validate", "ss_fwd",
-                          "ss_fwd_host", "ss_device_error"}
+                          "ss_fwd_host", "ss_device_error", "ss_fwd_workspace_size"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -104,6 +104,8 @@ def test_valid_params_pass(lib):
     (lambda p: setattr(p, "out", p.z + 64), 6),               # partial overlap with z
     (lambda p: setattr(p, "last_state", p.A), 6),
     (lambda p: setattr(p, "last_state", p.out + 128), 6),
+    (lambda p: setattr(p, "workspace_bytes", -1), 2),
+    (lambda p: (setattr(p, "workspace", p.u + 64), setattr(p, "workspace_bytes", 256)), 6),
 ])
 def test_invalid_params_rejected(lib, mutate, status):
     p = _good()

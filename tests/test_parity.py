@@ -244,3 +244,43 @@ def test_repeatable_bitwise():
     a = api.selective_scan_fn(**dev, delta_softplus=True)
     b = api.selective_scan_fn(**dev, delta_softplus=True)
     assert torch.equal(a, b)
+
+
+SEGMENTED = [
+    # few channels and long sequences: the sequence is split across CTAs
+    (1, 64, 8192, 16, 1, "variable", "bf16", True, True),
+    (1, 40, 8000, 16, 1, "fixed", "fp32", False, True),
+    (2, 32, 12345, 16, 2, "variable", "fp16", True, True),
+    (1, 48, 9000, 5, 1, "variable", "fp32", False, True),
+    (1, 24, 8193, 16, 1, "fixed", "bf16", True, False),
+]
+
+
+@pytest.mark.parametrize("case", SEGMENTED, ids=[f"{c[6]}-{c[5]}-b{c[0]}d{c[1]}l{c[2]}n{c[3]}" for c in SEGMENTED])
+def test_segmented_sequence(case, monkeypatch):
+    """Few (batch, channel) rows and a long sequence: the forward cuts the
+    sequence into segments joined through per-segment state summaries. It must
+    match the oracle, and the single-pass schedule up to rounding."""
+    b, d, l, n, g, bc, dt, z, last = case
+    w = workloads.Workload("seg", b, d, l, n, groups=g, bc=bc, dtype=dt, has_z=z, return_last_state=last,
+                           bc_4d=g > 1, seed=77 + l, dt_range=(0.001, 0.01) if bc == "fixed" else (0.001, 0.1),
+                           bc_std=1.0 / 16 if bc == "fixed" else 1.0)
+    x = workloads.make_inputs(w)
+    dev = _to_dev(x)
+    nu = api.normalise(*(dev[k] for k in NAMES))
+    out = torch.empty(nu[0].shape, dtype=nu[0].dtype, device="cuda")
+    lst = torch.empty(b, d, n, device="cuda") if last else None
+    p = api.make_params(*nu, True, out, lst)
+    ws = api.attach_workspace(p, out.device)
+    assert ws is not None and p.workspace_bytes > 0, "expected a segmented schedule"
+    import ctypes
+    assert api.load_library().ss_fwd(ctypes.byref(p), torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    _check_full(w, x, out, lst)
+    monkeypatch.setenv("SSFWD_NO_SEGMENTS", "1")
+    o1, l1 = _run(x, dev)
+    scale = float(o1.float().abs().max())
+    assert float((out.float() - o1.float()).abs().max()) <= TOL[dt] * scale
+    if last:
+        assert float((lst - l1).abs().max()) <= TOL[dt] * float(l1.abs().max())
