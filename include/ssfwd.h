@@ -60,7 +60,8 @@ typedef enum ss_status {
   SS_ERR_UNSUPPORTED = 7,  /* dstate > 64, or a feature this build lacks      */
   SS_ERR_CUDA = 8,         /* a CUDA runtime/driver call failed               */
   SS_ERR_INTERNAL = 9,     /* a device-side self-check tripped                */
-  SS_ERR_VERSION = 10      /* params->abi_version != SS_ABI_VERSION           */
+  SS_ERR_VERSION = 10,     /* params->abi_version != SS_ABI_VERSION           */
+  SS_ERR_SCRATCH = 11      /* ss_fwd_noalloc: needs more than SS_NOALLOC_MAX_SCRATCH */
 } ss_status;
 
 /*
@@ -147,6 +148,34 @@ int ss_fwd_host(const ss_fwd_params *p,
                 const void *h_B, const void *h_C,
                 const float *h_A, const float *h_D, const float *h_delta_bias,
                 void *h_out, float *h_last_state, void *stream);
+
+/*
+ * Allocation-free variant of ss_fwd, for callers that cannot allocate device
+ * memory: for instance code running where device allocation is forbidden or
+ * unavailable (an inference runtime that owns all device memory and hands
+ * out only input/output buffers, or a plugin inside another framework's
+ * allocator). It has no counterpart in the pages describing the operator; it
+ * is the same forward, including the split-sequence schedule, with that
+ * schedule's segment summaries kept in a static device buffer of
+ * SS_NOALLOC_MAX_SCRATCH bytes that the library carries on every device
+ * (held until the process exits) instead of a caller workspace.
+ *
+ *  - p->workspace / p->workspace_bytes are ignored; inputs and outputs are
+ *    the caller's device buffers as for ss_fwd. Nothing is allocated: no
+ *    cudaMalloc, cudaFree or allocating library call.
+ *  - A problem whose schedule needs more scratch than the buffer holds is
+ *    rejected with SS_ERR_SCRATCH before anything is enqueued (ss_fwd with a
+ *    workspace handles it).
+ *  - The first call on a device looks up the buffer's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture on the device.
+ *  - All calls share the one buffer and it keeps the previous call's
+ *    contents. Each call writes every summary it later reads, so nothing needs
+ *    clearing, but calls whose work overlaps on the GPU (e.g. concurrent
+ *    streams) race on it: serialise them.
+ */
+#define SS_NOALLOC_MAX_SCRATCH (2 * 1024 * 1024)
+int ss_fwd_noalloc(const ss_fwd_params *p, void *stream);
 
 /*
  * Device-side error word of the library on the current device (nonzero after

@@ -77,6 +77,8 @@ def load_library():
             lib.ss_fwd_validate.restype = ctypes.c_int
             lib.ss_fwd.argtypes = [P, vp]
             lib.ss_fwd.restype = ctypes.c_int
+            lib.ss_fwd_noalloc.argtypes = [P, vp]
+            lib.ss_fwd_noalloc.restype = ctypes.c_int
             lib.ss_fwd_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
             lib.ss_fwd_workspace_size.restype = ctypes.c_int
             lib.ss_fwd_host.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]

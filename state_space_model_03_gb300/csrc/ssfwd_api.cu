@@ -399,6 +399,29 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free entry point (ss_fwd_noalloc)
+// ---------------------------------------------------------------------------
+// Scratch for callers that cannot allocate device memory: a fixed buffer that
+// is part of the loaded library image on every device (held until exit). Only
+// the segment summaries of the split-sequence schedule live here.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SS_NOALLOC_MAX_SCRATCH];
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on `dev` (which must be current): the
+// name itself is only a host-side stand-in, so the address is looked up once
+// per device and cached.
+void *noalloc_scratch(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_noalloc_ptr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  return g_noalloc_ptr[dev];
+}
+
 // The host-staged entry point copies whole tensors, so the device buffers must
 // be laid out contiguously (a dimension of extent 1 may carry any stride).
 bool contiguous(const int64_t *sizes, const int64_t *strides, int nd) {
@@ -447,6 +470,9 @@ const char *ss_status_string(int s) {
     case SS_ERR_CUDA: return "a CUDA call failed";
     case SS_ERR_INTERNAL: return "a device-side self-check failed";
     case SS_ERR_VERSION: return "ABI version mismatch";
+    case SS_ERR_SCRATCH:
+      return "the problem needs more scratch than ss_fwd_noalloc's static buffer holds "
+             "(SS_NOALLOC_MAX_SCRATCH bytes); call ss_fwd with a workspace instead";
     default: return "unknown status";
   }
 }
@@ -465,6 +491,25 @@ int ss_fwd(const ss_fwd_params *p, void *stream) {
   int st = validate(p);
   if (st != SS_OK) return st;
   return launch(p, static_cast<cudaStream_t>(stream), p->workspace, p->workspace_bytes);
+}
+
+int ss_fwd_noalloc(const ss_fwd_params *p, void *stream) {
+  int st = validate(p);
+  if (st != SS_OK) return st;
+  int64_t need = 0;
+  st = workspace_bytes(p, &need);
+  if (st != SS_OK) return st;
+  if (need > SS_NOALLOC_MAX_SCRATCH) return SS_ERR_SCRATCH;
+  void *ws = nullptr;
+  if (need > 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+    ws = noalloc_scratch(dev);
+    if (!ws) return SS_ERR_CUDA;
+  }
+  // The summaries are fully written by the summary pass before the forward
+  // pass reads them, so the buffer needs no clearing between calls.
+  return launch(p, static_cast<cudaStream_t>(stream), ws, need);
 }
 
 int ss_fwd_host(const ss_fwd_params *p, const void *h_u, const void *h_delta, const void *h_z, const void *h_B,

@@ -30,14 +30,14 @@ def _declared_functions():
 def test_exports_every_declared_symbol(lib):
     names = _declared_functions()
     assert set(names) == {"ss_abi_version", "ss_status_string", "ss_fwd_validate", "ss_fwd",
-                          "ss_fwd_host", "ss_device_error", "ss_fwd_workspace_size"}
+                          "ss_fwd_host", "ss_device_error", "ss_fwd_workspace_size", "ss_fwd_noalloc"}
     for n in names:
         assert hasattr(lib, n), n
 
 
 def test_abi_version_and_strings(lib):
     assert lib.ss_abi_version() == api.SS_ABI_VERSION
-    for s in range(0, 11):
+    for s in range(0, 12):
         assert api.status_string(s) and api.status_string(s) != "unknown status"
     assert api.status_string(99) == "unknown status"
 
