@@ -139,6 +139,22 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+def max_over_ranks(values, world, device=None):
+    """Element-wise max of per-rank timings (one tiny all-reduce of the
+    timings themselves; the selective scan has no data-path collective)."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job rate: every rank processes its own copy of the workload
+    (weak scaling), in the slowest rank's time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def _oracle_rows_rate(w, x, rows, threads):
     import oracle
     t0 = time.perf_counter()
@@ -264,13 +280,10 @@ def run_ours(args, rank, world, local_rank):
     kms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(kms) / len(kms)
     region_ms = region0.elapsed_time(region1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms, region_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, region_ms = float(t[0]), float(t[1])
+    ms, region_ms = max_over_ranks([ms, region_ms], world, dev)
     cb = workloads.compulsory_bytes(w)
-    gbs = world * cb / (ms * 1e-3) / 1e9
-    elems = world * w.elems / (ms * 1e-3)
+    gbs = job_rate(cb, world, ms) / 1e9
+    elems = job_rate(w.elems, world, ms)
     peak, peak_src = _peaks()
     clocks = clk.summary()
 
@@ -291,11 +304,7 @@ def run_ours(args, rank, world, local_rank):
         runner.enqueue(**hx)
     e1.record(runner.stream)
     runner.stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], world, dev)[0]
 
     if rank != 0:
         return
@@ -323,7 +332,7 @@ def run_ours(args, rank, world, local_rank):
                       "fp32_lanes_per_sm_clk": 128, "sms": nsm, "sm_mhz": sm_mhz,
                       "floor_ms": alu_floor_s * 1e3,
                       "gbs_at_floor": cb / alu_floor_s / 1e9},
-        "e2e": {"value": world * cb / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": job_rate(cb, world, e2e_ms) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
                 "steps": e2e_steps},
         "gpu_launches": args.steps * launches_per_step,
