@@ -20,7 +20,10 @@ import threading
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libssfwd.so")
+# SSFWD_LIBRARY may point at another build of the same library (e.g. one built
+# with different compile-time knobs); default: the in-tree build.
+_LIB_PATH = os.environ.get("SSFWD_LIBRARY") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "_build", "libssfwd.so")
 _lock = threading.Lock()
 _lib = None
 

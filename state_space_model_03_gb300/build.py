@@ -25,22 +25,25 @@ FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-li
 def _stale(obj: str, src: str) -> bool:
     if not os.path.exists(obj):
         return True
-    deps = [src] + [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "ssfwd.h")]
+    deps = [src] + [os.path.join(os.path.dirname(src), h) for h in HEADERS] + [os.path.join(ROOT, "include", "ssfwd.h")]
     return any(os.path.getmtime(d) > os.path.getmtime(obj) for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(OUT, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, out_dir: str = OUT, extra_flags=(), csrc: str = CSRC) -> str:
+    """Compile the library into out_dir/libssfwd.so from the sources in csrc;
+    extra_flags (e.g. -D knobs) are passed to every nvcc compile."""
+    os.makedirs(out_dir, exist_ok=True)
+    lib = os.path.join(out_dir, "libssfwd.so")
     jobs = []
     for src in SOURCES:
-        s = os.path.join(CSRC, src)
-        o = os.path.join(OUT, src.replace(".cu", ".o"))
+        s = os.path.join(csrc, src)
+        o = os.path.join(out_dir, src.replace(".cu", ".o"))
         if force or _stale(o, s):
             jobs.append((s, o))
 
     def compile_one(job):
         s, o = job
-        cmd = [NVCC, *FLAGS, "-c", s, "-o", o + ".tmp"]
+        cmd = [NVCC, *FLAGS, "-I", csrc, *extra_flags, "-c", s, "-o", o + ".tmp"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {s}:\n{r.stdout}\n{r.stderr}")
@@ -51,14 +54,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if jobs:
         with ThreadPoolExecutor(len(jobs)) as ex:
             list(ex.map(compile_one, jobs))
-    objs = [os.path.join(OUT, s.replace(".cu", ".o")) for s in SOURCES]
-    if force or jobs or not os.path.exists(LIB):
-        tmp = LIB + f".tmp{os.getpid()}"
+    objs = [os.path.join(out_dir, s.replace(".cu", ".o")) for s in SOURCES]
+    if force or jobs or not os.path.exists(lib):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [NVCC, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-cudart", "static",
                "-o", tmp, *objs]
         subprocess.run(cmd, check=True, capture_output=True, text=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

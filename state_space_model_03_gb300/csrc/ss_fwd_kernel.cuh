@@ -39,6 +39,10 @@
 
 #include <type_traits>
 
+#ifndef SSK_CPL
+#define SSK_CPL 2
+#endif
+
 namespace ssk {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -305,24 +309,30 @@ __device__ __forceinline__ void stg_row(T *dst, const float (&v)[N], bool vec, i
 // ----------------------------------------------------------------------------
 // Configuration
 // ----------------------------------------------------------------------------
-template <typename T, int NP, int K, bool FIXED, bool BCF32>
+template <typename T, int NP, int K, bool FIXED, bool BCF32, int SUB = 16>
 struct Cfg {
   using BCT = typename std::conditional<BCF32, float, T>::type;  // stored B/C type (variable B/C)
   static constexpr int TN = NP / K;              // scan lanes per channel
   static constexpr int CH = 32;                  // channels per CTA
-  static constexpr int CPW = 32 / TN;            // channels per scan warp
-  static constexpr int WS = CH / CPW;            // scan warps (= TN)
+  // channels per scan lane: B/C values loaded once per step serve CPL
+  // channels (fewer shared-memory bytes and conversions per (state, step))
+  static constexpr int CPL = (TN == 1) ? 1 : SSK_CPL;
+  static constexpr int CPW = CPL * 32 / TN;      // channels per scan warp
+  static constexpr int WS = CH / CPW;            // scan warps
   static constexpr int WE = 2;                   // element warps
   static constexpr int THREADS = 32 * (WS + WE + 1);
   static constexpr int PRODUCER = WS + WE;       // warp index of the producer
   static constexpr int L = 128 / (int)sizeof(T); // steps per chunk (one 128-byte row)
-  static constexpr int S = 16;                   // steps per sub-chunk
+  static constexpr int S = SUB;                  // steps per sub-chunk (hand-off granularity)
   static constexpr int SUBS = L / S;             // sub-chunks per chunk
-  static constexpr int EPT = 8;                  // element-warp steps per lane per sub-chunk
+  static constexpr int EPT = CH * S / (WE * 32); // element-warp steps per lane per sub-chunk
   static constexpr int STAGES = 2;
   static_assert(NP % K == 0 && TN >= 1 && TN <= 8, "bad state split");
   static_assert(K % 4 == 0, "K must be a multiple of 4 (16-byte B/C loads)");
-  static_assert(CH * S == WE * 32 * EPT, "element warps cover the sub-chunk exactly");
+  static_assert(CH * S == WE * 32 * EPT && EPT >= 2, "element warps cover the sub-chunk exactly");
+  static_assert(L % S == 0, "sub-chunks tile the chunk");
+  static_assert(CPL == 1 || CPL == 2, "one or two channels per scan lane");
+  static_assert(CPW <= CH && CH % CPW == 0, "scan warps tile the CTA's channels");
   // shared memory map (bytes); TMA tiles are 1024-aligned for the 128B swizzle
   static constexpr int TILE = CH * 128;                          // u / delta / z tile
   static constexpr int BC_ROW = L * (int)sizeof(BCT);             // bytes of one raw B/C row
@@ -357,15 +367,18 @@ struct Cfg {
 // ----------------------------------------------------------------------------
 // SUMMARY = true: the segment-summary pass (end state from a zero state and
 // the sum of dt over the segment, written to p.ws; no outputs).
-template <typename T, int NP, int K, bool FIXED, bool BCF32, bool USE_TMA, bool SUMMARY>
-__global__ void __launch_bounds__(Cfg<T, NP, K, FIXED, BCF32>::THREADS, Cfg<T, NP, K, FIXED, BCF32>::MINB)
+// SUB: steps per hand-off between element and scan warps. 8 halves the
+// hand-off buffers (a fourth CTA fits per SM on 16-bit inputs) at the cost of
+// twice the hand-offs; the host picks it only when that occupancy is needed.
+template <typename T, int NP, int K, bool FIXED, bool BCF32, bool USE_TMA, bool SUMMARY, int SUB = 16>
+__global__ void __launch_bounds__(Cfg<T, NP, K, FIXED, BCF32, SUB>::THREADS, Cfg<T, NP, K, FIXED, BCF32, SUB>::MINB)
 ss_fwd_kernel(const __grid_constant__ KParams p,
               const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
               const __grid_constant__ CUtensorMap tm_C) {
-  using CF = Cfg<T, NP, K, FIXED, BCF32>;
+  using CF = Cfg<T, NP, K, FIXED, BCF32, SUB>;
   using BCT = typename CF::BCT;
-  constexpr int TN = CF::TN, CPW = CF::CPW, CH = CF::CH, L = CF::L, S = CF::S, SUBS = CF::SUBS;
+  constexpr int TN = CF::TN, CPW = CF::CPW, CPL = CF::CPL, CH = CF::CH, L = CF::L, S = CF::S, SUBS = CF::SUBS;
   constexpr int STAGES = CF::STAGES, WS = CF::WS, WE = CF::WE, EPT = CF::EPT;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-align the base by an offset from the __shared__ array itself, so the
@@ -541,12 +554,26 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         for (int it = le; it < 2 * NP; it += WE * 32) {
           const int hh = it & 1, m = (it >> 1) % (NP / 2), tensor = (it >> 1) / (NP / 2);
           const unsigned char *raw = tensor ? scr : sbr;
-          const int col = sub * S + hh * EPT;  // EPT 16-bit values = one 16-byte chunk
+          const int col = sub * S + hh * EPT;  // EPT 16-bit values: inside one 16-byte chunk
           const int n = 2 * m;
-          uint4 r0 = make_uint4(0, 0, 0, 0), r1 = make_uint4(0, 0, 0, 0);
-          if (n < nrow_bc) r0 = *reinterpret_cast<const uint4 *>(raw + swz(n, col * 2));
-          if (n + 1 < nrow_bc) r1 = *reinterpret_cast<const uint4 *>(raw + swz(n + 1, col * 2));
-          const uint32_t a[4] = {r0.x, r0.y, r0.z, r0.w}, bb[4] = {r1.x, r1.y, r1.z, r1.w};
+          uint32_t a[EPT / 2], bb[EPT / 2];
+#pragma unroll
+          for (int k = 0; k < EPT / 2; ++k) a[k] = bb[k] = 0u;
+          auto load_row = [&](int row, uint32_t (&v)[EPT / 2]) {
+            const unsigned char *src = raw + swz(row, col * 2);
+            if constexpr (EPT == 8) {
+              const uint4 r = *reinterpret_cast<const uint4 *>(src);
+              v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+            } else if constexpr (EPT == 4) {
+              const uint2 r = *reinterpret_cast<const uint2 *>(src);
+              v[0] = r.x; v[1] = r.y;
+            } else {
+#pragma unroll
+              for (int k = 0; k < EPT / 2; ++k) v[k] = reinterpret_cast<const uint32_t *>(src)[k];
+            }
+          };
+          if (n < nrow_bc) load_row(n, a);
+          if (n + 1 < nrow_bc) load_row(n + 1, bb);
           const int grp = n / K, wi = (n % K) / 2 + (tensor ? K / 2 : 0);
           uint32_t *dst = bcw + (hh * EPT) * NP + grp * K + wi;
 #pragma unroll
@@ -656,55 +683,60 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   }
 
   // ==========================================================================
-  // Scan warps: the recurrence, K states per lane, TN lanes per channel
+  // Scan warps: the recurrence, K states of CPL channels per lane
   // ==========================================================================
-  const int cl = lane / TN;          // channel within warp
+  const int cl = lane / TN;          // channel group within warp
   const int j = lane - cl * TN;      // state group within channel
-  const int c = warp * CPW + cl;     // channel within CTA
-  const int dloc = tile * CH + c;    // channel within group
-  const bool ch_ok = (dloc < p.dpg);
-  const int d = ch_ok ? d0 + c : d0;  // clamp for parameter loads
+  const int cbase = warp * CPW + cl * CPL;  // first of my CPL adjacent channels
   const int n0 = j * K;
-
-  float a2[K];
-  f2 cb2[K / 2];  // fixed B/C: C*B per state pair
-  float bfix[K];  // fixed B/C: B per state (for last_state)
+  bool ch_ok[CPL];
+  int dch[CPL];
+  f2 a2p[CPL][K / 2];
+  f2 cb2[CPL][K / 2];   // fixed B/C: C*B per state pair
+  float bfix[CPL][K];   // fixed B/C: B per state (for last_state)
+  f2 x2[CPL][K / 2];
 #pragma unroll
-  for (int k = 0; k < K; ++k) {
-    const int n = n0 + k;
-    a2[k] = (n < p.dstate) ? p.A[(long long)d * p.sA[0] + n] * kLog2e : 0.f;
-    if constexpr (FIXED) {
-      float bv = 0.f, cv = 0.f;
-      if (n < p.dstate) {
-        bv = static_cast<const float *>(p.B)[(long long)d * p.sB[0] + n];
-        cv = static_cast<const float *>(p.C)[(long long)d * p.sC[0] + n];
+  for (int i = 0; i < CPL; ++i) {
+    const int c = cbase + i;
+    ch_ok[i] = (tile * CH + c) < p.dpg;
+    dch[i] = ch_ok[i] ? d0 + c : d0;  // clamp for parameter loads
+    float a2[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int n = n0 + k;
+      a2[k] = (n < p.dstate) ? p.A[(long long)dch[i] * p.sA[0] + n] * kLog2e : 0.f;
+      if constexpr (FIXED) {
+        float bv = 0.f, cv = 0.f;
+        if (n < p.dstate) {
+          bv = static_cast<const float *>(p.B)[(long long)dch[i] * p.sB[0] + n];
+          cv = static_cast<const float *>(p.C)[(long long)dch[i] * p.sC[0] + n];
+        }
+        bfix[i][k] = bv;
+        if (k & 1) cb2[i][k / 2] = pk(upk(cb2[i][k / 2]).x, cv * bv);
+        else cb2[i][k / 2] = pk(cv * bv, 0.f);
       }
-      bfix[k] = bv;
-      if (k & 1) cb2[k / 2] = pk(upk(cb2[k / 2]).x, cv * bv);
-      else cb2[k / 2] = pk(cv * bv, 0.f);
     }
-  }
-  f2 a2p[K / 2];
 #pragma unroll
-  for (int k = 0; k < K / 2; ++k) a2p[k] = pk(a2[2 * k], a2[2 * k + 1]);
-  f2 x2[K / 2];
+    for (int k = 0; k < K / 2; ++k) {
+      a2p[i][k] = pk(a2[2 * k], a2[2 * k + 1]);
+      x2[i][k] = pk(0.f, 0.f);
+    }
+    if (!SUMMARY && seg > 0) {
+      // carry-in: fold the summaries of segments 0..seg-1 (state after segment
+      // k from state x: exp(A * sum dt) x + end state from zero)
+      const long long row_bd = (long long)b * p.dim + dch[i];
+      const float *wsx = p.ws + row_bd * nsum * NP;
+      const float *wsl = p.ws + (long long)nsum * NP * p.batch * p.dim + row_bd * nsum;
+      for (int kseg = 0; kseg < seg; ++kseg) {
+        const float lk = wsl[kseg];
+        const f2 l2 = pk(lk, lk);
 #pragma unroll
-  for (int k = 0; k < K / 2; ++k) x2[k] = pk(0.f, 0.f);
-  const long long row_bd = (long long)b * p.dim + d;
-  if (!SUMMARY && seg > 0) {
-    // carry-in: fold the summaries of segments 0..seg-1 (state after segment
-    // k from state x: exp(A * sum dt) x + end state from zero)
-    const float *wsx = p.ws + row_bd * nsum * NP;
-    const float *wsl = p.ws + (long long)nsum * NP * p.batch * p.dim + row_bd * nsum;
-    for (int kseg = 0; kseg < seg; ++kseg) {
-      const float lk = wsl[kseg];
-      const f2 l2 = pk(lk, lk);
-#pragma unroll
-      for (int k = 0; k < K / 2; ++k) {
-        const float2 e = upk(mul2(l2, a2p[k]));
-        const f2 dec = pk(ex2(e.x), ex2(e.y));
-        const float2 xe = *reinterpret_cast<const float2 *>(wsx + kseg * NP + n0 + 2 * k);
-        x2[k] = fma2(dec, x2[k], pk(xe.x, xe.y));
+        for (int k = 0; k < K / 2; ++k) {
+          const float2 e = upk(mul2(l2, a2p[i][k]));
+          const f2 dec = pk(ex2(e.x), ex2(e.y));
+          const float2 xe = *reinterpret_cast<const float2 *>(wsx + kseg * NP + n0 + 2 * k);
+          x2[i][k] = fma2(dec, x2[i][k], pk(xe.x, xe.y));
+        }
       }
     }
   }
@@ -719,58 +751,68 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     float *Y = reinterpret_cast<float *>(smem + CF::OFF_Y + (q & 1) * CF::Y_SLOT);
 #pragma unroll
     for (int tl = 0; tl < S; ++tl) {
-      const float2 pw = P[tl * CH + c];
-      const f2 dt2 = pk(pw.x, pw.x);
-      const f2 w2 = pk(pw.y, pw.y);
-      f2 y2 = pk(0.f, 0.f);
-      if constexpr (FIXED) {
-#pragma unroll
-        for (int k = 0; k < K / 2; ++k) {
-          const float2 e = upk(mul2(dt2, a2p[k]));
-          const f2 a = pk(ex2(e.x), ex2(e.y));
-          x2[k] = fma2(a, x2[k], w2);
-          if constexpr (!SUMMARY) y2 = fma2(cb2[k], x2[k], y2);
-        }
-      } else if constexpr (CF::BCPACK) {
-        // K/2 words of B pairs then K/2 words of C pairs (16-byte loads)
-        uint32_t wv[K];
-#pragma unroll
-        for (int q4 = 0; q4 < K / 4; ++q4) {
-          const uint4 r = *reinterpret_cast<const uint4 *>(bcw + tl * NP + n0 + 4 * q4);
-          wv[4 * q4] = r.x; wv[4 * q4 + 1] = r.y; wv[4 * q4 + 2] = r.z; wv[4 * q4 + 3] = r.w;
-        }
-#pragma unroll
-        for (int k = 0; k < K / 2; ++k) {
-          const float2 bf = unpack2<T>(wv[k]);
-          const float2 cf = unpack2<T>(wv[K / 2 + k]);
-          const float2 e = upk(mul2(dt2, a2p[k]));
-          const f2 a = pk(ex2(e.x), ex2(e.y));
-          x2[k] = fma2(a, x2[k], mul2(w2, pk(bf.x, bf.y)));
-          if constexpr (!SUMMARY) y2 = fma2(pk(cf.x, cf.y), x2[k], y2);
-        }
+      // (dt, w) of my CPL adjacent channels: one 8- or 16-byte load
+      f2 dt2[CPL], w2[CPL];
+      if constexpr (CPL == 2) {
+        const float4 pw = *reinterpret_cast<const float4 *>(P + tl * CH + cbase);
+        dt2[0] = pk(pw.x, pw.x); w2[0] = pk(pw.y, pw.y);
+        dt2[1] = pk(pw.z, pw.z); w2[1] = pk(pw.w, pw.w);
       } else {
+        const float2 pw = P[tl * CH + cbase];
+        dt2[0] = pk(pw.x, pw.x); w2[0] = pk(pw.y, pw.y);
+      }
+      // B and C of my K states at this step, as fp32 state pairs
+      f2 bp[K / 2], cp[K / 2];
+      if constexpr (!FIXED) {
+        if constexpr (CF::BCPACK) {
+          // K/2 words of B pairs then K/2 words of C pairs (16-byte loads)
+          uint32_t wv[K];
 #pragma unroll
-        for (int k = 0; k < K / 2; k += 2) {
-          // B, C for states n0+2k .. n0+2k+3 (one 16-byte load each)
-          const float4 bq = *reinterpret_cast<const float4 *>(b32 + tl * NP + n0 + 2 * k);
-          const float4 cq = *reinterpret_cast<const float4 *>(c32 + tl * NP + n0 + 2 * k);
-          {
-            const float2 e = upk(mul2(dt2, a2p[k]));
-            const f2 a = pk(ex2(e.x), ex2(e.y));
-            x2[k] = fma2(a, x2[k], mul2(w2, pk(bq.x, bq.y)));
-            if constexpr (!SUMMARY) y2 = fma2(pk(cq.x, cq.y), x2[k], y2);
+          for (int q4 = 0; q4 < K / 4; ++q4) {
+            const uint4 r = *reinterpret_cast<const uint4 *>(bcw + tl * NP + n0 + 4 * q4);
+            wv[4 * q4] = r.x; wv[4 * q4 + 1] = r.y; wv[4 * q4 + 2] = r.z; wv[4 * q4 + 3] = r.w;
           }
-          {
-            const float2 e = upk(mul2(dt2, a2p[k + 1]));
-            const f2 a = pk(ex2(e.x), ex2(e.y));
-            x2[k + 1] = fma2(a, x2[k + 1], mul2(w2, pk(bq.z, bq.w)));
-            if constexpr (!SUMMARY) y2 = fma2(pk(cq.z, cq.w), x2[k + 1], y2);
+#pragma unroll
+          for (int k = 0; k < K / 2; ++k) {
+            const float2 bf = unpack2<T>(wv[k]);
+            bp[k] = pk(bf.x, bf.y);
+            if constexpr (!SUMMARY) {
+              const float2 cf = unpack2<T>(wv[K / 2 + k]);
+              cp[k] = pk(cf.x, cf.y);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < K / 2; k += 2) {
+            // B, C for states n0+2k .. n0+2k+3 (one 16-byte load each)
+            const float4 bq = *reinterpret_cast<const float4 *>(b32 + tl * NP + n0 + 2 * k);
+            bp[k] = pk(bq.x, bq.y); bp[k + 1] = pk(bq.z, bq.w);
+            if constexpr (!SUMMARY) {
+              const float4 cq = *reinterpret_cast<const float4 *>(c32 + tl * NP + n0 + 2 * k);
+              cp[k] = pk(cq.x, cq.y); cp[k + 1] = pk(cq.z, cq.w);
+            }
           }
         }
       }
-      if constexpr (!SUMMARY) {
-        const float2 yy = upk(y2);
-        Y[tl * (CH * TN) + c * TN + j] = yy.x + yy.y;  // step-major: one 128-byte row per warp
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        f2 y2 = pk(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < K / 2; ++k) {
+          const float2 e = upk(mul2(dt2[i], a2p[i][k]));
+          const f2 a = pk(ex2(e.x), ex2(e.y));
+          if constexpr (FIXED) {
+            x2[i][k] = fma2(a, x2[i][k], w2[i]);
+            if constexpr (!SUMMARY) y2 = fma2(cb2[i][k], x2[i][k], y2);
+          } else {
+            x2[i][k] = fma2(a, x2[i][k], mul2(w2[i], bp[k]));
+            if constexpr (!SUMMARY) y2 = fma2(cp[k], x2[i][k], y2);
+          }
+        }
+        if constexpr (!SUMMARY) {
+          const float2 yy = upk(y2);
+          Y[tl * (CH * TN) + (cbase + i) * TN + j] = yy.x + yy.y;  // step-major rows
+        }
       }
     }
     __syncwarp();
@@ -782,24 +824,30 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
 
   if constexpr (SUMMARY) {
     // end state of this segment from a zero state (x, or x / B for fixed B/C)
-    if (ch_ok) {
-      float *wsx = p.ws + (row_bd * nsum + seg) * NP;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      if (!ch_ok[i]) continue;
+      float *wsx = p.ws + (((long long)b * p.dim + dch[i]) * nsum + seg) * NP;
 #pragma unroll
       for (int k = 0; k < K / 2; ++k)
-        *reinterpret_cast<float2 *>(wsx + n0 + 2 * k) = upk(x2[k]);
+        *reinterpret_cast<float2 *>(wsx + n0 + 2 * k) = upk(x2[i][k]);
     }
     return;
   }
 
-  if (p.want_last && ch_ok && seg == p.nseg - 1) {
-    float *lr = p.last + (long long)b * p.sl[0] + (long long)d * p.sl[1];
+  if (p.want_last && seg == p.nseg - 1) {
 #pragma unroll
-    for (int k = 0; k < K / 2; ++k) {
-      float2 xv = upk(x2[k]);
-      if constexpr (FIXED) { xv.x *= bfix[2 * k]; xv.y *= bfix[2 * k + 1]; }
-      const int n = n0 + 2 * k;
-      if (n < p.dstate) lr[n * p.sl[2]] = xv.x;
-      if (n + 1 < p.dstate) lr[(n + 1) * p.sl[2]] = xv.y;
+    for (int i = 0; i < CPL; ++i) {
+      if (!ch_ok[i]) continue;
+      float *lr = p.last + (long long)b * p.sl[0] + (long long)dch[i] * p.sl[1];
+#pragma unroll
+      for (int k = 0; k < K / 2; ++k) {
+        float2 xv = upk(x2[i][k]);
+        if constexpr (FIXED) { xv.x *= bfix[i][2 * k]; xv.y *= bfix[i][2 * k + 1]; }
+        const int n = n0 + 2 * k;
+        if (n < p.dstate) lr[n * p.sl[2]] = xv.x;
+        if (n + 1 < p.dstate) lr[(n + 1) * p.sl[2]] = xv.y;
+      }
     }
   }
 }

@@ -24,7 +24,8 @@ __device__ int32_t g_error_word;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int32_t *g_err_ptr[kMaxDevices] = {};
-bool g_attr_done[kMaxDevices][3][5][2][2][2][2] = {};
+bool g_attr_done[kMaxDevices][3][5][2][2][2][2][2] = {};
+int g_occupancy[kMaxDevices][3][5][2][2][2] = {};  // CTAs/SM of the TMA forward, [..][sub8]
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -153,11 +154,11 @@ int padded_states(int64_t n) {
 
 int np_index(int np) { return np == 4 ? 0 : np == 8 ? 1 : np == 16 ? 2 : np == 32 ? 3 : 4; }
 
-ssk::KernelInfo lookup(int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary) {
+ssk::KernelInfo lookup(int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8 = false) {
   switch (dt) {
-    case SS_F32: return ssk::lookup_f32(np, fixed, bc_f32, tma, summary);
-    case SS_F16: return ssk::lookup_f16(np, fixed, bc_f32, tma, summary);
-    default: return ssk::lookup_bf16(np, fixed, bc_f32, tma, summary);
+    case SS_F32: return ssk::lookup_f32(np, fixed, bc_f32, tma, summary, sub8);
+    case SS_F16: return ssk::lookup_f16(np, fixed, bc_f32, tma, summary, sub8);
+    default: return ssk::lookup_bf16(np, fixed, bc_f32, tma, summary, sub8);
   }
 }
 
@@ -275,9 +276,10 @@ SegPlan plan_segments(const ss_fwd_params *p, int np, int L, int ch, int nsm) {
   return sp;
 }
 
-bool set_smem_attr(int dev, const ssk::KernelInfo &ki, int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary) {
+bool set_smem_attr(int dev, const ssk::KernelInfo &ki, int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary,
+                   bool sub8 = false) {
   std::lock_guard<std::mutex> lk(g_mu);
-  bool &done = g_attr_done[dev][dt][np_index(np)][fixed][bc_f32 && !fixed][tma][summary];
+  bool &done = g_attr_done[dev][dt][np_index(np)][fixed][bc_f32 && !fixed][tma][summary][sub8];
   if (!done) {
     if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) != cudaSuccess)
       return false;
@@ -375,6 +377,34 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   if (!tma) ki = lookup(p->in_dtype, np, fixed, bc_f32, false, false);
   if (!ki.fn) return SS_ERR_UNSUPPORTED;
   if (!set_smem_attr(dev, ki, p->in_dtype, np, fixed, bc_f32, tma, false)) return SS_ERR_CUDA;
+  const unsigned gx = static_cast<unsigned>(kp.tiles_per_group * kp.ngroups), gy = static_cast<unsigned>(kp.batch);
+  bool sub8 = false;
+  if (tma && !std::getenv("SSFWD_NO_SUB8")) {
+    // More CTAs than the 16-step kernel keeps resident: use 8-step hand-offs
+    // if their smaller buffers let all CTAs be resident at once.
+    const int64_t ctas = int64_t(gx) * gy * sp.nseg;
+    const int nsm = num_sms(dev);
+    ssk::KernelInfo k8 = lookup(p->in_dtype, np, fixed, bc_f32, true, false, true);
+    if (k8.fn && nsm > 0) {
+      if (!set_smem_attr(dev, k8, p->in_dtype, np, fixed, bc_f32, true, false, true)) return SS_ERR_CUDA;
+      int occ[2] = {0, 0};
+      {
+        std::lock_guard<std::mutex> lk(g_mu);
+        int *slot = g_occupancy[dev][p->in_dtype][np_index(np)][fixed][bc_f32 && !fixed];
+        const ssk::KernelInfo *ks[2] = {&ki, &k8};
+        for (int v = 0; v < 2; ++v) {
+          if (!slot[v] && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&slot[v], ks[v]->fn, ks[v]->threads,
+                                                                        ks[v]->smem) != cudaSuccess)
+            slot[v] = 0;
+          occ[v] = slot[v];
+        }
+      }
+      if (occ[0] > 0 && ctas > int64_t(occ[0]) * nsm && int64_t(occ[1]) * nsm >= ctas) {
+        ki = k8;
+        sub8 = true;
+      }
+    }
+  }
   ssk::KernelInfo ks{};
   if (sp.nseg > 1) {
     ks = lookup(p->in_dtype, np, fixed, bc_f32, tma, true);
@@ -382,12 +412,11 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
     if (!set_smem_attr(dev, ks, p->in_dtype, np, fixed, bc_f32, tma, true)) return SS_ERR_CUDA;
   }
   if (fault_injected("launch")) return SS_ERR_CUDA;
-  const unsigned gx = static_cast<unsigned>(kp.tiles_per_group * kp.ngroups), gy = static_cast<unsigned>(kp.batch);
   if (std::getenv("SSFWD_DEBUG"))  // opt-in launch report on stderr
     std::fprintf(stderr,
-                 "ssfwd: %s np=%d fixed=%d bc_f32=%d ch=%d L=%d grid=%ux%ux%d seg_len=%d threads=%d smem=%d\n",
+                 "ssfwd: %s np=%d fixed=%d bc_f32=%d ch=%d L=%d grid=%ux%ux%d seg_len=%d sub=%d threads=%d smem=%d\n",
                  tma ? "tma" : "generic", np, (int)fixed, (int)bc_f32, ki.ch, ki.L, gx, gy, sp.nseg, sp.seg_len,
-                 ki.threads, ki.smem);
+                 sub8 ? 8 : 16, ki.threads, ki.smem);
   void *args[6] = {&kp, &tm[0], &tm[1], &tm[2], &tm[3], &tm[4]};
   if (sp.nseg > 1) {
     cudaError_t e = cudaLaunchKernel(ks.fn, dim3(gx, gy, sp.nseg - 1), dim3(ks.threads), args,

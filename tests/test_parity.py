@@ -116,6 +116,8 @@ SWEEP = [
     (1, 40, 100, 3, 1, "fixed", "fp16", None, True, False, False, True, True),
     (1, 8, 64, 64, 1, "fixed", "fp32", None, True, True, True, True, True),
     (3, 5, 70, 16, 1, "variable", "fp32", None, True, True, True, True, False),
+    # more CTAs than the 16-step kernel keeps resident: 8-step hand-offs
+    (4, 4096, 200, 16, 4, "variable", "bf16", None, True, True, True, True, True),
 ]
 
 
@@ -284,3 +286,17 @@ def test_segmented_sequence(case, monkeypatch):
     assert float((out.float() - o1.float()).abs().max()) <= TOL[dt] * scale
     if last:
         assert float((lst - l1).abs().max()) <= TOL[dt] * float(l1.abs().max())
+
+
+def test_eight_step_handoffs_agree(monkeypatch):
+    """A grid larger than the 16-step kernel's resident CTAs runs with 8-step
+    hand-offs; it must agree with the 16-step schedule up to rounding."""
+    w = workloads.Workload("sub8", 4, 4096, 300, 16, groups=4, bc_4d=True, dtype="bf16",
+                           return_last_state=True, seed=31)
+    x = workloads.make_inputs(w)
+    dev = _to_dev(x)
+    o8, l8 = _run(x, dev)
+    monkeypatch.setenv("SSFWD_NO_SUB8", "1")
+    o16, l16 = _run(x, dev)
+    assert float((o8.float() - o16.float()).abs().max()) <= 1e-2 * float(o16.float().abs().max())
+    assert float((l8 - l16).abs().max()) <= 1e-5 * float(l16.abs().max())
