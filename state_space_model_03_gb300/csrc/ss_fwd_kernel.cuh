@@ -309,17 +309,17 @@ __device__ __forceinline__ void stg_row(T *dst, const float (&v)[N], bool vec, i
 // ----------------------------------------------------------------------------
 // Configuration
 // ----------------------------------------------------------------------------
-template <typename T, int NP, int K, bool FIXED, bool BCF32, int SUB = 16>
+template <typename T, int NP, int K, bool FIXED, bool BCF32, int SUB = 16, int CHN = 32>
 struct Cfg {
   using BCT = typename std::conditional<BCF32, float, T>::type;  // stored B/C type (variable B/C)
   static constexpr int TN = NP / K;              // scan lanes per channel
-  static constexpr int CH = 32;                  // channels per CTA
+  static constexpr int CH = CHN;                 // channels per CTA (32, or 16 for finer balance)
   // channels per scan lane: B/C values loaded once per step serve CPL
   // channels (fewer shared-memory bytes and conversions per (state, step))
   static constexpr int CPL = (TN == 1) ? 1 : SSK_CPL;
   static constexpr int CPW = CPL * 32 / TN;      // channels per scan warp
   static constexpr int WS = CH / CPW;            // scan warps
-  static constexpr int WE = 2;                   // element warps
+  static constexpr int WE = CH / 16;             // element warps (two lanes per channel)
   static constexpr int THREADS = 32 * (WS + WE + 1);
   static constexpr int PRODUCER = WS + WE;       // warp index of the producer
   static constexpr int L = 128 / (int)sizeof(T); // steps per chunk (one 128-byte row)
@@ -370,13 +370,15 @@ struct Cfg {
 // SUB: steps per hand-off between element and scan warps. 8 halves the
 // hand-off buffers (a fourth CTA fits per SM on 16-bit inputs) at the cost of
 // twice the hand-offs; the host picks it only when that occupancy is needed.
-template <typename T, int NP, int K, bool FIXED, bool BCF32, bool USE_TMA, bool SUMMARY, int SUB = 16>
-__global__ void __launch_bounds__(Cfg<T, NP, K, FIXED, BCF32, SUB>::THREADS, Cfg<T, NP, K, FIXED, BCF32, SUB>::MINB)
+// CHN: channels per CTA; 16 gives twice the CTAs for a finer spread over SMs.
+template <typename T, int NP, int K, bool FIXED, bool BCF32, bool USE_TMA, bool SUMMARY, int SUB = 16, int CHN = 32>
+__global__ void __launch_bounds__(Cfg<T, NP, K, FIXED, BCF32, SUB, CHN>::THREADS,
+                                  Cfg<T, NP, K, FIXED, BCF32, SUB, CHN>::MINB)
 ss_fwd_kernel(const __grid_constant__ KParams p,
               const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
               const __grid_constant__ CUtensorMap tm_C) {
-  using CF = Cfg<T, NP, K, FIXED, BCF32, SUB>;
+  using CF = Cfg<T, NP, K, FIXED, BCF32, SUB, CHN>;
   using BCT = typename CF::BCT;
   constexpr int TN = CF::TN, CPW = CF::CPW, CPL = CF::CPL, CH = CF::CH, L = CF::L, S = CF::S, SUBS = CF::SUBS;
   constexpr int STAGES = CF::STAGES, WS = CF::WS, WE = CF::WE, EPT = CF::EPT;

@@ -24,8 +24,8 @@ __device__ int32_t g_error_word;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int32_t *g_err_ptr[kMaxDevices] = {};
-bool g_attr_done[kMaxDevices][3][5][2][2][2][2][2] = {};
-int g_occupancy[kMaxDevices][3][5][2][2][2] = {};  // CTAs/SM of the TMA forward, [..][sub8]
+bool g_attr_done[kMaxDevices][3][5][2][2][2][2][2][2] = {};
+int g_occupancy[kMaxDevices][3][5][2][2][4] = {};  // CTAs/SM of the TMA forward, [..][sub8 | ch16 << 1]
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -154,11 +154,12 @@ int padded_states(int64_t n) {
 
 int np_index(int np) { return np == 4 ? 0 : np == 8 ? 1 : np == 16 ? 2 : np == 32 ? 3 : 4; }
 
-ssk::KernelInfo lookup(int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8 = false) {
+ssk::KernelInfo lookup(int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8 = false,
+                       bool ch16 = false) {
   switch (dt) {
-    case SS_F32: return ssk::lookup_f32(np, fixed, bc_f32, tma, summary, sub8);
-    case SS_F16: return ssk::lookup_f16(np, fixed, bc_f32, tma, summary, sub8);
-    default: return ssk::lookup_bf16(np, fixed, bc_f32, tma, summary, sub8);
+    case SS_F32: return ssk::lookup_f32(np, fixed, bc_f32, tma, summary, sub8, ch16);
+    case SS_F16: return ssk::lookup_f16(np, fixed, bc_f32, tma, summary, sub8, ch16);
+    default: return ssk::lookup_bf16(np, fixed, bc_f32, tma, summary, sub8, ch16);
   }
 }
 
@@ -277,9 +278,9 @@ SegPlan plan_segments(const ss_fwd_params *p, int np, int L, int ch, int nsm) {
 }
 
 bool set_smem_attr(int dev, const ssk::KernelInfo &ki, int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary,
-                   bool sub8 = false) {
+                   bool sub8 = false, bool ch16 = false) {
   std::lock_guard<std::mutex> lk(g_mu);
-  bool &done = g_attr_done[dev][dt][np_index(np)][fixed][bc_f32 && !fixed][tma][summary][sub8];
+  bool &done = g_attr_done[dev][dt][np_index(np)][fixed][bc_f32 && !fixed][tma][summary][sub8][ch16];
   if (!done) {
     if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) != cudaSuccess)
       return false;
@@ -355,7 +356,8 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   kp.sA[0] = p->A_stride[0]; kp.sA[1] = p->A_stride[1];
   kp.err = err;
 
-  SegPlan sp = plan_segments(p, np, ki.L, ki.ch, num_sms(dev));
+  const int nsm = num_sms(dev);
+  SegPlan sp = plan_segments(p, np, ki.L, ki.ch, nsm);
   if (sp.nseg > 1 && (!ws || ws_bytes < sp.ws_bytes || !aligned(ws, 16) || std::getenv("SSFWD_NO_SEGMENTS"))) {
     sp.nseg = 1;  // no (or too small a) workspace: single pass over the whole sequence
     sp.seg_len = kp.seqlen;
@@ -366,63 +368,86 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
 
   // TMA when every streamed tensor has a legal descriptor; else the generic
   // (plain-load) producer with the same compute path.
-  CUtensorMap tm[5];
-  std::memset(tm, 0, sizeof(tm));
-  bool tma = g_encode != nullptr && !std::getenv("SSFWD_NO_TMA");
-  if (tma) tma = make_map3(&tm[0], p->u, es, p, p->u_stride, ki.L, ki.ch);
-  if (tma) tma = make_map3(&tm[1], p->delta, es, p, p->delta_stride, ki.L, ki.ch);
-  if (tma && p->z) tma = make_map3(&tm[2], p->z, es, p, p->z_stride, ki.L, ki.ch);
-  if (tma && !fixed) tma = make_map4(&tm[3], p->B, bs, p, p->B_stride, ki.L);
-  if (tma && !fixed) tma = make_map4(&tm[4], p->C, bs, p, p->C_stride, ki.L);
-  if (!tma) ki = lookup(p->in_dtype, np, fixed, bc_f32, false, false);
-  if (!ki.fn) return SS_ERR_UNSUPPORTED;
-  if (!set_smem_attr(dev, ki, p->in_dtype, np, fixed, bc_f32, tma, false)) return SS_ERR_CUDA;
-  const unsigned gx = static_cast<unsigned>(kp.tiles_per_group * kp.ngroups), gy = static_cast<unsigned>(kp.batch);
-  bool sub8 = false;
-  if (tma && !std::getenv("SSFWD_NO_SUB8")) {
-    // More CTAs than the 16-step kernel keeps resident: use 8-step hand-offs
-    // if their smaller buffers let all CTAs be resident at once.
-    const int64_t ctas = int64_t(gx) * gy * sp.nseg;
-    const int nsm = num_sms(dev);
-    ssk::KernelInfo k8 = lookup(p->in_dtype, np, fixed, bc_f32, true, false, true);
-    if (k8.fn && nsm > 0) {
-      if (!set_smem_attr(dev, k8, p->in_dtype, np, fixed, bc_f32, true, false, true)) return SS_ERR_CUDA;
-      int occ[2] = {0, 0};
+  auto encode = [&](CUtensorMap *tm, int ch) -> bool {
+    std::memset(tm, 0, 5 * sizeof(CUtensorMap));
+    bool ok = make_map3(&tm[0], p->u, es, p, p->u_stride, ki.L, ch);
+    if (ok) ok = make_map3(&tm[1], p->delta, es, p, p->delta_stride, ki.L, ch);
+    if (ok && p->z) ok = make_map3(&tm[2], p->z, es, p, p->z_stride, ki.L, ch);
+    if (ok && !fixed) ok = make_map4(&tm[3], p->B, bs, p, p->B_stride, ki.L);
+    if (ok && !fixed) ok = make_map4(&tm[4], p->C, bs, p, p->C_stride, ki.L);
+    return ok;
+  };
+  CUtensorMap tm[5], tm_sum[5];
+  bool tma = g_encode != nullptr && !std::getenv("SSFWD_NO_TMA") && encode(tm_sum, ki.ch);
+  const int groups = kp.ngroups;
+  // Forward variant: CTA width (32 or 16 channels) x hand-off length (16 or
+  // 8 steps). Cost model: per-SM CTA load (in CTA waves when more CTAs than
+  // resident slots) x channels per CTA x a measured per-variant overhead.
+  bool sub8 = false, ch16 = false;
+  if (tma) {
+    double best = 0.0;
+    ssk::KernelInfo bestk = ki;
+    for (int v = 0; v < 4; ++v) {
+      const bool v8 = v & 1, v16 = v & 2;
+      if (v16 && std::getenv("SSFWD_NO_CH16")) continue;
+      if (v8 && std::getenv("SSFWD_NO_SUB8")) continue;
+      ssk::KernelInfo kv = lookup(p->in_dtype, np, fixed, bc_f32, true, false, v8, v16);
+      if (!kv.fn) continue;
+      if (!set_smem_attr(dev, kv, p->in_dtype, np, fixed, bc_f32, true, false, v8, v16)) return SS_ERR_CUDA;
+      int occ = 0;
       {
         std::lock_guard<std::mutex> lk(g_mu);
-        int *slot = g_occupancy[dev][p->in_dtype][np_index(np)][fixed][bc_f32 && !fixed];
-        const ssk::KernelInfo *ks[2] = {&ki, &k8};
-        for (int v = 0; v < 2; ++v) {
-          if (!slot[v] && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&slot[v], ks[v]->fn, ks[v]->threads,
-                                                                        ks[v]->smem) != cudaSuccess)
-            slot[v] = 0;
-          occ[v] = slot[v];
-        }
+        int &slot = g_occupancy[dev][p->in_dtype][np_index(np)][fixed][bc_f32 && !fixed][v];
+        if (!slot && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&slot, kv.fn, kv.threads, kv.smem) != cudaSuccess)
+          slot = 0;
+        occ = slot;
       }
-      if (occ[0] > 0 && ctas > int64_t(occ[0]) * nsm && int64_t(occ[1]) * nsm >= ctas) {
-        ki = k8;
-        sub8 = true;
+      if (occ <= 0 || nsm <= 0) continue;
+      const int64_t ctas = int64_t((kp.dpg + kv.ch - 1) / kv.ch) * groups * kp.batch * sp.nseg;
+      const int64_t per_sm = (ctas + nsm - 1) / nsm;
+      const int64_t load = per_sm <= occ ? per_sm : (ctas + int64_t(occ) * nsm - 1) / (int64_t(occ) * nsm) * occ;
+      const double cost = double(load) * kv.ch * (v8 ? 1.06 : 1.0) * (v16 ? 1.16 : 1.0);
+      if (v == 0 || cost < best) {
+        best = cost;
+        bestk = kv;
+        sub8 = v8;
+        ch16 = v16;
       }
     }
+    ki = bestk;
+    if (ch16 && !encode(tm, ki.ch)) return SS_ERR_INTERNAL;
+    if (!ch16) std::memcpy(tm, tm_sum, sizeof(tm));
+  } else {
+    ki = lookup(p->in_dtype, np, fixed, bc_f32, false, false);
+    if (!ki.fn) return SS_ERR_UNSUPPORTED;
+    if (!set_smem_attr(dev, ki, p->in_dtype, np, fixed, bc_f32, false, false)) return SS_ERR_CUDA;
+    std::memset(tm, 0, sizeof(tm));
+    std::memset(tm_sum, 0, sizeof(tm_sum));
   }
+  kp.tiles_per_group = (kp.dpg + ki.ch - 1) / ki.ch;
+  ssk::KParams kps = kp;  // summary pass: 32-channel CTAs
   ssk::KernelInfo ks{};
   if (sp.nseg > 1) {
     ks = lookup(p->in_dtype, np, fixed, bc_f32, tma, true);
     if (!ks.fn) return SS_ERR_UNSUPPORTED;
     if (!set_smem_attr(dev, ks, p->in_dtype, np, fixed, bc_f32, tma, true)) return SS_ERR_CUDA;
+    kps.tiles_per_group = (kp.dpg + ks.ch - 1) / ks.ch;
   }
   if (fault_injected("launch")) return SS_ERR_CUDA;
+  const unsigned gx = static_cast<unsigned>(kp.tiles_per_group * kp.ngroups), gy = static_cast<unsigned>(kp.batch);
   if (std::getenv("SSFWD_DEBUG"))  // opt-in launch report on stderr
     std::fprintf(stderr,
                  "ssfwd: %s np=%d fixed=%d bc_f32=%d ch=%d L=%d grid=%ux%ux%d seg_len=%d sub=%d threads=%d smem=%d\n",
                  tma ? "tma" : "generic", np, (int)fixed, (int)bc_f32, ki.ch, ki.L, gx, gy, sp.nseg, sp.seg_len,
                  sub8 ? 8 : 16, ki.threads, ki.smem);
-  void *args[6] = {&kp, &tm[0], &tm[1], &tm[2], &tm[3], &tm[4]};
   if (sp.nseg > 1) {
-    cudaError_t e = cudaLaunchKernel(ks.fn, dim3(gx, gy, sp.nseg - 1), dim3(ks.threads), args,
+    void *sargs[6] = {&kps, &tm_sum[0], &tm_sum[1], &tm_sum[2], &tm_sum[3], &tm_sum[4]};
+    const unsigned sx = static_cast<unsigned>(kps.tiles_per_group * kps.ngroups);
+    cudaError_t e = cudaLaunchKernel(ks.fn, dim3(sx, gy, sp.nseg - 1), dim3(ks.threads), sargs,
                                      static_cast<size_t>(ks.smem), stream);
     if (e != cudaSuccess) return SS_ERR_CUDA;
   }
+  void *args[6] = {&kp, &tm[0], &tm[1], &tm[2], &tm[3], &tm[4]};
   cudaError_t e = cudaLaunchKernel(ki.fn, dim3(gx, gy, sp.nseg), dim3(ki.threads), args,
                                    static_cast<size_t>(ki.smem), stream);
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;

@@ -118,6 +118,8 @@ SWEEP = [
     (3, 5, 70, 16, 1, "variable", "fp32", None, True, True, True, True, False),
     # more CTAs than the 16-step kernel keeps resident: 8-step hand-offs
     (4, 4096, 200, 16, 4, "variable", "bf16", None, True, True, True, True, True),
+    # 2.1 CTAs of 32 channels per SM: 16-channel CTAs spread the work better
+    (2, 5120, 256, 16, 1, "variable", "fp16", None, True, True, True, True, True),
 ]
 
 
@@ -300,3 +302,16 @@ def test_eight_step_handoffs_agree(monkeypatch):
     o16, l16 = _run(x, dev)
     assert float((o8.float() - o16.float()).abs().max()) <= 1e-2 * float(o16.float().abs().max())
     assert float((l8 - l16).abs().max()) <= 1e-5 * float(l16.abs().max())
+
+
+def test_sixteen_channel_ctas_agree(monkeypatch):
+    """A grid of 16-channel CTAs (picked for load balance) agrees with the
+    32-channel schedule up to rounding."""
+    w = workloads.Workload("ch16", 2, 5120, 300, 16, dtype="fp16", return_last_state=True, seed=37)
+    x = workloads.make_inputs(w)
+    dev = _to_dev(x)
+    o16, l16 = _run(x, dev)
+    monkeypatch.setenv("SSFWD_NO_CH16", "1")
+    o32, l32 = _run(x, dev)
+    assert float((o16.float() - o32.float()).abs().max()) <= 1e-2 * float(o32.float().abs().max())
+    assert float((l16 - l32).abs().max()) <= 1e-5 * float(l32.abs().max())
