@@ -506,8 +506,12 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   // ==========================================================================
   if (warp >= WS) {
     const int le = (warp - WS) * 32 + lane;  // 0 .. WE*32-1
-    const int c = le >> 1;                   // channel within CTA
-    const int h = le & 1;                    // which half (EPT steps) of the sub-chunk
+    // lanes 0-7: channels 0-7 first half, 8-15: same channels second half,
+    // 16-31: channels 8-15 ...: each quarter warp reads 8 consecutive rows of a
+    // swizzled tile at one column, which the 128-byte swizzle spreads over
+    // all 32 banks.
+    const int c = (le & 7) + 8 * (le >> 4);  // channel within CTA
+    const int h = (le >> 3) & 1;             // which half (EPT steps) of the sub-chunk
     const int dloc = tile * CH + c;
     const bool ch_ok = dloc < p.dpg;
     const int d = ch_ok ? d0 + c : d0;
@@ -671,8 +675,8 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
           if (lane == 0) mbar_arrive(&bar_empty[(q / SUBS) % STAGES]);
         }
       }
-      // two lanes per channel: combine their step sums
-      lam += __shfl_xor_sync(0xffffffffu, lam, 1);
+      // the two half-lanes of a channel (8 lanes apart): combine their step sums
+      lam += __shfl_xor_sync(0xffffffffu, lam, 8);
       if (ok && h == 0 && ch_ok)
         p.ws[(long long)nsum * NP * p.batch * p.dim + ((long long)b * p.dim + d) * nsum + seg] = lam;
     } else if (nsub > 0 && prep(0)) {
@@ -751,6 +755,8 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     const float *c32 = b32 + S * NP;
     const uint32_t *bcw = reinterpret_cast<const uint32_t *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
     float *Y = reinterpret_cast<float *>(smem + CF::OFF_Y + (q & 1) * CF::Y_SLOT);
+    float yv[CPL][S];  // partial y of the sub-chunk, stored after the loop so
+                       // the loads of later steps can be issued early
 #pragma unroll
     for (int tl = 0; tl < S; ++tl) {
       // (dt, w) of my CPL adjacent channels: one 8- or 16-byte load
@@ -813,9 +819,15 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         }
         if constexpr (!SUMMARY) {
           const float2 yy = upk(y2);
-          Y[tl * (CH * TN) + (cbase + i) * TN + j] = yy.x + yy.y;  // step-major rows
+          yv[i][tl] = yy.x + yy.y;
         }
       }
+    }
+    if constexpr (!SUMMARY) {
+#pragma unroll
+      for (int tl = 0; tl < S; ++tl)
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) Y[tl * (CH * TN) + (cbase + i) * TN + j] = yv[i][tl];  // step-major rows
     }
     __syncwarp();
     if (lane == 0) {
