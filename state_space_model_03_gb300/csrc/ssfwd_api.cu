@@ -381,8 +381,8 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   bool tma = g_encode != nullptr && !std::getenv("SSFWD_NO_TMA") && encode(tm_sum, ki.ch);
   const int groups = kp.ngroups;
   // Forward variant: CTA width (32 or 16 channels) x hand-off length (16 or
-  // 8 steps). Cost model: per-SM CTA load (in CTA waves when more CTAs than
-  // resident slots) x channels per CTA x a measured per-variant overhead.
+  // 8 steps). Cost model: CTAs per SM x channels per CTA x the measured
+  // per-CTA overhead of the variant relative to 32 channels / 16 steps.
   bool sub8 = false, ch16 = false;
   if (tma) {
     double best = 0.0;
@@ -403,10 +403,11 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
         occ = slot;
       }
       if (occ <= 0 || nsm <= 0) continue;
+      // CTAs beyond the resident slots run in a tail on otherwise idle SMs, so
+      // the load is counted per SM without a wave penalty.
       const int64_t ctas = int64_t((kp.dpg + kv.ch - 1) / kv.ch) * groups * kp.batch * sp.nseg;
-      const int64_t per_sm = (ctas + nsm - 1) / nsm;
-      const int64_t load = per_sm <= occ ? per_sm : (ctas + int64_t(occ) * nsm - 1) / (int64_t(occ) * nsm) * occ;
-      const double cost = double(load) * kv.ch * (v8 ? 1.06 : 1.0) * (v16 ? 1.16 : 1.0);
+      const int64_t load = (ctas + nsm - 1) / nsm;
+      const double cost = double(load) * kv.ch * (v8 ? 1.2 : 1.0) * (v16 ? 1.35 : 1.0);
       if (v == 0 || cost < best) {
         best = cost;
         bestk = kv;
