@@ -17,7 +17,7 @@ static KernelInfo pick3(bool summary, bool sub8, bool ch16) {
   if (summary) return ch16 ? KernelInfo{nullptr, 0, 0, 0, 0} : info<NP, K, FIXED, BCF32, TMA, true, 16>();
   if constexpr (TMA) {
     if constexpr (NP == 16) {  // 16-channel CTAs: the common state size only
-      if (ch16) return sub8 ? info<NP, K, FIXED, BCF32, TMA, false, 8, 16>() : info<NP, K, FIXED, BCF32, TMA, false, 16, 16>();
+      if (ch16 && !sub8) return info<NP, K, FIXED, BCF32, TMA, false, 16, 16>();
     }
     if (ch16) return KernelInfo{nullptr, 0, 0, 0, 0};
     if (sub8) return info<NP, K, FIXED, BCF32, TMA, false, 8>();

@@ -42,8 +42,23 @@
 #ifndef SSK_CPL
 #define SSK_CPL 2
 #endif
+#ifndef SSK_PACKG
+#define SSK_PACKG 8
+#endif
+#ifndef SSK_NSLOT
+#define SSK_NSLOT 2
+#endif
 
 namespace ssk {
+
+// Scan-loop tuning by input type (measured on GB300): PF = steps of operand
+// prefetch, YB = steps of partial y kept in registers per batch of stores,
+// BCPACK = 16-bit B/C handed to the scan warps as packed state pairs (else as
+// fp32). bf16 widens with one integer op per value, so packing pays; fp16
+// needs a conversion per value in every scan lane, so fp32 hand-off wins.
+// SSK_PF / SSK_YB / SSK_BCPACK override these for experiments.
+template <typename T> struct Tune { static constexpr int PF = 2, YB = 4; static constexpr bool BCPACK = false; };
+template <> struct Tune<__nv_bfloat16> { static constexpr int PF = 1, YB = 16; static constexpr bool BCPACK = true; };
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -327,6 +342,11 @@ struct Cfg {
   static constexpr int SUBS = L / S;             // sub-chunks per chunk
   static constexpr int EPT = CH * S / (WE * 32); // element-warp steps per lane per sub-chunk
   static constexpr int STAGES = 2;
+  // hand-off slots (P, B/C, Y) between element and scan warps; a third slot
+  // lets the element warps run two sub-chunks ahead, which needs chunks of at
+  // least four sub-chunks so that the TMA stage ring still prefetches
+  static constexpr int NSLOT = (SUBS >= 4) ? SSK_NSLOT : 2;
+  static_assert(NSLOT >= 2 && NSLOT <= 4 && SUBS >= NSLOT - 1, "hand-off slots");
   static_assert(NP % K == 0 && TN >= 1 && TN <= 8, "bad state split");
   static_assert(K % 4 == 0, "K must be a multiple of 4 (16-byte B/C loads)");
   static_assert(CH * S == WE * 32 * EPT && EPT >= 2, "element warps cover the sub-chunk exactly");
@@ -344,16 +364,20 @@ struct Cfg {
   static constexpr int OFF_CR = OFF_BR + (FIXED ? 0 : STAGES * BCMAX);
   static constexpr int OFF_P = OFF_CR + (FIXED ? 0 : STAGES * BCMAX);
   static constexpr int P_SLOT = S * CH * 8;                       // (dt, w) [S][CH]
-  static constexpr int OFF_BC = OFF_P + 2 * P_SLOT;
+  static constexpr int OFF_BC = OFF_P + NSLOT * P_SLOT;
   // B/C of one sub-chunk: fp32 B then C [S][NP] each when stored fp32; else the
   // stored 16-bit values packed per step as, for each state group of K,
   // K/2 words of (B_n, B_n+1) followed by K/2 words of (C_n, C_n+1).
-  static constexpr bool BCPACK = !BCF32;
+#ifdef SSK_BCPACK
+  static constexpr bool BCPACK = !BCF32 && SSK_BCPACK != 0;
+#else
+  static constexpr bool BCPACK = !BCF32 && Tune<T>::BCPACK;
+#endif
   static constexpr int BC_SLOT = FIXED ? 0 : (BCPACK ? S * NP * 4 : 2 * S * NP * 4);
-  static constexpr int OFF_Y = OFF_BC + 2 * BC_SLOT;
+  static constexpr int OFF_Y = OFF_BC + NSLOT * BC_SLOT;
   static constexpr int Y_SLOT = S * CH * TN * 4;                  // partial y [S][CH*TN]
-  static constexpr int OFF_BAR = OFF_Y + 2 * Y_SLOT;
-  static constexpr int NBAR = 2 * STAGES + 8;
+  static constexpr int OFF_BAR = OFF_Y + NSLOT * Y_SLOT;
+  static constexpr int NBAR = 2 * STAGES + 4 * NSLOT;
   static constexpr int SMEM = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024
   // CTAs per SM the shared memory allows (228 KB per SM, 1 KB reserved per CTA);
@@ -388,10 +412,11 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *bar_full = reinterpret_cast<uint64_t *>(smem + CF::OFF_BAR);  // [STAGES] TMA landed
   uint64_t *bar_empty = bar_full + STAGES;   // [STAGES] element warps done with the stage
-  uint64_t *bar_pfull = bar_empty + STAGES;  // [2] P/BC slot written (element warps)
-  uint64_t *bar_pempty = bar_pfull + 2;      // [2] P/BC slot consumed (scan warps)
-  uint64_t *bar_yfull = bar_pempty + 2;      // [2] Y slot written (scan warps)
-  uint64_t *bar_yempty = bar_yfull + 2;      // [2] Y slot consumed (element warps)
+  constexpr int NSLOT = CF::NSLOT;
+  uint64_t *bar_pfull = bar_empty + STAGES;  // [NSLOT] P/BC slot written (element warps)
+  uint64_t *bar_pempty = bar_pfull + NSLOT;  // [NSLOT] P/BC slot consumed (scan warps)
+  uint64_t *bar_yfull = bar_pempty + NSLOT;  // [NSLOT] Y slot written (scan warps)
+  uint64_t *bar_yempty = bar_yfull + NSLOT;  // [NSLOT] Y slot consumed (element warps)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.x / p.tiles_per_group;
@@ -411,7 +436,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], WE);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&bar_pfull[s], WE);
       mbar_init(&bar_pempty[s], WS);
       mbar_init(&bar_yfull[s], WS);
@@ -527,14 +552,15 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     constexpr bool bc_swz = (bc_row == 128);
 
     float lam = 0.f;  // SUMMARY: sum of dt over my steps of the segment
-    // prep of sub-chunk q: (dt, w) and the sub-chunk's B/C into slot q & 1
+    // prep of sub-chunk q: (dt, w) and the sub-chunk's B/C into slot q % NSLOT
     auto prep = [&](int q) -> bool {
       const int ci = q / SUBS, sub = q - ci * SUBS, s = ci % STAGES;
+      const int slot = q % NSLOT;
       if (!mbar_wait(&bar_full[s], (ci / STAGES) & 1, p.err, kErrWaitFull)) return false;
-      if (q >= 2 && !mbar_wait(&bar_pempty[q & 1], ((q - 2) >> 1) & 1, p.err, kErrWaitEmpty)) return false;
+      if (q >= NSLOT && !mbar_wait(&bar_pempty[slot], ((q / NSLOT) - 1) & 1, p.err, kErrWaitEmpty)) return false;
       const unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
       const unsigned char *sd = smem + CF::OFF_DL + s * CF::TILE;
-      float2 *P = reinterpret_cast<float2 *>(smem + CF::OFF_P + (q & 1) * CF::P_SLOT);
+      float2 *P = reinterpret_cast<float2 *>(smem + CF::OFF_P + slot * CF::P_SLOT);
       const int col0 = sub * S + h * EPT;
       const int t0 = tseg0 + ci * L + col0;
       float uv[EPT], dv[EPT];
@@ -555,35 +581,39 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         static_assert(CF::BC_ROW == 128, "16-bit B/C rows are one swizzled 128-byte line");
         const unsigned char *sbr = smem + CF::OFF_BR + s * CF::BCMAX;
         const unsigned char *scr = smem + CF::OFF_CR + s * CF::BCMAX;
-        uint32_t *bcw = reinterpret_cast<uint32_t *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
-        // items: (tensor, state pair m, half) -> EPT steps of rows 2m and 2m+1
-        for (int it = le; it < 2 * NP; it += WE * 32) {
-          const int hh = it & 1, m = (it >> 1) % (NP / 2), tensor = (it >> 1) / (NP / 2);
+        uint32_t *bcw = reinterpret_cast<uint32_t *>(smem + CF::OFF_BC + slot * CF::BC_SLOT);
+        // items: (tensor, state pair m, group of G steps) -> G steps of rows
+        // 2m and 2m+1 (eight steps measured fastest, although for 16 states
+        // that leaves the second element warp without packing work)
+        constexpr int G = SSK_PACKG < S ? SSK_PACKG : S;
+        constexpr int NG = S / G;
+        static_assert(S % G == 0, "step groups tile the sub-chunk");
+        for (int it = le; it < NP * NG; it += WE * 32) {
+          const int sg = it % NG, m = (it / NG) % (NP / 2), tensor = (it / NG) / (NP / 2);
           const unsigned char *raw = tensor ? scr : sbr;
-          const int col = sub * S + hh * EPT;  // EPT 16-bit values: inside one 16-byte chunk
+          const int col = sub * S + sg * G;  // G 16-bit values: inside one 16-byte chunk
           const int n = 2 * m;
-          uint32_t a[EPT / 2], bb[EPT / 2];
+          uint32_t a[G / 2], bb[G / 2];
 #pragma unroll
-          for (int k = 0; k < EPT / 2; ++k) a[k] = bb[k] = 0u;
-          auto load_row = [&](int row, uint32_t (&v)[EPT / 2]) {
+          for (int k = 0; k < G / 2; ++k) a[k] = bb[k] = 0u;
+          auto load_row = [&](int row, uint32_t (&v)[G / 2]) {
             const unsigned char *src = raw + swz(row, col * 2);
-            if constexpr (EPT == 8) {
+            if constexpr (G == 8) {
               const uint4 r = *reinterpret_cast<const uint4 *>(src);
               v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
-            } else if constexpr (EPT == 4) {
+            } else if constexpr (G == 4) {
               const uint2 r = *reinterpret_cast<const uint2 *>(src);
               v[0] = r.x; v[1] = r.y;
             } else {
-#pragma unroll
-              for (int k = 0; k < EPT / 2; ++k) v[k] = reinterpret_cast<const uint32_t *>(src)[k];
+              v[0] = *reinterpret_cast<const uint32_t *>(src);
             }
           };
           if (n < nrow_bc) load_row(n, a);
           if (n + 1 < nrow_bc) load_row(n + 1, bb);
           const int grp = n / K, wi = (n % K) / 2 + (tensor ? K / 2 : 0);
-          uint32_t *dst = bcw + (hh * EPT) * NP + grp * K + wi;
+          uint32_t *dst = bcw + (sg * G) * NP + grp * K + wi;
 #pragma unroll
-          for (int k = 0; k < EPT / 2; ++k) {
+          for (int k = 0; k < G / 2; ++k) {
             dst[(2 * k) * NP] = __byte_perm(a[k], bb[k], 0x5410);      // step 2k: low halves
             dst[(2 * k + 1) * NP] = __byte_perm(a[k], bb[k], 0x7632);  // step 2k+1: high halves
           }
@@ -592,7 +622,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       if constexpr (!FIXED && !CF::BCPACK) {
         const unsigned char *sbr = smem + CF::OFF_BR + s * CF::BCMAX;
         const unsigned char *scr = smem + CF::OFF_CR + s * CF::BCMAX;
-        float *bc = reinterpret_cast<float *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
+        float *bc = reinterpret_cast<float *>(smem + CF::OFF_BC + slot * CF::BC_SLOT);
         // items: (tensor, state n, half) -> EPT consecutive steps of one row
         for (int it = le; it < 4 * NP; it += WE * 32) {
           const int hh = it & 1, n = (it >> 1) % NP, tensor = (it >> 1) / NP;
@@ -617,14 +647,15 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_pfull[q & 1]);
+      if (lane == 0) mbar_arrive(&bar_pfull[slot]);
       return true;
     };
     // epilogue of sub-chunk q: sum partial y, D skip, gate, round, store
     auto epilogue = [&](int q) -> bool {
       const int ci = q / SUBS, sub = q - ci * SUBS, s = ci % STAGES;
-      if (!mbar_wait(&bar_yfull[q & 1], (q >> 1) & 1, p.err, kErrWaitReady)) return false;
-      const float *Y = reinterpret_cast<const float *>(smem + CF::OFF_Y + (q & 1) * CF::Y_SLOT);
+      const int slot = q % NSLOT;
+      if (!mbar_wait(&bar_yfull[slot], (q / NSLOT) & 1, p.err, kErrWaitReady)) return false;
+      const float *Y = reinterpret_cast<const float *>(smem + CF::OFF_Y + slot * CF::Y_SLOT);
       float y[EPT];
 #pragma unroll
       for (int k = 0; k < EPT; ++k) {
@@ -643,7 +674,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         y[k] = acc;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_yempty[q & 1]);
+      if (lane == 0) mbar_arrive(&bar_yempty[slot]);
       const unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
       const unsigned char *sz = smem + CF::OFF_Z + s * CF::TILE;
       const int col0 = sub * S + h * EPT;
@@ -679,10 +710,13 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       lam += __shfl_xor_sync(0xffffffffu, lam, 8);
       if (ok && h == 0 && ch_ok)
         p.ws[(long long)nsum * NP * p.batch * p.dim + ((long long)b * p.dim + d) * nsum + seg] = lam;
-    } else if (nsub > 0 && prep(0)) {
-      for (int q = 1; q <= nsub; ++q) {
-        if (q < nsub && !prep(q)) break;
-        if (!epilogue(q - 1)) break;
+    } else {
+      // prep runs NSLOT - 1 sub-chunks ahead of the epilogue
+      bool ok = true;
+      for (int q = 0; q < NSLOT - 1 && q < nsub && ok; ++q) ok = prep(q);
+      for (int q = 0; q < nsub && ok; ++q) {
+        if (q + NSLOT - 1 < nsub && !prep(q + NSLOT - 1)) break;
+        ok = epilogue(q);
       }
     }
     return;
@@ -748,57 +782,87 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   }
 
   for (int q = 0; q < nsub; ++q) {
-    if (!mbar_wait(&bar_pfull[q & 1], (q >> 1) & 1, p.err, kErrWaitReady)) break;
-    if (!SUMMARY && q >= 2 && !mbar_wait(&bar_yempty[q & 1], ((q - 2) >> 1) & 1, p.err, kErrWaitEmpty)) break;
-    const float2 *P = reinterpret_cast<const float2 *>(smem + CF::OFF_P + (q & 1) * CF::P_SLOT);
-    const float *b32 = reinterpret_cast<const float *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
+    const int slot = q % NSLOT;
+    if (!mbar_wait(&bar_pfull[slot], (q / NSLOT) & 1, p.err, kErrWaitReady)) break;
+    if (!SUMMARY && q >= NSLOT && !mbar_wait(&bar_yempty[slot], ((q / NSLOT) - 1) & 1, p.err, kErrWaitEmpty)) break;
+    const float2 *P = reinterpret_cast<const float2 *>(smem + CF::OFF_P + slot * CF::P_SLOT);
+    const float *b32 = reinterpret_cast<const float *>(smem + CF::OFF_BC + slot * CF::BC_SLOT);
     const float *c32 = b32 + S * NP;
-    const uint32_t *bcw = reinterpret_cast<const uint32_t *>(smem + CF::OFF_BC + (q & 1) * CF::BC_SLOT);
-    float *Y = reinterpret_cast<float *>(smem + CF::OFF_Y + (q & 1) * CF::Y_SLOT);
-    float yv[CPL][S];  // partial y of the sub-chunk, stored after the loop so
-                       // the loads of later steps can be issued early
+    const uint32_t *bcw = reinterpret_cast<const uint32_t *>(smem + CF::OFF_BC + slot * CF::BC_SLOT);
+    float *Y = reinterpret_cast<float *>(smem + CF::OFF_Y + slot * CF::Y_SLOT);
+    // Operands of step tl are loaded PF steps ahead into a register ring
+    // (raw words, converted when used); partial y's are stored in batches of
+    // YB steps, after the loads issued so far.
+#ifdef SSK_PF
+    constexpr int PF = SSK_PF;
+#else
+    constexpr int PF = Tune<T>::PF;
+#endif
+#ifdef SSK_YB
+    constexpr int YB = SSK_YB < S ? SSK_YB : S;
+#else
+    // fixed B/C and 8 states per lane hold more per-lane constants: 4-step batches
+    constexpr int YB0 = (FIXED || K > 4) && Tune<T>::YB > 4 ? 4 : Tune<T>::YB;
+    constexpr int YB = YB0 < S ? YB0 : S;
+#endif
+    static_assert(PF >= 1 && PF < S && S % YB == 0, "prefetch distance / y batch");
+    constexpr int NBW = (!FIXED && CF::BCPACK) ? K : 1;             // packed B/C words
+    constexpr int NBQ = (!FIXED && !CF::BCPACK) ? K / 4 : 1;        // fp32 B (and C) quads
+    float4 rp[PF + 1];
+    uint32_t rw[PF + 1][NBW];
+    float4 rb[PF + 1][NBQ], rc[PF + 1][NBQ];
+    auto load = [&](int tl, int r) {
+      if constexpr (CPL == 2) {
+        rp[r] = *reinterpret_cast<const float4 *>(P + tl * CH + cbase);
+      } else {
+        const float2 v = P[tl * CH + cbase];
+        rp[r] = make_float4(v.x, v.y, 0.f, 0.f);
+      }
+      if constexpr (!FIXED && CF::BCPACK) {
+        // K/2 words of B pairs then K/2 words of C pairs (16-byte loads)
+#pragma unroll
+        for (int q4 = 0; q4 < K / 4; ++q4) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(bcw + tl * NP + n0 + 4 * q4);
+          rw[r][4 * q4] = v.x; rw[r][4 * q4 + 1] = v.y; rw[r][4 * q4 + 2] = v.z; rw[r][4 * q4 + 3] = v.w;
+        }
+      } else if constexpr (!FIXED) {
+        // fp32 B, C for states n0+4q .. n0+4q+3 (one 16-byte load each)
+#pragma unroll
+        for (int q4 = 0; q4 < K / 4; ++q4) {
+          rb[r][q4] = *reinterpret_cast<const float4 *>(b32 + tl * NP + n0 + 4 * q4);
+          if constexpr (!SUMMARY) rc[r][q4] = *reinterpret_cast<const float4 *>(c32 + tl * NP + n0 + 4 * q4);
+        }
+      }
+    };
+    float yv[CPL][YB];
+#pragma unroll
+    for (int tl = 0; tl < PF; ++tl) load(tl, tl);
 #pragma unroll
     for (int tl = 0; tl < S; ++tl) {
-      // (dt, w) of my CPL adjacent channels: one 8- or 16-byte load
+      if (tl + PF < S) load(tl + PF, (tl + PF) % (PF + 1));
+      const int r = tl % (PF + 1);
+      // (dt, w) of my CPL adjacent channels
       f2 dt2[CPL], w2[CPL];
-      if constexpr (CPL == 2) {
-        const float4 pw = *reinterpret_cast<const float4 *>(P + tl * CH + cbase);
-        dt2[0] = pk(pw.x, pw.x); w2[0] = pk(pw.y, pw.y);
-        dt2[1] = pk(pw.z, pw.z); w2[1] = pk(pw.w, pw.w);
-      } else {
-        const float2 pw = P[tl * CH + cbase];
-        dt2[0] = pk(pw.x, pw.x); w2[0] = pk(pw.y, pw.y);
-      }
+      dt2[0] = pk(rp[r].x, rp[r].x); w2[0] = pk(rp[r].y, rp[r].y);
+      if constexpr (CPL == 2) { dt2[1] = pk(rp[r].z, rp[r].z); w2[1] = pk(rp[r].w, rp[r].w); }
       // B and C of my K states at this step, as fp32 state pairs
       f2 bp[K / 2], cp[K / 2];
-      if constexpr (!FIXED) {
-        if constexpr (CF::BCPACK) {
-          // K/2 words of B pairs then K/2 words of C pairs (16-byte loads)
-          uint32_t wv[K];
+      if constexpr (!FIXED && CF::BCPACK) {
 #pragma unroll
-          for (int q4 = 0; q4 < K / 4; ++q4) {
-            const uint4 r = *reinterpret_cast<const uint4 *>(bcw + tl * NP + n0 + 4 * q4);
-            wv[4 * q4] = r.x; wv[4 * q4 + 1] = r.y; wv[4 * q4 + 2] = r.z; wv[4 * q4 + 3] = r.w;
+        for (int k = 0; k < K / 2; ++k) {
+          const float2 bf = unpack2<T>(rw[r][k]);
+          bp[k] = pk(bf.x, bf.y);
+          if constexpr (!SUMMARY) {
+            const float2 cf = unpack2<T>(rw[r][K / 2 + k]);
+            cp[k] = pk(cf.x, cf.y);
           }
+        }
+      } else if constexpr (!FIXED) {
 #pragma unroll
-          for (int k = 0; k < K / 2; ++k) {
-            const float2 bf = unpack2<T>(wv[k]);
-            bp[k] = pk(bf.x, bf.y);
-            if constexpr (!SUMMARY) {
-              const float2 cf = unpack2<T>(wv[K / 2 + k]);
-              cp[k] = pk(cf.x, cf.y);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < K / 2; k += 2) {
-            // B, C for states n0+2k .. n0+2k+3 (one 16-byte load each)
-            const float4 bq = *reinterpret_cast<const float4 *>(b32 + tl * NP + n0 + 2 * k);
-            bp[k] = pk(bq.x, bq.y); bp[k + 1] = pk(bq.z, bq.w);
-            if constexpr (!SUMMARY) {
-              const float4 cq = *reinterpret_cast<const float4 *>(c32 + tl * NP + n0 + 2 * k);
-              cp[k] = pk(cq.x, cq.y); cp[k + 1] = pk(cq.z, cq.w);
-            }
+        for (int q4 = 0; q4 < K / 4; ++q4) {
+          bp[2 * q4] = pk(rb[r][q4].x, rb[r][q4].y); bp[2 * q4 + 1] = pk(rb[r][q4].z, rb[r][q4].w);
+          if constexpr (!SUMMARY) {
+            cp[2 * q4] = pk(rc[r][q4].x, rc[r][q4].y); cp[2 * q4 + 1] = pk(rc[r][q4].z, rc[r][q4].w);
           }
         }
       }
@@ -819,20 +883,23 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         }
         if constexpr (!SUMMARY) {
           const float2 yy = upk(y2);
-          yv[i][tl] = yy.x + yy.y;
+          yv[i][tl % YB] = yy.x + yy.y;
+        }
+      }
+      if constexpr (!SUMMARY) {
+        if (tl % YB == YB - 1) {
+#pragma unroll
+          for (int u = 0; u < YB; ++u)
+#pragma unroll
+            for (int i = 0; i < CPL; ++i)  // step-major rows
+              Y[(tl - YB + 1 + u) * (CH * TN) + (cbase + i) * TN + j] = yv[i][u];
         }
       }
     }
-    if constexpr (!SUMMARY) {
-#pragma unroll
-      for (int tl = 0; tl < S; ++tl)
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) Y[tl * (CH * TN) + (cbase + i) * TN + j] = yv[i][tl];  // step-major rows
-    }
     __syncwarp();
     if (lane == 0) {
-      mbar_arrive(&bar_pempty[q & 1]);
-      if constexpr (!SUMMARY) mbar_arrive(&bar_yfull[q & 1]);
+      mbar_arrive(&bar_pempty[slot]);
+      if constexpr (!SUMMARY) mbar_arrive(&bar_yfull[slot]);
     }
   }
 

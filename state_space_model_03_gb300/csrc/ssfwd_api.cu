@@ -25,7 +25,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int32_t *g_err_ptr[kMaxDevices] = {};
 bool g_attr_done[kMaxDevices][3][5][2][2][2][2][2][2] = {};
-int g_occupancy[kMaxDevices][3][5][2][2][4] = {};  // CTAs/SM of the TMA forward, [..][sub8 | ch16 << 1]
+int g_occupancy[kMaxDevices][3][5][2][2][3] = {};  // CTAs/SM of the TMA forward variants 0, 1, 2
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -380,40 +380,52 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   CUtensorMap tm[5], tm_sum[5];
   bool tma = g_encode != nullptr && !std::getenv("SSFWD_NO_TMA") && encode(tm_sum, ki.ch);
   const int groups = kp.ngroups;
-  // Forward variant: CTA width (32 or 16 channels) x hand-off length (16 or
-  // 8 steps). Cost model: CTAs per SM x channels per CTA x the measured
-  // per-CTA overhead of the variant relative to 32 channels / 16 steps.
+  // Forward variant: 32-channel CTAs with 16-step hand-offs (0), the same
+  // with 8-step hand-offs (1: smaller buffers, one more resident CTA per SM,
+  // about 1.36x the time per CTA), or 16-channel CTAs (2). A CTA's time
+  // grows only mildly with the CTAs that share its SM (the recurrence is
+  // latency-bound), so the variant that runs the grid in the fewest waves of
+  // resident CTAs wins. Among equals: 16-channel CTAs when the 32-channel grid
+  // leaves no SM more than two CTAs (about 5% faster there), else variant 0.
   bool sub8 = false, ch16 = false;
   if (tma) {
-    double best = 0.0;
-    ssk::KernelInfo bestk = ki;
-    for (int v = 0; v < 4; ++v) {
-      const bool v8 = v & 1, v16 = v & 2;
+    ssk::KernelInfo kv[3] = {};
+    int64_t waves[3] = {0, 0, 0}, ctas[3] = {0, 0, 0};
+    const char *force = std::getenv("SSFWD_VARIANT");  // diagnostics: one variant only
+    for (int v = 0; v < 3; ++v) {
+      const bool v8 = v == 1, v16 = v == 2;
       if (v16 && std::getenv("SSFWD_NO_CH16")) continue;
       if (v8 && std::getenv("SSFWD_NO_SUB8")) continue;
-      ssk::KernelInfo kv = lookup(p->in_dtype, np, fixed, bc_f32, true, false, v8, v16);
-      if (!kv.fn) continue;
-      if (!set_smem_attr(dev, kv, p->in_dtype, np, fixed, bc_f32, true, false, v8, v16)) return SS_ERR_CUDA;
+      if (force && std::atoi(force) != v) continue;
+      ssk::KernelInfo k = lookup(p->in_dtype, np, fixed, bc_f32, true, false, v8, v16);
+      if (!k.fn) continue;
+      if (!set_smem_attr(dev, k, p->in_dtype, np, fixed, bc_f32, true, false, v8, v16)) return SS_ERR_CUDA;
       int occ = 0;
       {
         std::lock_guard<std::mutex> lk(g_mu);
         int &slot = g_occupancy[dev][p->in_dtype][np_index(np)][fixed][bc_f32 && !fixed][v];
-        if (!slot && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&slot, kv.fn, kv.threads, kv.smem) != cudaSuccess)
+        if (!slot && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&slot, k.fn, k.threads, k.smem) != cudaSuccess)
           slot = 0;
         occ = slot;
       }
       if (occ <= 0 || nsm <= 0) continue;
-      // CTAs beyond the resident slots run in a tail on otherwise idle SMs, so
-      // the load is counted per SM without a wave penalty.
-      const int64_t ctas = int64_t((kp.dpg + kv.ch - 1) / kv.ch) * groups * kp.batch * sp.nseg;
-      const int64_t load = (ctas + nsm - 1) / nsm;
-      const double cost = double(load) * kv.ch * (v8 ? 1.2 : 1.0) * (v16 ? 1.35 : 1.0);
-      if (v == 0 || cost < best) {
-        best = cost;
-        bestk = kv;
-        sub8 = v8;
-        ch16 = v16;
-      }
+      kv[v] = k;
+      ctas[v] = int64_t((kp.dpg + k.ch - 1) / k.ch) * groups * kp.batch * sp.nseg;
+      waves[v] = (ctas[v] + int64_t(occ) * nsm - 1) / (int64_t(occ) * nsm);
+    }
+    const int64_t ctas32 = int64_t((kp.dpg + 31) / 32) * groups * kp.batch * sp.nseg;
+    const int order_small[3] = {2, 0, 1}, order[3] = {0, 2, 1};
+    const int *pref = ctas32 <= 2 * int64_t(nsm) ? order_small : order;
+    int best = -1;
+    for (int i = 0; i < 3; ++i) {
+      const int v = pref[i];
+      if (kv[v].fn && (best < 0 || waves[v] < waves[best])) best = v;
+    }
+    ssk::KernelInfo bestk = ki;
+    if (best >= 0) {
+      bestk = kv[best];
+      sub8 = best == 1;
+      ch16 = best == 2;
     }
     ki = bestk;
     if (ch16 && !encode(tm, ki.ch)) return SS_ERR_INTERNAL;

@@ -290,28 +290,56 @@ def test_segmented_sequence(case, monkeypatch):
         assert float((lst - l1).abs().max()) <= TOL[dt] * float(l1.abs().max())
 
 
-def test_eight_step_handoffs_agree(monkeypatch):
-    """A grid larger than the 16-step kernel's resident CTAs runs with 8-step
-    hand-offs; it must agree with the 16-step schedule up to rounding."""
-    w = workloads.Workload("sub8", 4, 4096, 300, 16, groups=4, bc_4d=True, dtype="bf16",
-                           return_last_state=True, seed=31)
-    x = workloads.make_inputs(w)
-    dev = _to_dev(x)
-    o8, l8 = _run(x, dev)
-    monkeypatch.setenv("SSFWD_NO_SUB8", "1")
-    o16, l16 = _run(x, dev)
-    assert float((o8.float() - o16.float()).abs().max()) <= 1e-2 * float(o16.float().abs().max())
-    assert float((l8 - l16).abs().max()) <= 1e-5 * float(l16.abs().max())
+VARIANT_OF = {("32", "16"): 0, ("32", "8"): 1, ("16", "16"): 2}  # (ch, sub) of the launch report
+VARIANT_CASES = [
+    # 16 states (all three forward variants exist), ragged channel tiles and
+    # steps, two groups; one 16-bit and one fp32 case
+    workloads.Workload("variants_bf16", 2, 2 * 80, 296, 16, groups=2, bc_4d=True, dtype="bf16",
+                       return_last_state=True, seed=31),
+    workloads.Workload("variants_fp32", 1, 48, 200, 13, dtype="fp32", return_last_state=True, seed=33),
+]
 
 
-def test_sixteen_channel_ctas_agree(monkeypatch):
-    """A grid of 16-channel CTAs (picked for load balance) agrees with the
-    32-channel schedule up to rounding."""
-    w = workloads.Workload("ch16", 2, 5120, 300, 16, dtype="fp16", return_last_state=True, seed=37)
+@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("w", VARIANT_CASES, ids=lambda w: w.name)
+def test_each_forward_variant(w, variant, monkeypatch, capfd):
+    """Every forward variant (0: 32-channel CTAs, 16-step hand-offs; 1: 8-step
+    hand-offs; 2: 16-channel CTAs), forced one at a time, matches the oracle.
+    Rows are 16-byte aligned so that the TMA path (which has the variants)
+    runs."""
+    monkeypatch.setenv("SSFWD_VARIANT", str(variant))
+    monkeypatch.setenv("SSFWD_DEBUG", "1")
+    x = workloads.make_inputs(w)
+    capfd.readouterr()
+    out, last = _run(x)
+    line = [ln for ln in capfd.readouterr().err.splitlines() if ln.startswith("ssfwd:")][-1]
+    f = dict(kv.split("=") for kv in line.split()[2:] if "=" in kv)
+    assert line.split()[1] == "tma" and VARIANT_OF[(f["ch"], f["sub"])] == variant, line
+    _check_full(w, x, out, last)
+
+
+def _picked(capfd, w):
+    """Variant the launch picks for workload w (from the SSFWD_DEBUG report)."""
     x = workloads.make_inputs(w)
     dev = _to_dev(x)
-    o16, l16 = _run(x, dev)
-    monkeypatch.setenv("SSFWD_NO_CH16", "1")
-    o32, l32 = _run(x, dev)
-    assert float((o16.float() - o32.float()).abs().max()) <= 1e-2 * float(o32.float().abs().max())
-    assert float((l16 - l32).abs().max()) <= 1e-5 * float(l32.abs().max())
+    capfd.readouterr()
+    _run(x, dev)
+    err = capfd.readouterr().err
+    line = [ln for ln in err.splitlines() if ln.startswith("ssfwd:")][-1]
+    f = dict(kv.split("=") for kv in line.split()[2:] if "=" in kv)
+    return VARIANT_OF[(f["ch"], f["sub"])]
+
+
+def test_variant_choice_follows_waves(capfd, monkeypatch):
+    """With 152 SMs: a grid that fits the resident 32-channel CTAs runs variant
+    0; one that needs a second wave of them but fits with 8-step hand-offs runs
+    variant 1; one that leaves every SM at most two 32-channel CTAs runs
+    16-channel CTAs. Sizes are small in seqlen; the choice depends only on
+    the grid."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the expected choices are stated for 152 SMs")
+    monkeypatch.setenv("SSFWD_DEBUG", "1")
+    mk = lambda b, d, g: workloads.Workload("pick", b, d, 96, 16, groups=g, bc_4d=g > 1, dtype="bf16", seed=5)
+    assert _picked(capfd, mk(8, 1536, 1)) == 0   # 384 CTAs <= 3 per SM
+    assert _picked(capfd, mk(4, 4096, 4)) == 1   # 512 CTAs: 4 per SM fit only with 8-step hand-offs
+    assert _picked(capfd, mk(4, 1536, 1)) == 2   # 192 CTAs: at most 2 per SM
