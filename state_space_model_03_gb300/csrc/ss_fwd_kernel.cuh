@@ -418,7 +418,14 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   uint64_t *bar_yfull = bar_pempty + NSLOT;  // [NSLOT] Y slot written (scan warps)
   uint64_t *bar_yempty = bar_yfull + NSLOT;  // [NSLOT] Y slot consumed (element warps)
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Role of each warp. The hardware spreads a CTA's warps 0-3 over the four
+  // SM sub-partitions and puts warp 4 on warp 0's; warp 0 is therefore the
+  // lightest worker (the last element warp, which packs no B/C when there are
+  // 16 states), so that the producer (the last warp) shares its issue slots
+  // with it rather than with a scan warp. Logical order: scan warps
+  // 0..WS-1, element warps WS..WS+WE-1, producer WS+WE.
+  const int pw = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = (pw == 0) ? WS + WE - 1 : (pw == WS + WE ? pw : pw - 1);
   const int g = blockIdx.x / p.tiles_per_group;
   const int tile = blockIdx.x - g * p.tiles_per_group;
   const int b = blockIdx.y;
