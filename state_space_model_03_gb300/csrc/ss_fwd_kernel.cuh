@@ -418,12 +418,17 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   uint64_t *bar_yfull = bar_pempty + NSLOT;  // [NSLOT] Y slot written (scan warps)
   uint64_t *bar_yempty = bar_yfull + NSLOT;  // [NSLOT] Y slot consumed (element warps)
 
-  // Role of each warp. The hardware spreads a CTA's warps 0-3 over the four
-  // SM sub-partitions and puts warp 4 on warp 0's; warp 0 is therefore the
+  // Role of each warp. Measured placement on GB300: warp k of the j-th CTA
+  // resident on an SM runs on sub-partition (r + j * nwarps + k) % 4, so a
+  // CTA's warp 4 shares warp 0's sub-partition. Warp 0 is therefore the
   // lightest worker (the last element warp, which packs no B/C when there are
   // 16 states), so that the producer (the last warp) shares its issue slots
-  // with it rather than with a scan warp. Logical order: scan warps
-  // 0..WS-1, element warps WS..WS+WE-1, producer WS+WE.
+  // with it rather than with a scan warp. The scan warps stay adjacent
+  // (physical 1..WS): with three 5-warp CTAs per SM the two sub-partitions
+  // that must hold two scan warps then pair warps of different CTA pairs
+  // (placing them at 1 and 3 instead measured 4% slower on 3-CTA SMs).
+  // Logical order: scan warps 0..WS-1, element warps WS..WS+WE-1, producer
+  // WS+WE.
   const int pw = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int warp = (pw == 0) ? WS + WE - 1 : (pw == WS + WE ? pw : pw - 1);
   const int g = blockIdx.x / p.tiles_per_group;
