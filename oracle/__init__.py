@@ -60,7 +60,7 @@ def _load():
             i64, dp = ctypes.c_int64, ctypes.c_void_p
             f.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int,
                           dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
-                          dp, dp, i64, i64, dp]
+                          dp, dp, dp, i64, i64, dp]
             f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -91,11 +91,14 @@ def _normalise_bc(B, C, dim):
 
 
 def selective_scan_ref(u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                       delta_softplus=False, return_last_state=False, threads=1):
+                       delta_softplus=False, return_last_state=False, threads=1,
+                       initial_state=None):
     """Whole-problem fp64 reference. Returns out (b, d, l) fp64 numpy, and
-    last_state (b, d, n) fp64 when return_last_state."""
+    last_state (b, d, n) fp64 when return_last_state. initial_state (b, d, n),
+    if given, is the state before the first step (else zero)."""
     u, delta, A, B, C = (_f64(t) for t in (u, delta, A, B, C))
     D, z, delta_bias = _f64(D), _f64(z), _f64(delta_bias)
+    x0 = _f64(initial_state)
     batch, dim, seqlen = u.shape
     dstate = A.shape[1]
     B, C, fixed, ngroups = _normalise_bc(B, C, dim)
@@ -109,7 +112,7 @@ def selective_scan_ref(u, delta, A, B, C, D=None, z=None, delta_bias=None,
         rc = lib.ss_oracle_fwd(batch, dim, seqlen, dstate, ngroups, int(fixed),
                                _ptr(u), _ptr(delta), _ptr(z), _ptr(A), _ptr(B), _ptr(C),
                                _ptr(D), _ptr(delta_bias), int(bool(delta_softplus)),
-                               _ptr(out), _ptr(last), r0, r1, _ptr(scratch))
+                               _ptr(x0), _ptr(out), _ptr(last), r0, r1, _ptr(scratch))
         if rc != 0:
             raise ValueError("oracle: bad shape")
 
@@ -160,3 +163,44 @@ def selective_scan_rows(rows, u, delta, A, B, C, D=None, z=None, delta_bias=None
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(one, range(R)))
     return out, last
+
+
+def selective_state_update_ref(state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                               delta_softplus=False, bc_fixed=False):
+    """One step of the same recurrence for every (batch, channel), in plain
+    numpy fp64, written independently of ``ss_oracle.c`` (the decode step the
+    page lists as "selective_state_update"; it prints no signature, so the
+    operands are the scan's at a single time step):
+
+      state (b, d, n), u, delta, z (b, d), A (d, n), D, delta_bias (d,),
+      B, C per token (b, n) or grouped (b, g, n); with bc_fixed, (d, n).
+      dt = softplus(delta + delta_bias) (or the sum itself),
+      state' = exp(dt A) state + dt B u,  y = sum_n C state' + D u,
+      out = y silu(z) when z is given.
+
+    Returns (out (b, d), new state (b, d, n)) as fp64 arrays; the input state
+    is not modified."""
+    x = _f64(state)
+    u, delta, A, B, C = (_f64(t) for t in (u, delta, A, B, C))
+    D, z, delta_bias = _f64(D), _f64(z), _f64(delta_bias)
+    batch, dim = u.shape
+    v = delta + (delta_bias[None, :] if delta_bias is not None else 0.0)
+    if delta_softplus:
+        dt = np.maximum(v, 0.0) + np.log1p(np.exp(-np.abs(v)))
+    else:
+        dt = v
+    if bc_fixed:
+        Bd, Cd = B[None, :, :], C[None, :, :]          # per channel
+    else:
+        if B.ndim == 2:                                 # (b, n): one group
+            B, C = B[:, None, :], C[:, None, :]
+        g = B.shape[1]
+        grp = np.arange(dim) // (dim // g)
+        Bd, Cd = B[:, grp, :], C[:, grp, :]             # (b, d, n)
+    x = np.exp(dt[:, :, None] * A[None, :, :]) * x + (dt * u)[:, :, None] * Bd
+    y = np.sum(Cd * x, axis=2)
+    if D is not None:
+        y = y + D[None, :] * u
+    if z is not None:
+        y = y * (z / (1.0 + np.exp(-z)))
+    return y, x

@@ -23,7 +23,10 @@
  *     x_k  = exp(dt * A[k]) * x_k + dt * B[k,t] * u[t]   for every state k
  *     y    = sum_k C[k,t] * x_k  (x after the step-t update) + D * u[t]
  *     out  = y * silu(z[t]) = y * z / (1 + exp(-z))  when z is given, else y
- *   with x = 0 before t = 0 (the signature has no initial-state argument) and
+ *   with x = initial_state before t = 0 when one is given, else x = 0 (the
+ *   page's signature has no initial-state argument; the optional initial
+ *   state is the chaining input of a decode step, one of the operators the
+ *   same page lists next to the scan: "selective_state_update"), and
  *   last_state = x after the final step.
  *
  *   Channel d of a grouped B/C uses group d / (dim / groups) (each group serves
@@ -51,9 +54,9 @@ static void oracle_row(int64_t seqlen, int64_t dstate,
                        const double *A_row,
                        const double *B_row, int64_t b_kstride, int64_t b_tstride,
                        const double *C_row, int64_t c_kstride, int64_t c_tstride,
-                       double D_d, double bias_d, int delta_softplus,
+                       double D_d, double bias_d, int delta_softplus, const double *x0_row,
                        double *out_row, double *last_row, double *x) {
-  for (int64_t k = 0; k < dstate; ++k) x[k] = 0.0;
+  for (int64_t k = 0; k < dstate; ++k) x[k] = x0_row ? x0_row[k] : 0.0;
   for (int64_t t = 0; t < seqlen; ++t) {
     double uu = u_row[t];
     double v = delta_row[t] + bias_d;
@@ -82,6 +85,7 @@ static void oracle_row(int64_t seqlen, int64_t dstate,
  *   A                : (dim, dstate), contiguous.
  *   B, C             : bc_fixed ? (dim, dstate) : (batch, ngroups, dstate, seqlen), contiguous.
  *   D, delta_bias    : (dim,) or NULL (absent = 0).
+ *   initial_state    : (batch, dim, dstate) or NULL (absent = 0).
  *   last_state       : (batch, dim, dstate) or NULL.
  *   scratch          : dstate doubles owned by the caller (one per thread).
  * Returns 0, or -1 on a shape error (dim % ngroups != 0, non-positive sizes).
@@ -91,7 +95,7 @@ int ss_oracle_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, in
                   const double *u, const double *delta, const double *z,
                   const double *A, const double *B, const double *C,
                   const double *D, const double *delta_bias, int delta_softplus,
-                  double *out, double *last_state,
+                  const double *initial_state, double *out, double *last_state,
                   int64_t row_begin, int64_t row_end, double *scratch) {
   if (batch < 0 || dim <= 0 || seqlen < 0 || dstate <= 0) return -1;
   if (!bc_fixed && (ngroups <= 0 || dim % ngroups != 0)) return -1;
@@ -118,7 +122,7 @@ int ss_oracle_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, in
                A + d * dstate,
                B_row, kstride, tstride, C_row, kstride, tstride,
                D ? D[d] : 0.0, delta_bias ? delta_bias[d] : 0.0, delta_softplus,
-               out + r * seqlen, last_state ? last_state + r * dstate : NULL, scratch);
+               initial_state ? initial_state + r * dstate : NULL, out + r * seqlen, last_state ? last_state + r * dstate : NULL, scratch);
   }
   return 0;
 }
