@@ -11,7 +11,8 @@
  * with an Euler input term, per (batch b, channel d, state n, step t):
  *
  *     dt    = softplus(delta[b,d,t] + delta_bias[d])   (plain sum if !delta_softplus)
- *     x[n]  = exp(dt * A[d,n]) * x[n] + dt * B[n,t] * u[b,d,t]   (x = 0 before t = 0)
+ *     x[n]  = exp(dt * A[d,n]) * x[n] + dt * B[n,t] * u[b,d,t]
+ *             (x = initial_state[b,d,n] before t = 0 when given, else 0)
  *     y     = sum_n C[n,t] * x[n] + D[d] * u[b,d,t]
  *     out   = y * silu(z[b,d,t])  if z is given, else y;  silu(v) = v / (1 + e^-v)
  *     last_state[b,d,n] = x[n] after the last step
@@ -40,7 +41,7 @@
 extern "C" {
 #endif
 
-#define SS_ABI_VERSION 2
+#define SS_ABI_VERSION 3
 
 /* Element types. u, delta, z and out share `in_dtype`. */
 typedef enum ss_dtype { SS_F32 = 0, SS_F16 = 1, SS_BF16 = 2 } ss_dtype;
@@ -110,6 +111,14 @@ typedef struct ss_fwd_params {
    * instead (same results up to fp32 rounding, fewer CTAs). */
   void *workspace;
   int64_t workspace_bytes;
+  /* Optional start state (batch, dim, dstate) fp32 with stride {batch, dim,
+   * state}, state stride 1; NULL = zero. It lets a call continue a sequence
+   * from a previous call's last_state (the page's signature has none; it is
+   * the chaining input of the decode step below). It may be the very buffer
+   * passed as last_state with the same strides (each row is read before it is
+   * written); any other overlap with an output is SS_ERR_ALIAS. */
+  const float *initial_state;
+  int64_t initial_state_stride[3];
 } ss_fwd_params;
 
 /* SS_ABI_VERSION of the loaded library. */
@@ -176,6 +185,57 @@ int ss_fwd_host(const ss_fwd_params *p,
  */
 #define SS_NOALLOC_MAX_SCRATCH (2 * 1024 * 1024)
 int ss_fwd_noalloc(const ss_fwd_params *p, void *stream);
+
+/*
+ * One decode step of the same recurrence: section 4.4 of the page lists a
+ * "selective_state_update" operator for the Mamba models but prints no
+ * signature, so the operands are the scan's at a single time step. For every
+ * (batch b, channel d, state n):
+ *
+ *     dt    = softplus(delta[b,d] + delta_bias[d])   (plain sum if !delta_softplus)
+ *     state[b,d,n] = exp(dt * A[d,n]) * state[b,d,n] + dt * B[n] * u[b,d]
+ *     out[b,d]     = (sum_n C[n] * state[b,d,n] + D[d] * u[b,d]) * silu(z[b,d])
+ *
+ * with B[n] = B[b, d / (dim/ngroups), n] (variable) or B[d, n] (fixed), and
+ * no gate when z is NULL. The state is updated in place.
+ *
+ *   state              (batch, dim, dstate) fp32, stride {batch, dim, state},
+ *                      state stride 1; read and written.
+ *   u, delta, z, out   (batch, dim), in_dtype, stride {batch, dim}. z may be NULL.
+ *   B, C  variable     (batch, ngroups, dstate), dtype bc_dtype (in_dtype or
+ *                      SS_F32), stride {batch, group, state}, state stride 1.
+ *         fixed        (dim, dstate) fp32, stride {dim, 1}; ngroups ignored.
+ *   A                  (dim, dstate) fp32, state stride 1.
+ *   D, delta_bias      (dim,) fp32 contiguous, or NULL (absent = 0).
+ *
+ * Sizes: batch, dim >= 0, 1 <= dstate <= 64; batch * dim == 0 is a no-op.
+ * out must not overlap any input or the state, and the state must not
+ * overlap any input (SS_ERR_ALIAS). Same conventions as ss_fwd otherwise
+ * (device pointers, asynchronous on `stream`, nothing enqueued on error).
+ */
+typedef struct ss_state_update_params {
+  int32_t abi_version;      /* must be SS_ABI_VERSION */
+  int32_t in_dtype;         /* ss_dtype of u, delta, z, out */
+  int32_t bc_dtype;         /* ss_dtype of B, C */
+  int32_t bc_mode;          /* ss_bc_mode */
+  int32_t delta_softplus;
+  int32_t reserved0;
+  int64_t batch, dim, dstate, ngroups;
+  float *state;
+  const void *u, *delta, *z, *B, *C;
+  const float *A, *D, *delta_bias;
+  void *out;
+  int64_t state_stride[3];
+  int64_t u_stride[2], delta_stride[2], z_stride[2], out_stride[2];
+  int64_t B_stride[3], C_stride[3];
+  int64_t A_stride[2];
+} ss_state_update_params;
+
+/* Validate without launching (no CUDA call). */
+int ss_state_update_validate(const ss_state_update_params *p);
+
+/* The decode step on device buffers, enqueued on `stream`. */
+int ss_state_update(const ss_state_update_params *p, void *stream);
 
 /*
  * Device-side error word of the library on the current device (nonzero after

@@ -1,11 +1,12 @@
-"""GB300-native Mamba-1 selective-scan forward.
+"""GB300-native Mamba-1 selective-scan forward and decode step.
 
-``selective_scan_fn`` runs the hand-written sm_103a kernels of ``libssfwd.so``
-through its C ABI (``include/ssfwd.h``). There is no CPU fallback: the call
-raises if the CUDA library is missing or no GPU is present.
+``selective_scan_fn`` (with an optional start state) and
+``selective_state_update`` run the hand-written sm_103a kernels of
+``libssfwd.so`` through its C ABI (``include/ssfwd.h``). There is no CPU
+fallback: the calls raise if the CUDA library is missing or no GPU is present.
 """
 
-__all__ = ["selective_scan_fn", "selective_scan_fn_host"]
+__all__ = ["selective_scan_fn", "selective_scan_fn_host", "selective_state_update"]
 
 
 def __getattr__(name):

@@ -29,7 +29,7 @@ _lib = None
 
 SS_F32, SS_F16, SS_BF16 = 0, 1, 2
 SS_BC_FIXED, SS_BC_VARIABLE = 0, 1
-SS_ABI_VERSION = 2
+SS_ABI_VERSION = 3
 _DT = {torch.float32: SS_F32, torch.float16: SS_F16, torch.bfloat16: SS_BF16}
 
 _i64x2, _i64x3, _i64x4 = ctypes.c_int64 * 2, ctypes.c_int64 * 3, ctypes.c_int64 * 4
@@ -49,6 +49,24 @@ class SSFwdParams(ctypes.Structure):
         ("u_stride", _i64x3), ("delta_stride", _i64x3), ("z_stride", _i64x3), ("out_stride", _i64x3),
         ("B_stride", _i64x4), ("C_stride", _i64x4), ("A_stride", _i64x2), ("last_state_stride", _i64x3),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64),
+        ("initial_state", ctypes.c_void_p), ("initial_state_stride", _i64x3),
+    ]
+
+
+class SSStateUpdateParams(ctypes.Structure):
+    """Mirror of ``ss_state_update_params``."""
+    _fields_ = [
+        ("abi_version", ctypes.c_int32), ("in_dtype", ctypes.c_int32), ("bc_dtype", ctypes.c_int32),
+        ("bc_mode", ctypes.c_int32), ("delta_softplus", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+        ("state", ctypes.c_void_p),
+        ("u", ctypes.c_void_p), ("delta", ctypes.c_void_p), ("z", ctypes.c_void_p),
+        ("B", ctypes.c_void_p), ("C", ctypes.c_void_p),
+        ("A", ctypes.c_void_p), ("D", ctypes.c_void_p), ("delta_bias", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("state_stride", _i64x3),
+        ("u_stride", _i64x2), ("delta_stride", _i64x2), ("z_stride", _i64x2), ("out_stride", _i64x2),
+        ("B_stride", _i64x3), ("C_stride", _i64x3), ("A_stride", _i64x2),
     ]
 
 
@@ -86,6 +104,11 @@ def load_library():
             lib.ss_fwd_workspace_size.restype = ctypes.c_int
             lib.ss_fwd_host.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.ss_fwd_host.restype = ctypes.c_int
+            PS = ctypes.POINTER(SSStateUpdateParams)
+            lib.ss_state_update_validate.argtypes = [PS]
+            lib.ss_state_update_validate.restype = ctypes.c_int
+            lib.ss_state_update.argtypes = [PS, vp]
+            lib.ss_state_update.restype = ctypes.c_int
             lib.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
             lib.ss_device_error.restype = ctypes.c_int
             if lib.ss_abi_version() != SS_ABI_VERSION:
@@ -130,7 +153,8 @@ def normalise(u, delta, A, B, C, D=None, z=None, delta_bias=None):
     return u, delta, A, B, C, D, z, delta_bias
 
 
-def make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last_state) -> SSFwdParams:
+def make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last_state,
+                initial_state=None) -> SSFwdParams:
     """Fill an ss_fwd_params from already-normalised tensors (see normalise)."""
     if u.dim() != 3:
         raise ValueError("u must be (batch, dim, seqlen)")
@@ -180,6 +204,13 @@ def make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last_s
     p.out_stride[:] = list(out.stride())
     p.A_stride[:] = list(A.stride())
     p.last_state_stride[:] = list(last_state.stride()) if last_state is not None else [0, 0, 1]
+    if initial_state is not None:
+        if initial_state.dtype != torch.float32 or tuple(initial_state.shape) != (batch, dim, dstate):
+            raise TypeError("initial_state must be float32 (batch, dim, dstate)")
+        p.initial_state = _ptr(initial_state)
+        p.initial_state_stride[:] = list(initial_state.stride())
+    else:
+        p.initial_state_stride[:] = [0, 0, 1]
     return p
 
 
@@ -198,13 +229,14 @@ def attach_workspace(p: SSFwdParams, device) -> "torch.Tensor | None":
 
 
 def selective_scan_fn(u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                      delta_softplus=False, return_last_state=False):
+                      delta_softplus=False, return_last_state=False, initial_state=None):
     """Selective-scan forward on CUDA tensors; runs on the current stream.
 
     u, delta, z: (batch, dim, seqlen), fp32/fp16/bf16, one dtype.
     A: (dim, dstate) fp32 (real). B, C: (dim, dstate) fp32 fixed, or
     (batch, dstate, seqlen) / (batch, groups, dstate, seqlen) in u's dtype or
-    fp32. D, delta_bias: (dim,) fp32. Returns out (u's dtype), or
+    fp32. D, delta_bias: (dim,) fp32. initial_state: optional (batch, dim,
+    dstate) fp32 start state (zero if None). Returns out (u's dtype), or
     (out, last_state) with last_state (batch, dim, dstate) fp32.
     """
     if not u.is_cuda:
@@ -214,7 +246,9 @@ def selective_scan_fn(u, delta, A, B, C, D=None, z=None, delta_bias=None,
     out = torch.empty(u.shape, dtype=u.dtype, device=u.device)
     last = (torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
             if return_last_state else None)
-    p = make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last)
+    if initial_state is not None:
+        initial_state = _unit_last(initial_state)
+    p = make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last, initial_state)
     ws = attach_workspace(p, u.device)  # noqa: F841 (kept alive until the launch is enqueued)
     stream = torch.cuda.current_stream(u.device).cuda_stream
     with torch.cuda.device(u.device):
@@ -293,6 +327,82 @@ def selective_scan_fn_host(u, delta, A, B, C, D=None, z=None, delta_bias=None,
     if return_last_state:
         return res[0].clone(), res[1].clone()
     return res.clone()
+
+
+def make_state_update_params(state, u, delta, A, B, C, D, z, delta_bias, delta_softplus, out,
+                             bc_fixed=False) -> SSStateUpdateParams:
+    """Fill an ss_state_update_params from CUDA tensors (no copies made)."""
+    if u.dim() != 2 or u.dtype not in _DT:
+        raise TypeError("u must be (batch, dim) fp32/fp16/bf16")
+    batch, dim = u.shape
+    for name, t in (("delta", delta), ("z", z), ("out", out)):
+        if t is not None and (t.dtype != u.dtype or tuple(t.shape) != (batch, dim)):
+            raise TypeError(f"{name} must match u in shape and dtype")
+    if A.dim() != 2 or A.shape[0] != dim or A.dtype != torch.float32:
+        raise TypeError("A must be float32 (dim, dstate)")
+    dstate = A.shape[1]
+    if state.dtype != torch.float32 or tuple(state.shape) != (batch, dim, dstate):
+        raise TypeError("state must be float32 (batch, dim, dstate)")
+    for name, t in (("D", D), ("delta_bias", delta_bias)):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != (dim,)):
+            raise TypeError(f"{name} must be float32 (dim,)")
+    p = SSStateUpdateParams()
+    p.abi_version = SS_ABI_VERSION
+    p.in_dtype = _DT[u.dtype]
+    if bc_fixed:
+        if B.dtype != torch.float32 or C.dtype != torch.float32 or tuple(B.shape) != (dim, dstate) \
+                or tuple(C.shape) != (dim, dstate):
+            raise TypeError("fixed B/C must be float32 (dim, dstate)")
+        p.bc_mode, p.ngroups = SS_BC_FIXED, 1
+        p.B_stride[:] = [B.stride(0), B.stride(1), 0]
+        p.C_stride[:] = [C.stride(0), C.stride(1), 0]
+    else:
+        if B.dim() == 2:
+            B, C = B.unsqueeze(1), C.unsqueeze(1)
+        if B.dim() != 3 or B.shape[0] != batch or B.shape[2] != dstate or tuple(C.shape) != tuple(B.shape):
+            raise ValueError("B/C must be (batch, dstate) or (batch, groups, dstate)")
+        if B.dtype not in (u.dtype, torch.float32) or C.dtype != B.dtype:
+            raise TypeError("B/C must share a dtype, equal to u's or float32")
+        p.bc_mode, p.ngroups = SS_BC_VARIABLE, B.shape[1]
+        p.B_stride[:] = list(B.stride())
+        p.C_stride[:] = list(C.stride())
+    p.bc_dtype = _DT[B.dtype]
+    p.delta_softplus = int(bool(delta_softplus))
+    p.batch, p.dim, p.dstate = batch, dim, dstate
+    p.state = _ptr(state)
+    p.u, p.delta, p.z, p.B, p.C = _ptr(u), _ptr(delta), _ptr(z), _ptr(B), _ptr(C)
+    p.A, p.D, p.delta_bias, p.out = _ptr(A), _ptr(D), _ptr(delta_bias), _ptr(out)
+    p.state_stride[:] = list(state.stride())
+    p.u_stride[:] = list(u.stride())
+    p.delta_stride[:] = list(delta.stride())
+    p.z_stride[:] = list(z.stride()) if z is not None else [0, 0]
+    p.out_stride[:] = list(out.stride())
+    p.A_stride[:] = list(A.stride())
+    return p
+
+
+def selective_state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                           delta_softplus=False, bc_fixed=False):
+    """One decode step on CUDA tensors (current stream): updates ``state``
+    (batch, dim, dstate) fp32 in place and returns out (batch, dim).
+
+    u, delta, z: (batch, dim) in one dtype; B, C: (batch, dstate) or
+    (batch, groups, dstate) in u's dtype or fp32, or with bc_fixed (dim, dstate)
+    fp32; A: (dim, dstate) fp32; D, delta_bias: (dim,) fp32.
+    """
+    if not u.is_cuda:
+        raise RuntimeError("selective_state_update needs CUDA tensors (there is no CPU path)")
+    lib = load_library()
+    if state.stride(-1) != 1:
+        raise ValueError("state must have a unit last stride (it is updated in place)")
+    A = _unit_last(A)
+    B, C = _unit_last(B), _unit_last(C)
+    out = torch.empty(u.shape, dtype=u.dtype, device=u.device)
+    p = make_state_update_params(state, u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, bc_fixed)
+    stream = torch.cuda.current_stream(u.device).cuda_stream
+    with torch.cuda.device(u.device):
+        _check(lib.ss_state_update(ctypes.byref(p), stream))
+    return out
 
 
 def device_error(clear: bool = False) -> int:

@@ -84,6 +84,8 @@ struct KParams {
   // sums (one float per (batch, channel, segment)).
   int seg_len, nseg;
   float *ws;
+  const float *init;  // start state (batch, dim, dstate) fp32 or NULL (zero)
+  long long si[3];
   const void *u, *delta, *z, *B, *C;
   const float *A, *D, *bias;
   void *out;
@@ -464,7 +466,9 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], WE);
+      // a stage is released by the element warps and, when it converts the
+      // B/C tiles, by the producer (so it cannot refill a stage it still reads)
+      mbar_init(&bar_empty[s], WE + (CF::PPACK ? 1 : 0));
     }
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&bar_pfull[s], WE + (CF::PPACK ? 1 : 0));
@@ -648,7 +652,10 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         }
         convert_bc(q, lane, 32);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_pfull[slot]);
+        if (lane == 0) {
+          mbar_arrive(&bar_pfull[slot]);
+          if (q % SUBS == SUBS - 1) mbar_arrive(&bar_empty[ci % STAGES]);  // done reading this stage
+        }
       }
       while (ok && issued < nchunks) ok = issue_next();
     } else {
@@ -682,7 +689,10 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     T *gout = static_cast<T *>(p.out);
     const long long orow = (long long)b * p.so[0] + (long long)d * p.so[1];
     const bool out_vec = p.out_vec != 0;
-    float lam = 0.f;  // SUMMARY: sum of dt over my steps of the segment
+    // SUMMARY: sum of dt over my steps of the segment, accumulated in fp64:
+    // the forward decays the carried state by exp(A * sum), and an fp32 sum
+    // over thousands of steps would be off by ~1e-4 relative
+    double lam = 0.0;
     // prep of sub-chunk q: (dt, w) and the sub-chunk's B/C into slot q % NSLOT
     auto prep = [&](int q) -> bool {
       const int ci = q / SUBS, sub = q - ci * SUBS, s = ci % STAGES;
@@ -703,7 +713,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         float dt = softplus ? softplus_t<T>(v) : v;
         float w = dt * uv[k];
         if (t0 + k >= tseg1) { dt = 0.f; w = 0.f; }  // padded steps leave x unchanged
-        if constexpr (SUMMARY) lam += dt;
+        if constexpr (SUMMARY) lam += static_cast<double>(dt);
         P[(h * EPT + k) * CH + c] = make_float2(dt, w);
       }
       if constexpr (!CF::PPACK) convert_bc(q, le, WE * 32);
@@ -770,7 +780,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       // the two half-lanes of a channel (8 lanes apart): combine their step sums
       lam += __shfl_xor_sync(0xffffffffu, lam, 8);
       if (ok && h == 0 && ch_ok)
-        p.ws[(long long)nsum * NP * p.batch * p.dim + ((long long)b * p.dim + d) * nsum + seg] = lam;
+        p.ws[(long long)nsum * NP * p.batch * p.dim + ((long long)b * p.dim + d) * nsum + seg] = static_cast<float>(lam);
     } else {
       // prep runs NSLOT - 1 sub-chunks ahead of the epilogue
       bool ok = true;
@@ -796,6 +806,10 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
   f2 cb2[CPL][K / 2];   // fixed B/C: C*B per state pair
   float bfix[CPL][K];   // fixed B/C: B per state (for last_state)
   f2 x2[CPL][K / 2];
+  // A start state is folded in only by the forward pass (the summary pass
+  // works from zero); with fixed B/C it switches the lane from the x / B form
+  // to the general update, since x / B cannot hold a start state where B = 0.
+  const bool has_init = !SUMMARY && p.init != nullptr;
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
     const int c = cbase + i;
@@ -821,6 +835,11 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     for (int k = 0; k < K / 2; ++k) {
       a2p[i][k] = pk(a2[2 * k], a2[2 * k + 1]);
       x2[i][k] = pk(0.f, 0.f);
+      if (has_init && ch_ok[i]) {  // x-space start (fixed B/C then run the general update)
+        const float *xr = p.init + (long long)b * p.si[0] + (long long)dch[i] * p.si[1];
+        const int n = n0 + 2 * k;
+        x2[i][k] = pk(n < p.dstate ? xr[n] : 0.f, n + 1 < p.dstate ? xr[n + 1] : 0.f);
+      }
     }
     if (!SUMMARY && seg > 0) {
       // carry-in: fold the summaries of segments 0..seg-1 (state after segment
@@ -836,132 +855,161 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
           const float2 e = upk(mul2(l2, a2p[i][k]));
           const f2 dec = pk(ex2(e.x), ex2(e.y));
           const float2 xe = *reinterpret_cast<const float2 *>(wsx + kseg * NP + n0 + 2 * k);
-          x2[i][k] = fma2(dec, x2[i][k], pk(xe.x, xe.y));
+          f2 end = pk(xe.x, xe.y);
+          // fixed B/C summaries are x / B; the general update carries x itself
+          if (FIXED && has_init) end = mul2(pk(bfix[i][2 * k], bfix[i][2 * k + 1]), end);
+          x2[i][k] = fma2(dec, x2[i][k], end);
         }
       }
     }
   }
 
-  for (int q = 0; q < nsub; ++q) {
-    const int slot = q % NSLOT;
-    if (!mbar_wait(&bar_pfull[slot], (q / NSLOT) & 1, p.err, kErrWaitReady)) break;
-    if (!SUMMARY && q >= NSLOT && !mbar_wait(&bar_yempty[slot], ((q / NSLOT) - 1) & 1, p.err, kErrWaitEmpty)) break;
-    const float2 *P = reinterpret_cast<const float2 *>(smem + CF::OFF_P + slot * CF::P_SLOT);
-    const float *b32 = reinterpret_cast<const float *>(smem + CF::OFF_BC + slot * CF::BC_SLOT);
-    const float *c32 = b32 + S * NP;
-    const uint32_t *bcw = reinterpret_cast<const uint32_t *>(smem + CF::OFF_BC + slot * CF::BC_SLOT);
-    float *Y = reinterpret_cast<float *>(smem + CF::OFF_Y + slot * CF::Y_SLOT);
-    // Operands of step tl are loaded PF steps ahead into a register ring
-    // (raw words, converted when used); partial y's are stored in batches of
-    // YB steps, after the loads issued so far.
-#ifdef SSK_PF
-    constexpr int PF = SSK_PF;
-#else
-    constexpr int PF = Tune<T>::PF;
-#endif
-#ifdef SSK_YB
-    constexpr int YB = SSK_YB < S ? SSK_YB : S;
-#else
-    // fixed B/C and 8 states per lane hold more per-lane constants: 4-step batches
-    constexpr int YB0 = (FIXED || K > 4) && Tune<T>::YB > 4 ? 4 : Tune<T>::YB;
-    constexpr int YB = YB0 < S ? YB0 : S;
-#endif
-    static_assert(PF >= 1 && PF < S && S % YB == 0, "prefetch distance / y batch");
-    constexpr int NBW = (!FIXED && CF::BCPACK) ? K : 1;             // packed B/C words
-    constexpr int NBQ = (!FIXED && !CF::BCPACK) ? K / 4 : 1;        // fp32 B (and C) quads
-    float4 rp[PF + 1];
-    uint32_t rw[PF + 1][NBW];
-    float4 rb[PF + 1][NBQ], rc[PF + 1][NBQ];
-    auto load = [&](int tl, int r) {
-      if constexpr (CPL == 2) {
-        rp[r] = *reinterpret_cast<const float4 *>(P + tl * CH + cbase);
-      } else {
-        const float2 v = P[tl * CH + cbase];
-        rp[r] = make_float4(v.x, v.y, 0.f, 0.f);
-      }
-      if constexpr (!FIXED && CF::BCPACK) {
-        // K/2 words of B pairs then K/2 words of C pairs (16-byte loads)
+  // The sub-chunk loop, instantiated for the x / B form of fixed B/C and for
+  // the general update (variable B/C, or fixed B/C with a start state).
+  auto run = [&](auto general_tag) {
+    constexpr bool GEN = decltype(general_tag)::value;
+    f2 bf2[CPL][K / 2], cf2[CPL][K / 2];  // fixed B/C pairs for the general update
+    if constexpr (FIXED && GEN) {
 #pragma unroll
-        for (int q4 = 0; q4 < K / 4; ++q4) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(bcw + tl * NP + n0 + 4 * q4);
-          rw[r][4 * q4] = v.x; rw[r][4 * q4 + 1] = v.y; rw[r][4 * q4 + 2] = v.z; rw[r][4 * q4 + 3] = v.w;
-        }
-      } else if constexpr (!FIXED) {
-        // fp32 B, C for states n0+4q .. n0+4q+3 (one 16-byte load each)
-#pragma unroll
-        for (int q4 = 0; q4 < K / 4; ++q4) {
-          rb[r][q4] = *reinterpret_cast<const float4 *>(b32 + tl * NP + n0 + 4 * q4);
-          if constexpr (!SUMMARY) rc[r][q4] = *reinterpret_cast<const float4 *>(c32 + tl * NP + n0 + 4 * q4);
-        }
-      }
-    };
-    float yv[CPL][YB];
-#pragma unroll
-    for (int tl = 0; tl < PF; ++tl) load(tl, tl);
-#pragma unroll
-    for (int tl = 0; tl < S; ++tl) {
-      if (tl + PF < S) load(tl + PF, (tl + PF) % (PF + 1));
-      const int r = tl % (PF + 1);
-      // (dt, w) of my CPL adjacent channels
-      f2 dt2[CPL], w2[CPL];
-      dt2[0] = pk(rp[r].x, rp[r].x); w2[0] = pk(rp[r].y, rp[r].y);
-      if constexpr (CPL == 2) { dt2[1] = pk(rp[r].z, rp[r].z); w2[1] = pk(rp[r].w, rp[r].w); }
-      // B and C of my K states at this step, as fp32 state pairs
-      f2 bp[K / 2], cp[K / 2];
-      if constexpr (!FIXED && CF::BCPACK) {
+      for (int i = 0; i < CPL; ++i)
 #pragma unroll
         for (int k = 0; k < K / 2; ++k) {
-          const float2 bf = unpack2<T>(rw[r][k]);
-          bp[k] = pk(bf.x, bf.y);
-          if constexpr (!SUMMARY) {
-            const float2 cf = unpack2<T>(rw[r][K / 2 + k]);
-            cp[k] = pk(cf.x, cf.y);
+          const int n = n0 + 2 * k;
+          const float *cr = static_cast<const float *>(p.C) + (long long)dch[i] * p.sC[0];
+          bf2[i][k] = pk(bfix[i][2 * k], bfix[i][2 * k + 1]);
+          cf2[i][k] = pk(n < p.dstate ? cr[n] : 0.f, n + 1 < p.dstate ? cr[n + 1] : 0.f);
+        }
+    }
+    for (int q = 0; q < nsub; ++q) {
+      const int slot = q % NSLOT;
+      if (!mbar_wait(&bar_pfull[slot], (q / NSLOT) & 1, p.err, kErrWaitReady)) break;
+      if (!SUMMARY && q >= NSLOT && !mbar_wait(&bar_yempty[slot], ((q / NSLOT) - 1) & 1, p.err, kErrWaitEmpty)) break;
+      const float2 *P = reinterpret_cast<const float2 *>(smem + CF::OFF_P + slot * CF::P_SLOT);
+      const float *b32 = reinterpret_cast<const float *>(smem + CF::OFF_BC + slot * CF::BC_SLOT);
+      const float *c32 = b32 + S * NP;
+      const uint32_t *bcw = reinterpret_cast<const uint32_t *>(smem + CF::OFF_BC + slot * CF::BC_SLOT);
+      float *Y = reinterpret_cast<float *>(smem + CF::OFF_Y + slot * CF::Y_SLOT);
+      // Operands of step tl are loaded PF steps ahead into a register ring
+      // (raw words, converted when used); partial y's are stored in batches of
+      // YB steps, after the loads issued so far.
+  #ifdef SSK_PF
+      constexpr int PF = SSK_PF;
+  #else
+      constexpr int PF = Tune<T>::PF;
+  #endif
+  #ifdef SSK_YB
+      constexpr int YB = SSK_YB < S ? SSK_YB : S;
+  #else
+      // fixed B/C and 8 states per lane hold more per-lane constants: 4-step batches
+      constexpr int YB0 = (FIXED || K > 4) && Tune<T>::YB > 4 ? 4 : Tune<T>::YB;
+      constexpr int YB = YB0 < S ? YB0 : S;
+  #endif
+      static_assert(PF >= 1 && PF < S && S % YB == 0, "prefetch distance / y batch");
+      constexpr int NBW = (!FIXED && CF::BCPACK) ? K : 1;             // packed B/C words
+      constexpr int NBQ = (!FIXED && !CF::BCPACK) ? K / 4 : 1;        // fp32 B (and C) quads
+      float4 rp[PF + 1];
+      uint32_t rw[PF + 1][NBW];
+      float4 rb[PF + 1][NBQ], rc[PF + 1][NBQ];
+      auto load = [&](int tl, int r) {
+        if constexpr (CPL == 2) {
+          rp[r] = *reinterpret_cast<const float4 *>(P + tl * CH + cbase);
+        } else {
+          const float2 v = P[tl * CH + cbase];
+          rp[r] = make_float4(v.x, v.y, 0.f, 0.f);
+        }
+        if constexpr (!FIXED && CF::BCPACK) {
+          // K/2 words of B pairs then K/2 words of C pairs (16-byte loads)
+#pragma unroll
+          for (int q4 = 0; q4 < K / 4; ++q4) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(bcw + tl * NP + n0 + 4 * q4);
+            rw[r][4 * q4] = v.x; rw[r][4 * q4 + 1] = v.y; rw[r][4 * q4 + 2] = v.z; rw[r][4 * q4 + 3] = v.w;
+          }
+        } else if constexpr (!FIXED) {
+          // fp32 B, C for states n0+4q .. n0+4q+3 (one 16-byte load each)
+#pragma unroll
+          for (int q4 = 0; q4 < K / 4; ++q4) {
+            rb[r][q4] = *reinterpret_cast<const float4 *>(b32 + tl * NP + n0 + 4 * q4);
+            if constexpr (!SUMMARY) rc[r][q4] = *reinterpret_cast<const float4 *>(c32 + tl * NP + n0 + 4 * q4);
           }
         }
-      } else if constexpr (!FIXED) {
+      };
+      float yv[CPL][YB];
 #pragma unroll
-        for (int q4 = 0; q4 < K / 4; ++q4) {
-          bp[2 * q4] = pk(rb[r][q4].x, rb[r][q4].y); bp[2 * q4 + 1] = pk(rb[r][q4].z, rb[r][q4].w);
-          if constexpr (!SUMMARY) {
-            cp[2 * q4] = pk(rc[r][q4].x, rc[r][q4].y); cp[2 * q4 + 1] = pk(rc[r][q4].z, rc[r][q4].w);
+      for (int tl = 0; tl < PF; ++tl) load(tl, tl);
+#pragma unroll
+      for (int tl = 0; tl < S; ++tl) {
+        if (tl + PF < S) load(tl + PF, (tl + PF) % (PF + 1));
+        const int r = tl % (PF + 1);
+        // (dt, w) of my CPL adjacent channels
+        f2 dt2[CPL], w2[CPL];
+        dt2[0] = pk(rp[r].x, rp[r].x); w2[0] = pk(rp[r].y, rp[r].y);
+        if constexpr (CPL == 2) { dt2[1] = pk(rp[r].z, rp[r].z); w2[1] = pk(rp[r].w, rp[r].w); }
+        // B and C of my K states at this step, as fp32 state pairs
+        f2 bp[K / 2], cp[K / 2];
+        if constexpr (!FIXED && CF::BCPACK) {
+#pragma unroll
+          for (int k = 0; k < K / 2; ++k) {
+            const float2 bf = unpack2<T>(rw[r][k]);
+            bp[k] = pk(bf.x, bf.y);
+            if constexpr (!SUMMARY) {
+              const float2 cf = unpack2<T>(rw[r][K / 2 + k]);
+              cp[k] = pk(cf.x, cf.y);
+            }
+          }
+        } else if constexpr (!FIXED) {
+#pragma unroll
+          for (int q4 = 0; q4 < K / 4; ++q4) {
+            bp[2 * q4] = pk(rb[r][q4].x, rb[r][q4].y); bp[2 * q4 + 1] = pk(rb[r][q4].z, rb[r][q4].w);
+            if constexpr (!SUMMARY) {
+              cp[2 * q4] = pk(rc[r][q4].x, rc[r][q4].y); cp[2 * q4 + 1] = pk(rc[r][q4].z, rc[r][q4].w);
+            }
           }
         }
-      }
 #pragma unroll
-      for (int i = 0; i < CPL; ++i) {
-        f2 y2 = pk(0.f, 0.f);
+        for (int i = 0; i < CPL; ++i) {
+          f2 y2 = pk(0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < K / 2; ++k) {
-          const float2 e = upk(mul2(dt2[i], a2p[i][k]));
-          const f2 a = pk(ex2(e.x), ex2(e.y));
-          if constexpr (FIXED) {
-            x2[i][k] = fma2(a, x2[i][k], w2[i]);
-            if constexpr (!SUMMARY) y2 = fma2(cb2[i][k], x2[i][k], y2);
-          } else {
-            x2[i][k] = fma2(a, x2[i][k], mul2(w2[i], bp[k]));
-            if constexpr (!SUMMARY) y2 = fma2(cp[k], x2[i][k], y2);
+          for (int k = 0; k < K / 2; ++k) {
+            const float2 e = upk(mul2(dt2[i], a2p[i][k]));
+            const f2 a = pk(ex2(e.x), ex2(e.y));
+            if constexpr (FIXED && GEN) {
+              x2[i][k] = fma2(a, x2[i][k], mul2(w2[i], bf2[i][k]));
+              y2 = fma2(cf2[i][k], x2[i][k], y2);
+            } else if constexpr (FIXED) {
+              x2[i][k] = fma2(a, x2[i][k], w2[i]);
+              if constexpr (!SUMMARY) y2 = fma2(cb2[i][k], x2[i][k], y2);
+            } else {
+              x2[i][k] = fma2(a, x2[i][k], mul2(w2[i], bp[k]));
+              if constexpr (!SUMMARY) y2 = fma2(cp[k], x2[i][k], y2);
+            }
+          }
+          if constexpr (!SUMMARY) {
+            const float2 yy = upk(y2);
+            yv[i][tl % YB] = yy.x + yy.y;
           }
         }
         if constexpr (!SUMMARY) {
-          const float2 yy = upk(y2);
-          yv[i][tl % YB] = yy.x + yy.y;
+          if (tl % YB == YB - 1) {
+#pragma unroll
+            for (int u = 0; u < YB; ++u)
+#pragma unroll
+              for (int i = 0; i < CPL; ++i)  // step-major rows
+                Y[(tl - YB + 1 + u) * (CH * TN) + (cbase + i) * TN + j] = yv[i][u];
+          }
         }
       }
-      if constexpr (!SUMMARY) {
-        if (tl % YB == YB - 1) {
-#pragma unroll
-          for (int u = 0; u < YB; ++u)
-#pragma unroll
-            for (int i = 0; i < CPL; ++i)  // step-major rows
-              Y[(tl - YB + 1 + u) * (CH * TN) + (cbase + i) * TN + j] = yv[i][u];
-        }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar_pempty[slot]);
+        if constexpr (!SUMMARY) mbar_arrive(&bar_yfull[slot]);
       }
     }
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&bar_pempty[slot]);
-      if constexpr (!SUMMARY) mbar_arrive(&bar_yfull[slot]);
-    }
+  };
+  if constexpr (FIXED && !SUMMARY) {
+    if (has_init) run(std::true_type{});
+    else run(std::false_type{});
+  } else {
+    run(std::false_type{});
   }
 
   if constexpr (SUMMARY) {
@@ -985,7 +1033,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
 #pragma unroll
       for (int k = 0; k < K / 2; ++k) {
         float2 xv = upk(x2[i][k]);
-        if constexpr (FIXED) { xv.x *= bfix[i][2 * k]; xv.y *= bfix[i][2 * k + 1]; }
+        if (FIXED && !has_init) { xv.x *= bfix[i][2 * k]; xv.y *= bfix[i][2 * k + 1]; }
         const int n = n0 + 2 * k;
         if (n < p.dstate) lr[n * p.sl[2]] = xv.x;
         if (n + 1 < p.dstate) lr[(n + 1) * p.sl[2]] = xv.y;

@@ -85,6 +85,20 @@ int validate(const ss_fwd_params *p) {
   if (p->last_state && p->last_state_stride[2] != 1) return SS_ERR_STRIDE;
   for (int i = 0; i < 3; ++i)
     if (p->last_state && p->last_state_stride[i] < 0) return SS_ERR_STRIDE;
+  const int64_t szl[3] = {p->batch, p->dim, p->dstate};
+  Range last = p->last_state ? span(p->last_state, 4, szl, p->last_state_stride, 3) : Range{0, 0};
+  Range init{0, 0};
+  if (p->initial_state) {
+    if (p->initial_state_stride[2] != 1) return SS_ERR_STRIDE;
+    for (int i = 0; i < 3; ++i)
+      if (p->initial_state_stride[i] < 0) return SS_ERR_STRIDE;
+    if (!aligned(p->initial_state, 4)) return SS_ERR_ALIGN;
+    init = span(p->initial_state, 4, szl, p->initial_state_stride, 3);
+    // the start state may be last_state itself (same buffer and strides)
+    const bool same = p->last_state == p->initial_state && p->last_state_stride[0] == p->initial_state_stride[0] &&
+                      p->last_state_stride[1] == p->initial_state_stride[1];
+    if (!same && overlap(init, last)) return SS_ERR_ALIAS;
+  }
   if (p->seqlen == 0) return SS_OK;
   if (!p->u || !p->delta || !p->A || !p->B || !p->C || !p->out) return SS_ERR_NULL;
   const int64_t *st3[4] = {p->u_stride, p->delta_stride, p->z ? p->z_stride : p->u_stride, p->out_stride};
@@ -110,9 +124,7 @@ int validate(const ss_fwd_params *p) {
   // outputs must not overlap inputs or each other
   const int64_t sz3[3] = {p->batch, p->dim, p->seqlen};
   Range out = span(p->out, es, sz3, p->out_stride, 3);
-  const int64_t szl[3] = {p->batch, p->dim, p->dstate};
-  Range last = p->last_state ? span(p->last_state, 4, szl, p->last_state_stride, 3) : Range{0, 0};
-  Range ins[8];
+  Range ins[9];
   int ni = 0;
   ins[ni++] = span(p->u, es, sz3, p->u_stride, 3);
   ins[ni++] = span(p->delta, es, sz3, p->delta_stride, 3);
@@ -132,7 +144,8 @@ int validate(const ss_fwd_params *p) {
   if (p->delta_bias) ins[ni++] = span(p->delta_bias, 4, one, unit, 1);
   for (int i = 0; i < ni; ++i)
     if (overlap(out, ins[i]) || overlap(last, ins[i])) return SS_ERR_ALIAS;
-  if (overlap(out, last)) return SS_ERR_ALIAS;
+  if (overlap(out, last) || overlap(out, init)) return SS_ERR_ALIAS;
+  if (p->initial_state) ins[ni++] = init;  // the workspace must not overlap it either
   if (p->workspace_bytes < 0) return SS_ERR_SHAPE;
   if (p->workspace && p->workspace_bytes > 0) {
     const Range ws{reinterpret_cast<uintptr_t>(p->workspace),
@@ -223,12 +236,13 @@ int32_t *error_word_ptr(int dev) {
   return g_err_ptr[dev];
 }
 
-__global__ void zero_last_state(float *last, int64_t batch, int64_t dim, int64_t dstate, int64_t s0, int64_t s1,
-                                int64_t s2) {
+// seqlen == 0: last_state is the start state (or zero).
+__global__ void empty_sequence_state(float *last, const float *init, int64_t batch, int64_t dim, int64_t dstate,
+                                     int64_t s0, int64_t s1, int64_t s2, int64_t i0, int64_t i1) {
   const int64_t total = batch * dim * dstate;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = i % dstate, r = i / dstate, d = r % dim, b = r / dim;
-    last[b * s0 + d * s1 + n * s2] = 0.f;
+    last[b * s0 + d * s1 + n * s2] = init ? init[b * i0 + d * i1 + n] : 0.f;
   }
 }
 
@@ -314,8 +328,13 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
     if (fault_injected("launch")) return SS_ERR_CUDA;
     const int64_t total = p->batch * p->dim * p->dstate;
     const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 4096));
-    zero_last_state<<<blocks, 256, 0, stream>>>(p->last_state, p->batch, p->dim, p->dstate, p->last_state_stride[0],
-                                                p->last_state_stride[1], p->last_state_stride[2]);
+    if (p->initial_state == p->last_state && p->initial_state_stride[0] == p->last_state_stride[0] &&
+        p->initial_state_stride[1] == p->last_state_stride[1])
+      return SS_OK;  // in place: the start state already is the result
+    empty_sequence_state<<<blocks, 256, 0, stream>>>(p->last_state, p->initial_state, p->batch, p->dim, p->dstate,
+                                                     p->last_state_stride[0], p->last_state_stride[1],
+                                                     p->last_state_stride[2], p->initial_state_stride[0],
+                                                     p->initial_state_stride[1]);
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
   }
   int32_t *err = error_word_ptr(dev);
@@ -354,6 +373,8 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   }
   for (int i = 0; i < 4; ++i) { kp.sB[i] = p->B_stride[i]; kp.sC[i] = p->C_stride[i]; }
   kp.sA[0] = p->A_stride[0]; kp.sA[1] = p->A_stride[1];
+  kp.init = p->initial_state;
+  for (int i = 0; i < 3; ++i) kp.si[i] = p->initial_state ? p->initial_state_stride[i] : 0;
   kp.err = err;
 
   const int nsm = num_sms(dev);
@@ -518,6 +539,124 @@ bool host_layout_ok(const ss_fwd_params *p) {
   return true;
 }
 
+// ---------------------------------------------------------------------------
+// Decode step (ss_state_update)
+// ---------------------------------------------------------------------------
+int validate_su(const ss_state_update_params *p) {
+  if (!p) return SS_ERR_NULL;
+  if (p->abi_version != SS_ABI_VERSION) return SS_ERR_VERSION;
+  if (p->in_dtype < SS_F32 || p->in_dtype > SS_BF16) return SS_ERR_DTYPE;
+  if (p->bc_dtype < SS_F32 || p->bc_dtype > SS_BF16) return SS_ERR_DTYPE;
+  if (p->bc_mode != SS_BC_FIXED && p->bc_mode != SS_BC_VARIABLE) return SS_ERR_SHAPE;
+  const bool fixed = p->bc_mode == SS_BC_FIXED;
+  if (fixed && p->bc_dtype != SS_F32) return SS_ERR_DTYPE;
+  if (!fixed && p->bc_dtype != p->in_dtype && p->bc_dtype != SS_F32) return SS_ERR_DTYPE;
+  if (p->batch < 0 || p->dim < 0) return SS_ERR_SHAPE;
+  if (p->dstate < 1) return SS_ERR_SHAPE;
+  if (p->dstate > 64) return SS_ERR_UNSUPPORTED;
+  if (!fixed && (p->ngroups < 1 || (p->dim > 0 && p->dim % p->ngroups != 0))) return SS_ERR_SHAPE;
+  if (p->batch > (int64_t(1) << 30) || p->dim > (int64_t(1) << 30) || p->batch * p->dim > (int64_t(1) << 40))
+    return SS_ERR_UNSUPPORTED;
+  if (p->batch * p->dim == 0) return SS_OK;
+  if (!p->state || !p->u || !p->delta || !p->A || !p->B || !p->C || !p->out) return SS_ERR_NULL;
+  if (p->state_stride[2] != 1 || p->state_stride[0] < 0 || p->state_stride[1] < 0) return SS_ERR_STRIDE;
+  const int64_t *st2[4] = {p->u_stride, p->delta_stride, p->z ? p->z_stride : p->u_stride, p->out_stride};
+  for (auto st : st2)
+    if (st[0] < 0 || st[1] < 0) return SS_ERR_STRIDE;
+  if (p->A_stride[1] != 1 || p->A_stride[0] < 0) return SS_ERR_STRIDE;
+  if (fixed) {
+    if (p->B_stride[1] != 1 || p->C_stride[1] != 1 || p->B_stride[0] < 0 || p->C_stride[0] < 0) return SS_ERR_STRIDE;
+  } else {
+    for (int i = 0; i < 3; ++i)
+      if (p->B_stride[i] < 0 || p->C_stride[i] < 0) return SS_ERR_STRIDE;
+    if (p->B_stride[2] != 1 || p->C_stride[2] != 1) return SS_ERR_STRIDE;
+  }
+  const int es = elem_size(p->in_dtype), bs = elem_size(p->bc_dtype);
+  if (!aligned(p->u, es) || !aligned(p->delta, es) || !aligned(p->out, es) || (p->z && !aligned(p->z, es)))
+    return SS_ERR_ALIGN;
+  if (!aligned(p->B, bs) || !aligned(p->C, bs) || !aligned(p->A, 4) || !aligned(p->state, 4)) return SS_ERR_ALIGN;
+  if ((p->D && !aligned(p->D, 4)) || (p->delta_bias && !aligned(p->delta_bias, 4))) return SS_ERR_ALIGN;
+  const int64_t sz2[2] = {p->batch, p->dim};
+  const int64_t szs[3] = {p->batch, p->dim, p->dstate};
+  Range out = span(p->out, es, sz2, p->out_stride, 2);
+  Range state = span(p->state, 4, szs, p->state_stride, 3);
+  Range ins[8];
+  int ni = 0;
+  ins[ni++] = span(p->u, es, sz2, p->u_stride, 2);
+  ins[ni++] = span(p->delta, es, sz2, p->delta_stride, 2);
+  if (p->z) ins[ni++] = span(p->z, es, sz2, p->z_stride, 2);
+  const int64_t sza[2] = {p->dim, p->dstate};
+  ins[ni++] = span(p->A, 4, sza, p->A_stride, 2);
+  if (fixed) {
+    ins[ni++] = span(p->B, 4, sza, p->B_stride, 2);
+    ins[ni++] = span(p->C, 4, sza, p->C_stride, 2);
+  } else {
+    const int64_t szb[3] = {p->batch, p->ngroups, p->dstate};
+    ins[ni++] = span(p->B, bs, szb, p->B_stride, 3);
+    ins[ni++] = span(p->C, bs, szb, p->C_stride, 3);
+  }
+  const int64_t one[1] = {p->dim}, unit[1] = {1};
+  if (p->D) ins[ni++] = span(p->D, 4, one, unit, 1);
+  if (p->delta_bias) ins[ni++] = span(p->delta_bias, 4, one, unit, 1);
+  for (int i = 0; i < ni; ++i)
+    if (overlap(out, ins[i]) || overlap(state, ins[i])) return SS_ERR_ALIAS;
+  if (overlap(out, state)) return SS_ERR_ALIAS;
+  return SS_OK;
+}
+
+int launch_su(const ss_state_update_params *p, cudaStream_t stream) {
+  if (p->batch * p->dim == 0) return SS_OK;
+  const bool fixed = p->bc_mode == SS_BC_FIXED;
+  ssk::SUParams k{};
+  k.batch = static_cast<int>(p->batch);
+  k.dim = static_cast<int>(p->dim);
+  k.dstate = static_cast<int>(p->dstate);
+  k.dpg = fixed ? k.dim : static_cast<int>(p->dim / p->ngroups);
+  k.fixed = fixed;
+  k.has_z = p->z != nullptr;
+  k.has_D = p->D != nullptr;
+  k.has_bias = p->delta_bias != nullptr;
+  k.softplus = p->delta_softplus != 0;
+  k.state = p->state;
+  k.u = p->u; k.delta = p->delta; k.z = p->z; k.B = p->B; k.C = p->C;
+  k.A = p->A; k.D = p->D; k.bias = p->delta_bias;
+  k.out = p->out;
+  for (int i = 0; i < 3; ++i) k.sst[i] = p->state_stride[i];
+  for (int i = 0; i < 2; ++i) {
+    k.su[i] = p->u_stride[i]; k.sd[i] = p->delta_stride[i];
+    k.sz[i] = p->z ? p->z_stride[i] : 0; k.so[i] = p->out_stride[i]; k.sA[i] = p->A_stride[i];
+  }
+  for (int i = 0; i < 3; ++i) { k.sB[i] = p->B_stride[i]; k.sC[i] = p->C_stride[i]; }
+  // 16-byte state accesses when every row start is 16-byte aligned
+  k.vec = aligned(p->state, 16) && (p->state_stride[0] % 4 == 0 || p->batch == 1) &&
+          (p->state_stride[1] % 4 == 0 || p->dim == 1);
+  k.avec = aligned(p->A, 16) && (p->A_stride[0] % 4 == 0 || p->dim == 1);
+  {
+    // B/C rows: 4 values of the lane = 16 (fp32) or 8 (16-bit) bytes
+    const int bsz = elem_size(p->bc_dtype), need = 4 * bsz;
+    auto row_ok = [&](const void *base, const int64_t *st) {
+      if (!aligned(base, need)) return false;
+      if (fixed) return p->dim == 1 || (st[0] * bsz) % need == 0;
+      return (p->batch == 1 || (st[0] * bsz) % need == 0) && (p->ngroups == 1 || (st[1] * bsz) % need == 0);
+    };
+    k.bcvec = row_ok(p->B, p->B_stride) && row_ok(p->C, p->C_stride);
+  }
+  const int lanes = static_cast<int>((p->dstate + 3) / 4);
+  const int lpc = lanes <= 1 ? 1 : lanes <= 2 ? 2 : lanes <= 4 ? 4 : lanes <= 8 ? 8 : 16;
+  const bool bc_f32 = fixed || p->bc_dtype == SS_F32;
+  if (fault_injected("launch")) return SS_ERR_CUDA;
+  void *args[1] = {&k};
+  // grid: (channel tiles, batch rows [, batch rows beyond 65535])
+  const void *fn = ssk::state_update_kernel(p->in_dtype, bc_f32, lpc);
+  const int64_t gx = (p->dim + 256 / lpc - 1) / (256 / lpc);
+  const int64_t gy = std::min<int64_t>(p->batch, 65535), gz = (p->batch + gy - 1) / gy;
+  if (gx > 0x7fffffff || gz > 65535) return SS_ERR_UNSUPPORTED;
+  return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(gz)),
+                          dim3(256), args, 0, stream) == cudaSuccess
+             ? SS_OK
+             : SS_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -618,6 +757,14 @@ int ss_fwd_host(const ss_fwd_params *p, const void *h_u, const void *h_delta, co
       return SS_ERR_CUDA;
   }
   return SS_OK;
+}
+
+int ss_state_update_validate(const ss_state_update_params *p) { return validate_su(p); }
+
+int ss_state_update(const ss_state_update_params *p, void *stream) {
+  int st = validate_su(p);
+  if (st != SS_OK) return st;
+  return launch_su(p, static_cast<cudaStream_t>(stream));
 }
 
 int ss_device_error(int32_t *out_word, int clear) {

@@ -131,3 +131,61 @@ def compulsory_bytes(w: Workload) -> int:
     if w.return_last_state:
         total += 4 * w.batch * w.dim * w.dstate
     return total
+
+
+# ---------------------------------------------------------------------------
+# Decode step (one token per sequence against a resident state)
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    batch: int
+    dim: int
+    dstate: int
+    groups: int = 1            # B/C (batch, groups, dstate); 1 = (batch, dstate)
+    dtype: str = "bf16"        # u, delta, z, out and B/C
+    seed: int = 0
+
+    @property
+    def channels(self) -> int:
+        return self.batch * self.dim
+
+
+# Decode shapes of the same two Mamba layers (dim 1536 and 5120, dstate 16),
+# with batches large enough that one step streams tens of MB of state.
+DECODE_WORKLOADS = {
+    "decode130m_bf16": DecodeWorkload("decode130m_bf16", 256, 1536, 16, dtype="bf16", seed=11),
+    "decode2p8b_fp16": DecodeWorkload("decode2p8b_fp16", 64, 5120, 16, dtype="fp16", seed=12),
+}
+
+
+def make_decode_inputs(w: DecodeWorkload) -> dict:
+    """CPU tensors for one decode step, drawn in the order state, B, C, u,
+    delta, z, D, dt0 (same recipes as the forward workloads; the state is
+    N(0, 1)): state fp32 (b, d, n); u, delta, z (b, d) and B, C (b, [g,] n)
+    in the stored dtype; A, D, delta_bias fp32."""
+    rng = np.random.default_rng(w.seed)
+    f32 = np.float32
+    b, d, n, g = w.batch, w.dim, w.dstate, w.groups
+    st = rng.standard_normal((b, d, n), dtype=f32)
+    bc_shape = (b, n) if g == 1 else (b, g, n)
+    Bf = rng.standard_normal(bc_shape, dtype=f32)
+    Cf = rng.standard_normal(bc_shape, dtype=f32)
+    uf = rng.standard_normal((b, d), dtype=f32)
+    deltaf = rng.standard_normal((b, d), dtype=f32)
+    zf = rng.standard_normal((b, d), dtype=f32)
+    Df = rng.standard_normal(d, dtype=f32) * f32(0.1) + f32(1.0)
+    dt0 = rng.uniform(0.001, 0.1, size=d)
+    biasf = np.log(np.expm1(dt0)).astype(f32)
+    Af = -np.tile(np.arange(1, n + 1, dtype=f32), (d, 1))
+    return dict(state=torch.from_numpy(st), u=_cast(uf, w.dtype), delta=_cast(deltaf, w.dtype),
+                A=torch.from_numpy(Af), B=_cast(Bf, w.dtype), C=_cast(Cf, w.dtype),
+                D=torch.from_numpy(Df), z=_cast(zf, w.dtype), delta_bias=torch.from_numpy(biasf))
+
+
+def decode_compulsory_bytes(w: DecodeWorkload) -> int:
+    """Bytes one decode step must move: the fp32 state read and written,
+    u, delta, z and out, B/C once per (batch, group), A, D and delta_bias."""
+    s = torch.tensor([], dtype=_TORCH_DTYPES[w.dtype]).element_size()
+    return (8 * w.batch * w.dim * w.dstate + 4 * s * w.batch * w.dim
+            + 2 * s * w.batch * w.groups * w.dstate + 4 * w.dim * w.dstate + 8 * w.dim)

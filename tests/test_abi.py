@@ -30,7 +30,8 @@ def _declared_functions():
 def test_exports_every_declared_symbol(lib):
     names = _declared_functions()
     assert set(names) == {"ss_abi_version", "ss_status_string", "ss_fwd_validate", "ss_fwd",
-                          "ss_fwd_host", "ss_device_error", "ss_fwd_workspace_size", "ss_fwd_noalloc"}
+                          "ss_fwd_host", "ss_device_error", "ss_fwd_workspace_size", "ss_fwd_noalloc",
+                          "ss_state_update_validate", "ss_state_update"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -157,3 +158,90 @@ def test_complex_A_not_implemented():
     u = torch.zeros(1, 4, 8)
     with pytest.raises(NotImplementedError):
         api.normalise(u, u, torch.zeros(4, 4, dtype=torch.complex64), torch.zeros(1, 4, 8), torch.zeros(1, 4, 8))
+
+
+def test_initial_state_rules(lib):
+    """The forward's optional start state: state stride 1, 4-byte alignment, and
+    no overlap with out or (unless it is the very same buffer) last_state."""
+    p = _good()
+    base = p.out + (1 << 20)
+    p.initial_state = base
+    p.initial_state_stride[:] = [64 * 16, 16, 1]
+    assert _val(lib, p) == 0
+    p.initial_state_stride[2] = 2
+    assert _val(lib, p) == 4
+    p.initial_state_stride[:] = [64 * 16, 16, 1]
+    p.initial_state = base + 2
+    assert _val(lib, p) == 5
+    p.initial_state = p.out
+    assert _val(lib, p) == 6                                  # overlaps out
+    p.initial_state = p.last_state                            # in place: allowed
+    p.initial_state_stride[:] = list(p.last_state_stride)
+    assert _val(lib, p) == 0
+    p.initial_state = p.last_state + 64                       # partial overlap with last_state
+    assert _val(lib, p) == 6
+
+
+def _good_su():
+    """A valid decode-step problem with fake (never dereferenced) addresses."""
+    b, d, n, g = 4, 64, 16, 2
+    p = api.SSStateUpdateParams()
+    p.abi_version = api.SS_ABI_VERSION
+    p.in_dtype = p.bc_dtype = api.SS_BF16
+    p.bc_mode = api.SS_BC_VARIABLE
+    p.delta_softplus = 1
+    p.batch, p.dim, p.dstate, p.ngroups = b, d, n, g
+    cur = 1 << 40
+    addrs = {}
+    for k, nbytes in (("state", b * d * n * 4), ("u", b * d * 2), ("delta", b * d * 2), ("z", b * d * 2),
+                      ("B", b * g * n * 2), ("C", b * g * n * 2), ("A", d * n * 4), ("D", d * 4),
+                      ("delta_bias", d * 4), ("out", b * d * 2)):
+        addrs[k] = cur
+        cur += (nbytes + 255) // 256 * 256
+    for k, v in addrs.items():
+        setattr(p, k, v)
+    p.state_stride[:] = [d * n, n, 1]
+    for k in ("u_stride", "delta_stride", "z_stride", "out_stride"):
+        getattr(p, k)[:] = [d, 1]
+    p.B_stride[:] = [g * n, n, 1]
+    p.C_stride[:] = [g * n, n, 1]
+    p.A_stride[:] = [n, 1]
+    return p
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda p: None, 0),
+    (lambda p: setattr(p, "abi_version", 2), 10),
+    (lambda p: setattr(p, "state", None), 1),
+    (lambda p: setattr(p, "out", None), 1),
+    (lambda p: setattr(p, "in_dtype", 5), 3),
+    (lambda p: setattr(p, "bc_dtype", api.SS_F16), 3),
+    (lambda p: setattr(p, "ngroups", 3), 2),
+    (lambda p: setattr(p, "dstate", 0), 2),
+    (lambda p: setattr(p, "dstate", 65), 7),
+    (lambda p: p.state_stride.__setitem__(2, 2), 4),
+    (lambda p: p.B_stride.__setitem__(2, 2), 4),
+    (lambda p: p.u_stride.__setitem__(0, -1), 4),
+    (lambda p: setattr(p, "state", p.state + 2), 5),
+    (lambda p: setattr(p, "out", p.u), 6),                    # out aliases an input
+    (lambda p: setattr(p, "out", p.state + 64), 6),           # out inside the state
+    (lambda p: setattr(p, "state", p.A), 6),                  # state aliases an input
+    (lambda p: setattr(p, "batch", 0), 0),                    # empty: no-op
+])
+def test_state_update_validation(lib, mutate, status):
+    p = _good_su()
+    mutate(p)
+    assert lib.ss_state_update_validate(ctypes.byref(p)) == status
+    if status != 0:
+        assert lib.ss_state_update(ctypes.byref(p), None) == status
+
+
+def test_state_update_fixed_bc_rules(lib):
+    p = _good_su()
+    p.bc_mode = api.SS_BC_FIXED
+    p.bc_dtype = api.SS_F32
+    p.B_stride[:] = [16, 1, 0]
+    p.C_stride[:] = [16, 1, 0]
+    assert lib.ss_state_update_validate(ctypes.byref(p)) == 0
+    p.bc_dtype = api.SS_BF16
+    assert lib.ss_state_update_validate(ctypes.byref(p)) == 3
