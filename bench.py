@@ -477,15 +477,148 @@ def run_decode(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+CONV_METRIC = "causal conv1d fwd HBM GB/s (compulsory bytes / kernel time)"
+DEFAULT_CONV = "conv130m_bf16"
+
+
+def _conv_rate_oracle(w, x, budget_s):
+    """The numpy fp64 conv oracle on bounded row samples of the workload, for
+    about budget_s seconds; returns (GB/s in the bench metric, seconds, rows)."""
+    from oracle import conv1d
+    cb = workloads.conv_compulsory_bytes(w)
+    rows = w.batch * w.dim
+    per_row = cb / rows
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        b = n % w.batch
+        conv1d.causal_conv1d_ref(x["x"][b:b + 1, :64], x["weight"][:64], x["bias"][:64], activation="silu")
+        n += 64
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= rows:
+            return per_row * n / el / 1e9, el, n
+
+
+def run_conv(args, rank, world, local_rank):
+    """One causal conv1d forward (silu, bias) per bench step."""
+    import torch
+    from state_space_model_03_gb300 import api
+
+    name = args.workload if args.workload in workloads.CONV_WORKLOADS else DEFAULT_CONV
+    w = workloads.CONV_WORKLOADS[name]
+    x = workloads.make_conv_inputs(w)
+    cb = workloads.conv_compulsory_bytes(w)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        gbs, el, n = _conv_rate_oracle(w, x, max(1.0, args.cpu_budget))
+        cpu = {"value": gbs, "unit": "GB/s", "kind": "oracle", "cores": 1,
+               "sample": f"{n} of {w.batch * w.dim} rows of {w.name}, numpy fp64 oracle, {el:.1f} s"}
+        print(json.dumps({"impl": "reference", "metric": CONV_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1,
+                          "steps": 1, "warmup": 0, "ms_per_step": cb / (gbs * 1e9) * 1e3, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic (seeded, Mamba-layer shapes)",
+                          "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen,
+                                     "width": w.width},
+                          "cpu_baseline": cpu,
+                          "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = api.load_library()
+    d = {k: v.to(dev) for k, v in x.items()}
+    out = torch.empty(d["x"].shape, dtype=d["x"].dtype, device=dev)
+    params = api.make_conv1d_params(d["x"], d["weight"], d["bias"], None, None, None, out, "silu")
+    pref = ctypes.byref(params)
+    stream = torch.cuda.Stream(device=dev)
+    sptr = stream.cuda_stream
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def step():
+        st = lib.ss_causal_conv1d(pref, sptr)
+        if st != 0:
+            raise RuntimeError(api.status_string(st))
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            flush_buf.fill_(i & 0xFF)
+            step()
+    stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk, torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush_buf.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    kms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+    ms = max_over_ranks([sum(kms) / len(kms)], world, dev)[0]
+    gbs = job_rate(cb, world, ms) / 1e9
+    peak, peak_src = _peaks()
+    clocks = clk.summary()
+    # end to end: x from pinned host memory, the conv, out back to pinned host memory
+    hx = x["x"].pin_memory()
+    h_out = torch.empty(hx.shape, dtype=hx.dtype, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            d["x"].copy_(hx, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], world, dev)[0]
+    if rank != 0:
+        return
+    line = {
+        "metric": CONV_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {"fp32": "f32", "fp16": "f16", "bf16": "bf16"}[w.dtype],
+        "data": "synthetic (seeded, Mamba-layer shapes)",
+        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "width": w.width,
+                   "activation": "silu", "bias": True, "parallelism": f"independent x{world}",
+                   "l2": f"flushed before every step ({2 * l2 >> 20} MiB write, outside the kernel interval)"},
+        "elems_per_s": job_rate(w.elems, world, ms),
+        "compulsory_bytes_per_step": cb,
+        "roofline": {"bound": "hbm", "achieved": cb / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": cb / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src, "traffic": _traffic(w.name)},
+        "e2e": {"value": job_rate(cb, world, e2e_ms) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": hx.numel() * hx.element_size(),
+                "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "kernel_hash": _kernel_hash(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        gbs_cpu, el, n = _conv_rate_oracle(w, x, min(args.cpu_budget, 10.0))
+        line["cpu_baseline"] = {"value": gbs_cpu, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n} of {w.batch * w.dim} rows of {w.name}, numpy fp64 oracle, {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--op", default="scan", choices=["scan", "state_update"],
-                    help="scan: the selective-scan forward (the headline); state_update: one decode step")
+    ap.add_argument("--op", default="scan", choices=["scan", "state_update", "conv1d"],
+                    help="scan: the selective-scan forward (the headline); state_update: one decode step; "
+                         "conv1d: the causal conv1d forward")
     ap.add_argument("--workload", default=None,
-                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.DECODE_WORKLOADS))
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.DECODE_WORKLOADS)
+                    + sorted(workloads.CONV_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -493,6 +626,20 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = _env_int("RANK", 0), _env_int("WORLD_SIZE", 1), _env_int("LOCAL_RANK", 0)
+    if args.op == "conv1d":
+        if args.workload is not None and args.workload not in workloads.CONV_WORKLOADS:
+            ap.error("--op conv1d takes a conv workload")
+        if world > 1 and args.impl == "ours":
+            import torch
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl")
+        try:
+            run_conv(args, rank, world, local_rank)
+        finally:
+            if world > 1 and args.impl == "ours":
+                import torch
+                torch.distributed.destroy_process_group()
+        return
     if args.op == "state_update":
         if args.workload is not None and args.workload not in workloads.DECODE_WORKLOADS:
             ap.error("--op state_update takes a decode workload")

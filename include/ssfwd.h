@@ -238,6 +238,76 @@ int ss_state_update_validate(const ss_state_update_params *p);
 int ss_state_update(const ss_state_update_params *p, void *stream);
 
 /*
+ * Causal depthwise 1-D convolution, the `causal_conv1d_fn(x, weight, bias,
+ * seq_idx, initial_states, return_final_states, final_states_out,
+ * activation)` operator of the same page, section 4.2, which runs in front of
+ * the scan in a Mamba block. The page gives the operands; the computation
+ * taken is, per (batch b, channel d, step t) with kernel width W:
+ *
+ *     out[b,d,t] = act(bias[d] + sum_{k<W} weight[d,k] * x[b,d,t-(W-1)+k])
+ *
+ * where x at a position before 0 is initial_states[b,d,W-1+pos] (else 0), a
+ * position whose seq_idx differs from step t's counts as 0 (packed
+ * variable-length sequences), and act is the identity or silu (= swish,
+ * v / (1 + e^-v)). final_states[b,d,k] = the last W-1 inputs of the row,
+ * oldest first (initial states / zeros to the left of a short row).
+ *
+ *   x, out             (batch, dim, seqlen), dtype, seqlen stride 1.
+ *   weight             (dim, width) fp32, width stride 1; 2 <= width <= 4.
+ *   bias               (dim,) fp32 contiguous, or NULL.
+ *   seq_idx            (batch, seqlen) int32, seqlen stride 1, or NULL; not
+ *                      together with initial_states or final_states
+ *                      (SS_ERR_UNSUPPORTED), as on the page.
+ *   initial_states, final_states   (batch, dim, width-1) in dtype, or NULL.
+ *   activation         SS_ACT_NONE or SS_ACT_SILU.
+ * out and final_states must not overlap any input or each other.
+ */
+typedef enum ss_activation { SS_ACT_NONE = 0, SS_ACT_SILU = 1 } ss_activation;
+
+typedef struct ss_conv1d_params {
+  int32_t abi_version;      /* must be SS_ABI_VERSION */
+  int32_t dtype;            /* ss_dtype of x, out and the states */
+  int32_t activation;       /* ss_activation */
+  int32_t reserved0;
+  int64_t batch, dim, seqlen, width;
+  const void *x;
+  const float *weight, *bias;
+  const int32_t *seq_idx;
+  const void *initial_states;
+  void *final_states;
+  void *out;
+  int64_t x_stride[3], out_stride[3], weight_stride[2], seq_idx_stride[2];
+  int64_t initial_states_stride[3], final_states_stride[3];
+} ss_conv1d_params;
+
+int ss_causal_conv1d_validate(const ss_conv1d_params *p);
+int ss_causal_conv1d(const ss_conv1d_params *p, void *stream);
+
+/*
+ * One decode step of the convolution (the page's causal_conv1d_update):
+ * conv_state (batch, dim, width-1) holds the previous width-1 inputs, oldest
+ * first; with x (batch, dim) the new input,
+ *     out[b,d] = act(bias[d] + sum_{k<W-1} weight[d,k] conv_state[b,d,k] + weight[d,W-1] x[b,d])
+ * and conv_state shifts left by one with x appended (in place). The page's
+ * optional circular buffer (cache_seqlens) is not provided.
+ */
+typedef struct ss_conv1d_update_params {
+  int32_t abi_version;
+  int32_t dtype;            /* x, out, conv_state */
+  int32_t activation;
+  int32_t reserved0;
+  int64_t batch, dim, width;
+  const void *x;
+  void *conv_state;
+  const float *weight, *bias;
+  void *out;
+  int64_t x_stride[2], conv_state_stride[3], weight_stride[2], out_stride[2];
+} ss_conv1d_update_params;
+
+int ss_causal_conv1d_update_validate(const ss_conv1d_update_params *p);
+int ss_causal_conv1d_update(const ss_conv1d_update_params *p, void *stream);
+
+/*
  * Device-side error word of the library on the current device (nonzero after
  * a kernel gave up on a bounded wait or tripped a self-check; 0 otherwise).
  * Reading it synchronises with the device. `clear` nonzero resets it to 0.

@@ -70,9 +70,38 @@ class SSStateUpdateParams(ctypes.Structure):
     ]
 
 
+class SSConv1dParams(ctypes.Structure):
+    """Mirror of ``ss_conv1d_params``."""
+    _fields_ = [
+        ("abi_version", ctypes.c_int32), ("dtype", ctypes.c_int32), ("activation", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("width", ctypes.c_int64),
+        ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+        ("seq_idx", ctypes.c_void_p), ("initial_states", ctypes.c_void_p), ("final_states", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("x_stride", _i64x3), ("out_stride", _i64x3), ("weight_stride", _i64x2), ("seq_idx_stride", _i64x2),
+        ("initial_states_stride", _i64x3), ("final_states_stride", _i64x3),
+    ]
+
+
+class SSConv1dUpdateParams(ctypes.Structure):
+    """Mirror of ``ss_conv1d_update_params``."""
+    _fields_ = [
+        ("abi_version", ctypes.c_int32), ("dtype", ctypes.c_int32), ("activation", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("width", ctypes.c_int64),
+        ("x", ctypes.c_void_p), ("conv_state", ctypes.c_void_p), ("weight", ctypes.c_void_p),
+        ("bias", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("x_stride", _i64x2), ("conv_state_stride", _i64x3), ("weight_stride", _i64x2), ("out_stride", _i64x2),
+    ]
+
+
+SS_ACT_NONE, SS_ACT_SILU = 0, 1
+
+
 class SSError(RuntimeError):
     def __init__(self, status: int, msg: str):
-        super().__init__(f"ss_fwd failed: status {status} ({msg})")
+        super().__init__(f"libssfwd call failed: status {status} ({msg})")
         self.status = status
 
 
@@ -109,6 +138,15 @@ def load_library():
             lib.ss_state_update_validate.restype = ctypes.c_int
             lib.ss_state_update.argtypes = [PS, vp]
             lib.ss_state_update.restype = ctypes.c_int
+            PC, PU = ctypes.POINTER(SSConv1dParams), ctypes.POINTER(SSConv1dUpdateParams)
+            lib.ss_causal_conv1d_validate.argtypes = [PC]
+            lib.ss_causal_conv1d_validate.restype = ctypes.c_int
+            lib.ss_causal_conv1d.argtypes = [PC, vp]
+            lib.ss_causal_conv1d.restype = ctypes.c_int
+            lib.ss_causal_conv1d_update_validate.argtypes = [PU]
+            lib.ss_causal_conv1d_update_validate.restype = ctypes.c_int
+            lib.ss_causal_conv1d_update.argtypes = [PU, vp]
+            lib.ss_causal_conv1d_update.restype = ctypes.c_int
             lib.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
             lib.ss_device_error.restype = ctypes.c_int
             if lib.ss_abi_version() != SS_ABI_VERSION:
@@ -402,6 +440,107 @@ def selective_state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=
     stream = torch.cuda.current_stream(u.device).cuda_stream
     with torch.cuda.device(u.device):
         _check(lib.ss_state_update(ctypes.byref(p), stream))
+    return out
+
+
+def _activation(activation) -> int:
+    if activation is None:
+        return SS_ACT_NONE
+    if activation in ("silu", "swish"):
+        return SS_ACT_SILU
+    raise NotImplementedError("activation must be None, 'silu' or 'swish'")
+
+
+def make_conv1d_params(x, weight, bias, seq_idx, initial_states, final_states, out, activation) -> SSConv1dParams:
+    """Fill an ss_conv1d_params from CUDA tensors (no copies made)."""
+    if x.dim() != 3 or x.dtype not in _DT:
+        raise TypeError("x must be (batch, dim, seqlen) fp32/fp16/bf16")
+    batch, dim, seqlen = x.shape
+    if weight.dim() != 2 or weight.shape[0] != dim or weight.dtype != torch.float32:
+        raise TypeError("weight must be float32 (dim, width)")
+    width = weight.shape[1]
+    if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (dim,)):
+        raise TypeError("bias must be float32 (dim,)")
+    for name, t in (("initial_states", initial_states), ("final_states", final_states)):
+        if t is not None and (t.dtype != x.dtype or tuple(t.shape) != (batch, dim, width - 1)):
+            raise TypeError(f"{name} must be x's dtype (batch, dim, width - 1)")
+    if seq_idx is not None and (seq_idx.dtype != torch.int32 or tuple(seq_idx.shape) != (batch, seqlen)):
+        raise TypeError("seq_idx must be int32 (batch, seqlen)")
+    p = SSConv1dParams()
+    p.abi_version = SS_ABI_VERSION
+    p.dtype = _DT[x.dtype]
+    p.activation = _activation(activation)
+    p.batch, p.dim, p.seqlen, p.width = batch, dim, seqlen, width
+    p.x, p.weight, p.bias, p.seq_idx = _ptr(x), _ptr(weight), _ptr(bias), _ptr(seq_idx)
+    p.initial_states, p.final_states, p.out = _ptr(initial_states), _ptr(final_states), _ptr(out)
+    p.x_stride[:] = list(x.stride())
+    p.out_stride[:] = list(out.stride())
+    p.weight_stride[:] = list(weight.stride())
+    p.seq_idx_stride[:] = list(seq_idx.stride()) if seq_idx is not None else [0, 1]
+    p.initial_states_stride[:] = list(initial_states.stride()) if initial_states is not None else [0, 0, 1]
+    p.final_states_stride[:] = list(final_states.stride()) if final_states is not None else [0, 0, 1]
+    return p
+
+
+def causal_conv1d_fn(x, weight, bias=None, seq_idx=None, initial_states=None, return_final_states=False,
+                     final_states_out=None, activation=None):
+    """Causal depthwise conv1d on CUDA tensors (current stream), with the
+    signature of the page's causal_conv1d_fn: x (batch, dim, seqlen); weight
+    (dim, width) fp32, 2 <= width <= 4; bias (dim,) fp32; seq_idx (batch,
+    seqlen) int32; initial_states / final_states_out (batch, dim, width - 1) in
+    x's dtype; activation None, 'silu' or 'swish'. Returns out, or
+    (out, final_states) when return_final_states."""
+    if not x.is_cuda:
+        raise RuntimeError("causal_conv1d_fn needs CUDA tensors (there is no CPU path)")
+    lib = load_library()
+    _activation(activation)
+    if seq_idx is not None and (initial_states is not None or return_final_states):
+        raise ValueError("seq_idx cannot be combined with initial_states or return_final_states")
+    x = _unit_last(x)
+    weight = _unit_last(weight)
+    out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    fin = None
+    if return_final_states:
+        fin = final_states_out if final_states_out is not None else torch.empty(
+            (x.shape[0], x.shape[1], weight.shape[1] - 1), dtype=x.dtype, device=x.device)
+    p = make_conv1d_params(x, weight, bias, seq_idx, initial_states, fin, out, activation)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    with torch.cuda.device(x.device):
+        _check(lib.ss_causal_conv1d(ctypes.byref(p), stream))
+    return (out, fin) if return_final_states else out
+
+
+def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None):
+    """One decode step of the convolution on CUDA tensors: x (batch, dim) new
+    input, conv_state (batch, dim, width - 1) updated in place (oldest first).
+    Returns out (batch, dim)."""
+    if not x.is_cuda:
+        raise RuntimeError("causal_conv1d_update needs CUDA tensors (there is no CPU path)")
+    lib = load_library()
+    if x.dim() != 2 or x.dtype not in _DT:
+        raise TypeError("x must be (batch, dim) fp32/fp16/bf16")
+    batch, dim = x.shape
+    if weight.dim() != 2 or weight.shape[0] != dim or weight.dtype != torch.float32:
+        raise TypeError("weight must be float32 (dim, width)")
+    width = weight.shape[1]
+    if conv_state.dtype != x.dtype or tuple(conv_state.shape) != (batch, dim, width - 1):
+        raise TypeError("conv_state must be x's dtype (batch, dim, width - 1)")
+    if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (dim,)):
+        raise TypeError("bias must be float32 (dim,)")
+    out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    p = SSConv1dUpdateParams()
+    p.abi_version = SS_ABI_VERSION
+    p.dtype = _DT[x.dtype]
+    p.activation = _activation(activation)
+    p.batch, p.dim, p.width = batch, dim, width
+    p.x, p.conv_state, p.weight, p.bias, p.out = _ptr(x), _ptr(conv_state), _ptr(weight), _ptr(bias), _ptr(out)
+    p.x_stride[:] = list(x.stride())
+    p.conv_state_stride[:] = list(conv_state.stride())
+    p.weight_stride[:] = list(weight.stride())
+    p.out_stride[:] = list(out.stride())
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    with torch.cuda.device(x.device):
+        _check(lib.ss_causal_conv1d_update(ctypes.byref(p), stream))
     return out
 
 

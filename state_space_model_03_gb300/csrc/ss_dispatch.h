@@ -34,4 +34,30 @@ struct SUParams {
 };
 const void *state_update_kernel(int in_dtype, bool bc_f32, int lpc);
 
+// Causal depthwise conv1d (ss_causal_conv1d / ss_causal_conv1d_update).
+struct ConvParams {
+  int batch, dim, width;
+  long long seqlen;
+  int act;         // 0 identity, 1 silu
+  int xvec, ovec;  // 16-byte x loads / out stores allowed (aligned rows)
+  const void *x;
+  const float *weight, *bias;
+  const int *seq;  // seq_idx (batch, seqlen) or NULL
+  const void *init;  // (batch, dim, width-1) or NULL
+  void *fin;         // (batch, dim, width-1) or NULL
+  void *out;
+  long long sx[3], so[3], sw[2], sq[2], si[3], sf[3];
+};
+struct ConvUpdateParams {
+  int batch, dim, width, act;
+  const void *x;
+  void *state;
+  const float *weight, *bias;
+  void *out;
+  long long sx[2], ss[3], sw[2], so[2];
+};
+// ept: steps per thread of the forward (8); width 2..4.
+const void *conv1d_kernel(int dtype, int ept, int width);
+const void *conv1d_update_kernel(int dtype, int width);
+
 }  // namespace ssk

@@ -657,6 +657,160 @@ int launch_su(const ss_state_update_params *p, cudaStream_t stream) {
              : SS_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Causal depthwise conv1d (ss_causal_conv1d, ss_causal_conv1d_update)
+// ---------------------------------------------------------------------------
+int validate_conv(const ss_conv1d_params *p) {
+  if (!p) return SS_ERR_NULL;
+  if (p->abi_version != SS_ABI_VERSION) return SS_ERR_VERSION;
+  if (p->dtype < SS_F32 || p->dtype > SS_BF16) return SS_ERR_DTYPE;
+  if (p->activation != SS_ACT_NONE && p->activation != SS_ACT_SILU) return SS_ERR_UNSUPPORTED;
+  if (p->batch < 0 || p->dim < 0 || p->seqlen < 0 || p->width < 1) return SS_ERR_SHAPE;
+  if (p->width < 2 || p->width > 4) return SS_ERR_UNSUPPORTED;
+  if (p->batch > 65535 || p->dim > 65535 || p->seqlen > (int64_t(1) << 40)) return SS_ERR_UNSUPPORTED;
+  if (p->seq_idx && (p->initial_states || p->final_states)) return SS_ERR_UNSUPPORTED;
+  if (p->batch * p->dim == 0) return SS_OK;
+  if (!p->weight || (p->seqlen > 0 && (!p->out || !p->x))) return SS_ERR_NULL;
+  const int es = elem_size(p->dtype);
+  if (p->x_stride[2] != 1 || p->out_stride[2] != 1 || p->weight_stride[1] != 1) return SS_ERR_STRIDE;
+  for (int i = 0; i < 3; ++i)
+    if (p->x_stride[i] < 0 || p->out_stride[i] < 0 || (p->initial_states && p->initial_states_stride[i] < 0) ||
+        (p->final_states && p->final_states_stride[i] < 0))
+      return SS_ERR_STRIDE;
+  if (p->weight_stride[0] < 0 || (p->seq_idx && p->seq_idx_stride[0] < 0)) return SS_ERR_STRIDE;
+  if (p->seq_idx && p->seq_idx_stride[1] != 1) return SS_ERR_STRIDE;
+  if (!aligned(p->x, es) || !aligned(p->out, es) || !aligned(p->weight, 4) || (p->bias && !aligned(p->bias, 4)) ||
+      (p->seq_idx && !aligned(p->seq_idx, 4)) || (p->initial_states && !aligned(p->initial_states, es)) ||
+      (p->final_states && !aligned(p->final_states, es)))
+    return SS_ERR_ALIGN;
+  const int64_t sz3[3] = {p->batch, p->dim, p->seqlen}, szs[3] = {p->batch, p->dim, p->width - 1};
+  const int64_t szw[2] = {p->dim, p->width}, szq[2] = {p->batch, p->seqlen}, one[1] = {p->dim}, unit[1] = {1};
+  const Range out = span(p->out, es, sz3, p->out_stride, 3);
+  const Range fin = p->final_states ? span(p->final_states, es, szs, p->final_states_stride, 3) : Range{0, 0};
+  Range ins[5];
+  int ni = 0;
+  ins[ni++] = span(p->x, es, sz3, p->x_stride, 3);
+  ins[ni++] = span(p->weight, 4, szw, p->weight_stride, 2);
+  if (p->bias) ins[ni++] = span(p->bias, 4, one, unit, 1);
+  if (p->seq_idx) ins[ni++] = span(p->seq_idx, 4, szq, p->seq_idx_stride, 2);
+  if (p->initial_states) ins[ni++] = span(p->initial_states, es, szs, p->initial_states_stride, 3);
+  for (int i = 0; i < ni; ++i)
+    if (overlap(out, ins[i]) || overlap(fin, ins[i])) return SS_ERR_ALIAS;
+  if (overlap(out, fin)) return SS_ERR_ALIAS;
+  return SS_OK;
+}
+
+__global__ void conv_empty_final(ssk::ConvParams p, int es) {
+  // seqlen == 0: final states are the initial states (or zeros)
+  const int64_t total = (int64_t)p.batch * p.dim * (p.width - 1);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t k = i % (p.width - 1), r = i / (p.width - 1), d = r % p.dim, b = r / p.dim;
+    unsigned char *dst = static_cast<unsigned char *>(p.fin) + (b * p.sf[0] + d * p.sf[1] + k * p.sf[2]) * es;
+    const unsigned char *src = p.init ? static_cast<const unsigned char *>(p.init) + (b * p.si[0] + d * p.si[1] + k * p.si[2]) * es : nullptr;
+    for (int j = 0; j < es; ++j) dst[j] = src ? src[j] : 0;
+  }
+}
+
+int launch_conv(const ss_conv1d_params *p, cudaStream_t stream) {
+  if (p->batch * p->dim == 0) return SS_OK;
+  ssk::ConvParams k{};
+  k.batch = static_cast<int>(p->batch);
+  k.dim = static_cast<int>(p->dim);
+  k.width = static_cast<int>(p->width);
+  k.seqlen = p->seqlen;
+  k.act = p->activation == SS_ACT_SILU;
+  k.x = p->x; k.weight = p->weight; k.bias = p->bias; k.seq = p->seq_idx;
+  k.init = p->initial_states; k.fin = p->final_states; k.out = p->out;
+  for (int i = 0; i < 3; ++i) {
+    k.sx[i] = p->x_stride[i]; k.so[i] = p->out_stride[i];
+    k.si[i] = p->initial_states_stride[i]; k.sf[i] = p->final_states_stride[i];
+  }
+  for (int i = 0; i < 2; ++i) { k.sw[i] = p->weight_stride[i]; k.sq[i] = p->seq_idx_stride[i]; }
+  const int es = elem_size(p->dtype);
+  auto rows16 = [&](const void *base, const int64_t *st) {
+    return aligned(base, 16) && (p->batch == 1 || (st[0] * es) % 16 == 0) && (p->dim == 1 || (st[1] * es) % 16 == 0);
+  };
+  k.xvec = rows16(p->x, p->x_stride);
+  k.ovec = rows16(p->out, p->out_stride);
+  if (fault_injected("launch")) return SS_ERR_CUDA;
+  void *args[1] = {&k};
+  if (p->seqlen == 0) {
+    if (!p->final_states) return SS_OK;
+    const int64_t total = p->batch * p->dim * (p->width - 1);
+    const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 4096));
+    void *a2[2] = {&k, const_cast<int *>(&es)};
+    return cudaLaunchKernel(reinterpret_cast<const void *>(&conv_empty_final), dim3(blocks), dim3(256), a2, 0,
+                            stream) == cudaSuccess
+               ? SS_OK
+               : SS_ERR_CUDA;
+  }
+  // 8 steps per thread (16 steps measured the same on 8192-step rows and
+  // 18% slower on 2048-step rows)
+  const int ept = 8;
+  const void *fn = ssk::conv1d_kernel(p->dtype, ept, static_cast<int>(p->width));
+  const int64_t gx = (p->seqlen + 256 * ept - 1) / (256 * ept);
+  if (gx > 0x7fffffff) return SS_ERR_UNSUPPORTED;
+  return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(p->dim),
+                                   static_cast<unsigned>(p->batch)),
+                          dim3(256), args, 0, stream) == cudaSuccess
+             ? SS_OK
+             : SS_ERR_CUDA;
+}
+
+int validate_conv_update(const ss_conv1d_update_params *p) {
+  if (!p) return SS_ERR_NULL;
+  if (p->abi_version != SS_ABI_VERSION) return SS_ERR_VERSION;
+  if (p->dtype < SS_F32 || p->dtype > SS_BF16) return SS_ERR_DTYPE;
+  if (p->activation != SS_ACT_NONE && p->activation != SS_ACT_SILU) return SS_ERR_UNSUPPORTED;
+  if (p->batch < 0 || p->dim < 0 || p->width < 1) return SS_ERR_SHAPE;
+  if (p->width < 2 || p->width > 4) return SS_ERR_UNSUPPORTED;
+  if (p->batch > 65535 || p->dim > (int64_t(1) << 30)) return SS_ERR_UNSUPPORTED;
+  if (p->batch * p->dim == 0) return SS_OK;
+  if (!p->x || !p->conv_state || !p->weight || !p->out) return SS_ERR_NULL;
+  if (p->weight_stride[1] != 1) return SS_ERR_STRIDE;
+  for (int i = 0; i < 2; ++i)
+    if (p->x_stride[i] < 0 || p->out_stride[i] < 0 || p->weight_stride[i] < 0) return SS_ERR_STRIDE;
+  for (int i = 0; i < 3; ++i)
+    if (p->conv_state_stride[i] < 0) return SS_ERR_STRIDE;
+  const int es = elem_size(p->dtype);
+  if (!aligned(p->x, es) || !aligned(p->out, es) || !aligned(p->conv_state, es) || !aligned(p->weight, 4) ||
+      (p->bias && !aligned(p->bias, 4)))
+    return SS_ERR_ALIGN;
+  const int64_t sz2[2] = {p->batch, p->dim}, szs[3] = {p->batch, p->dim, p->width - 1};
+  const int64_t szw[2] = {p->dim, p->width}, one[1] = {p->dim}, unit[1] = {1};
+  const Range out = span(p->out, es, sz2, p->out_stride, 2);
+  const Range st = span(p->conv_state, es, szs, p->conv_state_stride, 3);
+  Range ins[3];
+  int ni = 0;
+  ins[ni++] = span(p->x, es, sz2, p->x_stride, 2);
+  ins[ni++] = span(p->weight, 4, szw, p->weight_stride, 2);
+  if (p->bias) ins[ni++] = span(p->bias, 4, one, unit, 1);
+  for (int i = 0; i < ni; ++i)
+    if (overlap(out, ins[i]) || overlap(st, ins[i])) return SS_ERR_ALIAS;
+  if (overlap(out, st)) return SS_ERR_ALIAS;
+  return SS_OK;
+}
+
+int launch_conv_update(const ss_conv1d_update_params *p, cudaStream_t stream) {
+  if (p->batch * p->dim == 0) return SS_OK;
+  ssk::ConvUpdateParams k{};
+  k.batch = static_cast<int>(p->batch);
+  k.dim = static_cast<int>(p->dim);
+  k.width = static_cast<int>(p->width);
+  k.act = p->activation == SS_ACT_SILU;
+  k.x = p->x; k.state = p->conv_state; k.weight = p->weight; k.bias = p->bias; k.out = p->out;
+  for (int i = 0; i < 2; ++i) { k.sx[i] = p->x_stride[i]; k.sw[i] = p->weight_stride[i]; k.so[i] = p->out_stride[i]; }
+  for (int i = 0; i < 3; ++i) k.ss[i] = p->conv_state_stride[i];
+  if (fault_injected("launch")) return SS_ERR_CUDA;
+  void *args[1] = {&k};
+  const void *fn = ssk::conv1d_update_kernel(p->dtype, static_cast<int>(p->width));
+  const int64_t gx = (p->dim + 255) / 256;
+  return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(p->batch)), dim3(256), args, 0,
+                          stream) == cudaSuccess
+             ? SS_OK
+             : SS_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -765,6 +919,22 @@ int ss_state_update(const ss_state_update_params *p, void *stream) {
   int st = validate_su(p);
   if (st != SS_OK) return st;
   return launch_su(p, static_cast<cudaStream_t>(stream));
+}
+
+int ss_causal_conv1d_validate(const ss_conv1d_params *p) { return validate_conv(p); }
+
+int ss_causal_conv1d(const ss_conv1d_params *p, void *stream) {
+  int st = validate_conv(p);
+  if (st != SS_OK) return st;
+  return launch_conv(p, static_cast<cudaStream_t>(stream));
+}
+
+int ss_causal_conv1d_update_validate(const ss_conv1d_update_params *p) { return validate_conv_update(p); }
+
+int ss_causal_conv1d_update(const ss_conv1d_update_params *p, void *stream) {
+  int st = validate_conv_update(p);
+  if (st != SS_OK) return st;
+  return launch_conv_update(p, static_cast<cudaStream_t>(stream));
 }
 
 int ss_device_error(int32_t *out_word, int clear) {

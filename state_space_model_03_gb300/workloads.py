@@ -189,3 +189,46 @@ def decode_compulsory_bytes(w: DecodeWorkload) -> int:
     s = torch.tensor([], dtype=_TORCH_DTYPES[w.dtype]).element_size()
     return (8 * w.batch * w.dim * w.dstate + 4 * s * w.batch * w.dim
             + 2 * s * w.batch * w.groups * w.dstate + 4 * w.dim * w.dstate + 8 * w.dim)
+
+
+# ---------------------------------------------------------------------------
+# Causal depthwise conv1d (the convolution in front of the scan)
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class ConvWorkload:
+    name: str
+    batch: int
+    dim: int
+    seqlen: int
+    width: int = 4
+    dtype: str = "bf16"
+    seed: int = 0
+
+    @property
+    def elems(self) -> int:
+        return self.batch * self.dim * self.seqlen
+
+
+# The two Mamba layers' convolutions (same batch, channels and length as the
+# forward workloads), width 4, silu activation, with bias.
+CONV_WORKLOADS = {
+    "conv130m_bf16": ConvWorkload("conv130m_bf16", 8, 1536, 2048, 4, "bf16", seed=21),
+    "conv2p8b_fp16": ConvWorkload("conv2p8b_fp16", 2, 5120, 8192, 4, "fp16", seed=22),
+}
+
+
+def make_conv_inputs(w: ConvWorkload) -> dict:
+    """x (b, d, l) in the stored dtype ~ N(0, 1); weight (d, width) fp32 ~
+    N(0, 1) / sqrt(width); bias (d,) fp32 ~ N(0, 0.1); drawn in that order."""
+    rng = np.random.default_rng(w.seed)
+    f32 = np.float32
+    xf = rng.standard_normal((w.batch, w.dim, w.seqlen), dtype=f32)
+    wf = rng.standard_normal((w.dim, w.width), dtype=f32) * f32(1.0 / np.sqrt(w.width))
+    bf = rng.standard_normal(w.dim, dtype=f32) * f32(0.1)
+    return dict(x=_cast(xf, w.dtype), weight=torch.from_numpy(wf), bias=torch.from_numpy(bf))
+
+
+def conv_compulsory_bytes(w: ConvWorkload) -> int:
+    """x read and out written once, plus weight and bias."""
+    s = torch.tensor([], dtype=_TORCH_DTYPES[w.dtype]).element_size()
+    return 2 * s * w.elems + 4 * w.dim * w.width + 4 * w.dim

@@ -24,14 +24,15 @@ def lib():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ss_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(ss_[a-z_0-9]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(lib):
     names = _declared_functions()
     assert set(names) == {"ss_abi_version", "ss_status_string", "ss_fwd_validate", "ss_fwd",
                           "ss_fwd_host", "ss_device_error", "ss_fwd_workspace_size", "ss_fwd_noalloc",
-                          "ss_state_update_validate", "ss_state_update"}
+                          "ss_state_update_validate", "ss_state_update", "ss_causal_conv1d_validate",
+                          "ss_causal_conv1d", "ss_causal_conv1d_update_validate", "ss_causal_conv1d_update"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -245,3 +246,65 @@ def test_state_update_fixed_bc_rules(lib):
     assert lib.ss_state_update_validate(ctypes.byref(p)) == 0
     p.bc_dtype = api.SS_BF16
     assert lib.ss_state_update_validate(ctypes.byref(p)) == 3
+
+
+def _good_conv():
+    b, d, l, w = 2, 64, 128, 4
+    p = api.SSConv1dParams()
+    p.abi_version = api.SS_ABI_VERSION
+    p.dtype = api.SS_BF16
+    p.activation = api.SS_ACT_SILU
+    p.batch, p.dim, p.seqlen, p.width = b, d, l, w
+    cur = 1 << 40
+    for k, nbytes in (("x", b * d * l * 2), ("weight", d * w * 4), ("bias", d * 4), ("out", b * d * l * 2)):
+        setattr(p, k, cur)
+        cur += (nbytes + 255) // 256 * 256
+    p.x_stride[:] = [d * l, l, 1]
+    p.out_stride[:] = [d * l, l, 1]
+    p.weight_stride[:] = [w, 1]
+    return p, cur
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda p, c: None, 0),
+    (lambda p, c: setattr(p, "width", 5), 7),
+    (lambda p, c: setattr(p, "width", 1), 7),
+    (lambda p, c: setattr(p, "activation", 2), 7),
+    (lambda p, c: setattr(p, "dtype", 9), 3),
+    (lambda p, c: setattr(p, "x", None), 1),
+    (lambda p, c: p.x_stride.__setitem__(2, 2), 4),
+    (lambda p, c: setattr(p, "out", p.x), 6),
+    (lambda p, c: setattr(p, "out", p.x + 2), 6),
+    (lambda p, c: setattr(p, "x", p.x + 1), 5),
+    (lambda p, c: (setattr(p, "seq_idx", c), setattr(p, "final_states", c + 4096),
+                   p.seq_idx_stride.__setitem__(slice(0, 2), [128, 1]),
+                   p.final_states_stride.__setitem__(slice(0, 3), [192, 3, 1])), 7),
+    (lambda p, c: (setattr(p, "final_states", p.weight),
+                   p.final_states_stride.__setitem__(slice(0, 3), [192, 3, 1])), 6),
+    (lambda p, c: setattr(p, "seqlen", -1), 2),
+])
+def test_conv1d_validation(lib, mutate, status):
+    p, cur = _good_conv()
+    mutate(p, cur)
+    assert lib.ss_causal_conv1d_validate(ctypes.byref(p)) == status
+    if status != 0:
+        assert lib.ss_causal_conv1d(ctypes.byref(p), None) == status
+
+
+def test_conv1d_update_validation(lib):
+    p = api.SSConv1dUpdateParams()
+    p.abi_version = api.SS_ABI_VERSION
+    p.dtype = api.SS_F32
+    p.batch, p.dim, p.width = 2, 16, 3
+    base = 1 << 40
+    p.x, p.conv_state, p.weight, p.out = base, base + 4096, base + 8192, base + 12288
+    p.x_stride[:] = [16, 1]
+    p.conv_state_stride[:] = [32, 2, 1]
+    p.weight_stride[:] = [3, 1]
+    p.out_stride[:] = [16, 1]
+    assert lib.ss_causal_conv1d_update_validate(ctypes.byref(p)) == 0
+    p.out = p.conv_state
+    assert lib.ss_causal_conv1d_update_validate(ctypes.byref(p)) == 6
+    p.out = base + 12288
+    p.width = 6
+    assert lib.ss_causal_conv1d_update_validate(ctypes.byref(p)) == 7
