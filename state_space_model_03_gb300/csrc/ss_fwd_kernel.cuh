@@ -689,10 +689,11 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     T *gout = static_cast<T *>(p.out);
     const long long orow = (long long)b * p.so[0] + (long long)d * p.so[1];
     const bool out_vec = p.out_vec != 0;
-    // SUMMARY: sum of dt over my steps of the segment, accumulated in fp64:
-    // the forward decays the carried state by exp(A * sum), and an fp32 sum
-    // over thousands of steps would be off by ~1e-4 relative
-    double lam = 0.0;
+    // SUMMARY: sum of dt over my steps of the segment. The forward decays the
+    // carried state by exp(A * sum), and a plain fp32 sum over thousands of
+    // steps is off by ~1e-4 relative, so it is compensated (Kahan); fp64 adds
+    // run at a small fraction of the fp32 rate on this part.
+    float lam = 0.f, lam_c = 0.f;
     // prep of sub-chunk q: (dt, w) and the sub-chunk's B/C into slot q % NSLOT
     auto prep = [&](int q) -> bool {
       const int ci = q / SUBS, sub = q - ci * SUBS, s = ci % STAGES;
@@ -713,7 +714,12 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         float dt = softplus ? softplus_t<T>(v) : v;
         float w = dt * uv[k];
         if (t0 + k >= tseg1) { dt = 0.f; w = 0.f; }  // padded steps leave x unchanged
-        if constexpr (SUMMARY) lam += static_cast<double>(dt);
+        if constexpr (SUMMARY) {
+          const float yk = dt - lam_c;
+          const float tk = lam + yk;
+          lam_c = (tk - lam) - yk;
+          lam = tk;
+        }
         P[(h * EPT + k) * CH + c] = make_float2(dt, w);
       }
       if constexpr (!CF::PPACK) convert_bc(q, le, WE * 32);
@@ -778,9 +784,10 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         }
       }
       // the two half-lanes of a channel (8 lanes apart): combine their step sums
+      lam -= lam_c;  // fold the compensation in before combining the halves
       lam += __shfl_xor_sync(0xffffffffu, lam, 8);
       if (ok && h == 0 && ch_ok)
-        p.ws[(long long)nsum * NP * p.batch * p.dim + ((long long)b * p.dim + d) * nsum + seg] = static_cast<float>(lam);
+        p.ws[(long long)nsum * NP * p.batch * p.dim + ((long long)b * p.dim + d) * nsum + seg] = lam;
     } else {
       // prep runs NSLOT - 1 sub-chunks ahead of the epilogue
       bool ok = true;
