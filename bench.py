@@ -58,16 +58,25 @@ def _peaks():
     return 6800.0, "fallback"
 
 
-def _kernel_hash():
+# Sources that define each timed kernel (its traffic record stays valid while
+# these files are unchanged).
+KERNEL_SOURCES = {
+    "scan": ("ss_fwd_kernel.cuh", "ss_fwd_f32.cu", "ss_fwd_f16.cu", "ss_fwd_bf16.cu"),
+    "state_update": ("ss_state_update.cu",),
+    "conv1d": ("ss_conv1d.cu",),
+}
+
+
+def _kernel_hash(op="scan"):
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "state_space_model_03_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
+    for name in KERNEL_SOURCES[op]:
+        with open(os.path.join(ROOT, "state_space_model_03_gb300", "csrc", name), "rb") as fh:
+            h.update(name.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def _traffic(workload):
+def _traffic(workload, op="scan"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel sources and this workload; else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -76,7 +85,7 @@ def _traffic(workload):
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("kernel_hash") != _kernel_hash():
+    if not e or e.get("kernel_hash") != _kernel_hash(op):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -462,13 +471,14 @@ def run_decode(args, rank, world, local_rank):
                    "l2": f"flushed before every step ({2 * l2 >> 20} MiB write, outside the kernel interval)"},
         "compulsory_bytes_per_step": cb,
         "roofline": {"bound": "hbm", "achieved": cb / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
-                     "frac": cb / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src, "traffic": _traffic(w.name)},
+                     "frac": cb / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
+                     "traffic": _traffic(w.name, "state_update")},
         "e2e": {"value": job_rate(cb, world, e2e_ms) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h_out.numel() * h_out.element_size(),
                 "steps": e2e_steps},
         "gpu_launches": args.steps,
         "clocks": clocks,
-        "kernel_hash": _kernel_hash(),
+        "kernel_hash": _kernel_hash("state_update"),
     }
     if world == 1 and not args.no_cpu_baseline:
         gbs_cpu, el, n = _decode_rate_oracle(w, x, min(args.cpu_budget, 10.0))
@@ -593,13 +603,14 @@ def run_conv(args, rank, world, local_rank):
         "elems_per_s": job_rate(w.elems, world, ms),
         "compulsory_bytes_per_step": cb,
         "roofline": {"bound": "hbm", "achieved": cb / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
-                     "frac": cb / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src, "traffic": _traffic(w.name)},
+                     "frac": cb / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
+                     "traffic": _traffic(w.name, "conv1d")},
         "e2e": {"value": job_rate(cb, world, e2e_ms) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": hx.numel() * hx.element_size(),
                 "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": e2e_steps},
         "gpu_launches": args.steps,
         "clocks": clocks,
-        "kernel_hash": _kernel_hash(),
+        "kernel_hash": _kernel_hash("conv1d"),
     }
     if world == 1 and not args.no_cpu_baseline:
         gbs_cpu, el, n = _conv_rate_oracle(w, x, min(args.cpu_budget, 10.0))
