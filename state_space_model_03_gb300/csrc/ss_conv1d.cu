@@ -29,19 +29,21 @@ __device__ __forceinline__ float act_f(float v, int act) {
 // x row value at step t of (b, d): x itself for t >= 0, else the initial state
 // (or 0).
 template <typename T>
-__device__ __forceinline__ float left_value(const ConvParams &p, const T *xrow, int b, int d, long long t) {
+__device__ __forceinline__ float left_value(const ConvParams &p, const T *xrow, int b, int d, int t) {
   if (t >= 0) return to_f<T>(xrow[t]);
   if (!p.init) return 0.f;
-  const long long k = (long long)(p.width - 1) + t;  // 0 .. W-2
+  const int k = p.width - 1 + t;  // 0 .. W-2
   return to_f<T>(static_cast<const T *>(p.init)[b * p.si[0] + (long long)d * p.si[1] + k * p.si[2]]);
 }
 
-template <typename T, int EPT, int W>  // W: kernel width (2..4)
+// W: kernel width (2..4); SEQ: packed sequences (seq_idx) present.
+template <typename T, int EPT, int W, bool SEQ>
 __global__ void __launch_bounds__(kConvThreads) ss_conv1d_kernel(const __grid_constant__ ConvParams p) {
   constexpr int H = W - 1;
   const int d = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31;
-  const long long t0 = ((long long)blockIdx.x * kConvThreads + threadIdx.x) * EPT;
+  const int seqlen = (int)p.seqlen;  // < 2^31 (checked by the host)
+  const int t0 = (blockIdx.x * kConvThreads + threadIdx.x) * EPT;
   const T *xrow = static_cast<const T *>(p.x) + b * p.sx[0] + (long long)d * p.sx[1];
   T *orow = static_cast<T *>(p.out) + b * p.so[0] + (long long)d * p.so[1];
   float w[W];
@@ -51,7 +53,7 @@ __global__ void __launch_bounds__(kConvThreads) ss_conv1d_kernel(const __grid_co
 
   // this thread's inputs (zeros past the end of the row)
   float v[EPT];
-  const bool full = t0 + EPT <= p.seqlen;
+  const bool full = t0 + EPT <= seqlen;
   if (full && p.xvec) {
     constexpr int NW = EPT * (int)sizeof(T) / 16;  // 16-byte words
 #pragma unroll
@@ -71,7 +73,7 @@ __global__ void __launch_bounds__(kConvThreads) ss_conv1d_kernel(const __grid_co
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < EPT; ++i) v[i] = t0 + i < p.seqlen ? to_f<T>(xrow[t0 + i]) : 0.f;
+    for (int i = 0; i < EPT; ++i) v[i] = t0 + i < seqlen ? to_f<T>(xrow[t0 + i]) : 0.f;
   }
   // the H (<= 3) inputs to the left: from the previous lane's last values,
   // lane 0 (or the row start) reads them itself
@@ -79,23 +81,22 @@ __global__ void __launch_bounds__(kConvThreads) ss_conv1d_kernel(const __grid_co
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
     const float up = __shfl_up_sync(0xffffffffu, v[EPT - 3 + k], 1);
-    const long long t = t0 - 3 + k;
-    h[k] = (lane > 0) ? up : (t0 < p.seqlen ? left_value<T>(p, xrow, b, d, t) : 0.f);
+    h[k] = (lane > 0) ? up : (t0 < seqlen ? left_value<T>(p, xrow, b, d, t0 - 3 + k) : 0.f);
   }
   // sequence ids of the EPT positions and the 3 to the left
   int sid[EPT], hs[3];
-  if (p.seq) {
+  if constexpr (SEQ) {
     const int *srow = p.seq + b * p.sq[0];
 #pragma unroll
-    for (int i = 0; i < EPT; ++i) sid[i] = t0 + i < p.seqlen ? srow[t0 + i] : -1;
+    for (int i = 0; i < EPT; ++i) sid[i] = t0 + i < seqlen ? srow[t0 + i] : -1;
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
       const int up = __shfl_up_sync(0xffffffffu, sid[EPT - 3 + k], 1);
-      const long long t = t0 - 3 + k;
-      hs[k] = (lane > 0) ? up : (t >= 0 && t0 < p.seqlen ? srow[t] : -2);
+      const int t = t0 - 3 + k;
+      hs[k] = (lane > 0) ? up : (t >= 0 && t0 < seqlen ? srow[t] : -2);
     }
   }
-  if (t0 >= p.seqlen) return;
+  if (t0 >= seqlen) return;
 
   // window e[j] = x[t0 - 3 + j], j = 0 .. EPT + 2
   float y[EPT];
@@ -106,12 +107,12 @@ __global__ void __launch_bounds__(kConvThreads) ss_conv1d_kernel(const __grid_co
     for (int k = 0; k < W; ++k) {
       const int j = i + 3 - H + k;  // window index of x[t0 + i - H + k]
       const float xv = j < 3 ? h[j] : v[j - 3];
-      float term = w[k] * xv;
-      if (p.seq) {
+      if constexpr (SEQ) {
         const int s = j < 3 ? hs[j] : sid[j - 3];
-        if (s != sid[i]) term = 0.f;
+        if (s == sid[i]) acc = fmaf(w[k], xv, acc);
+      } else {
+        acc = fmaf(w[k], xv, acc);
       }
-      acc += term;
     }
     y[i] = act_f<T>(acc, p.act);
   }
@@ -130,13 +131,13 @@ __global__ void __launch_bounds__(kConvThreads) ss_conv1d_kernel(const __grid_co
   } else {
 #pragma unroll
     for (int i = 0; i < EPT; ++i)
-      if (t0 + i < p.seqlen) orow[t0 + i] = from_f<T>(y[i]);
+      if (t0 + i < seqlen) orow[t0 + i] = from_f<T>(y[i]);
   }
   // final states: the last H inputs of the row (initial states to their left)
-  if (p.fin && t0 <= p.seqlen - 1 && p.seqlen - 1 < t0 + EPT) {
+  if (p.fin && t0 <= seqlen - 1 && seqlen - 1 < t0 + EPT) {
     T *frow = static_cast<T *>(p.fin) + b * p.sf[0] + (long long)d * p.sf[1];
 #pragma unroll
-    for (int k = 0; k < H; ++k) frow[k * p.sf[2]] = from_f<T>(left_value<T>(p, xrow, b, d, p.seqlen - H + k));
+    for (int k = 0; k < H; ++k) frow[k * p.sf[2]] = from_f<T>(left_value<T>(p, xrow, b, d, seqlen - H + k));
   }
 }
 
@@ -161,16 +162,17 @@ __global__ void __launch_bounds__(kConvThreads) ss_conv1d_update_kernel(const __
   for (int k = 0; k < W - 1; ++k) st[k * p.ss[2]] = raw[k + 1];
 }
 
-template <typename T, int EPT>
+template <typename T, int EPT, bool SEQ>
 const void *fwd_width(int width) {
-  return width == 2 ? (const void *)&ss_conv1d_kernel<T, EPT, 2>
-       : width == 3 ? (const void *)&ss_conv1d_kernel<T, EPT, 3>
-                    : (const void *)&ss_conv1d_kernel<T, EPT, 4>;
+  return width == 2 ? (const void *)&ss_conv1d_kernel<T, EPT, 2, SEQ>
+       : width == 3 ? (const void *)&ss_conv1d_kernel<T, EPT, 3, SEQ>
+                    : (const void *)&ss_conv1d_kernel<T, EPT, 4, SEQ>;
 }
 
 template <typename T>
-const void *fwd_kernel(int ept, int width) {
-  return ept == 8 ? fwd_width<T, 8>(width) : nullptr;
+const void *fwd_kernel(int ept, int width, bool seq) {
+  if (ept != 8) return nullptr;
+  return seq ? fwd_width<T, 8, true>(width) : fwd_width<T, 8, false>(width);
 }
 
 template <typename T>
@@ -182,11 +184,11 @@ const void *upd_kernel(int width) {
 
 }  // namespace
 
-const void *conv1d_kernel(int dtype, int ept, int width) {
+const void *conv1d_kernel(int dtype, int ept, int width, bool seq) {
   switch (dtype) {
-    case 0: return fwd_kernel<float>(ept, width);
-    case 1: return fwd_kernel<__half>(ept, width);
-    default: return fwd_kernel<__nv_bfloat16>(ept, width);
+    case 0: return fwd_kernel<float>(ept, width, seq);
+    case 1: return fwd_kernel<__half>(ept, width, seq);
+    default: return fwd_kernel<__nv_bfloat16>(ept, width, seq);
   }
 }
 

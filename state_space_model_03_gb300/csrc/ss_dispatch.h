@@ -57,7 +57,7 @@ struct ConvUpdateParams {
   long long sx[2], ss[3], sw[2], so[2];
 };
 // ept: steps per thread of the forward (8); width 2..4.
-const void *conv1d_kernel(int dtype, int ept, int width);
+const void *conv1d_kernel(int dtype, int ept, int width, bool seq);
 const void *conv1d_update_kernel(int dtype, int width);
 
 }  // namespace ssk

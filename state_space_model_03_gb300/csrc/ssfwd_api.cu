@@ -667,7 +667,7 @@ int validate_conv(const ss_conv1d_params *p) {
   if (p->activation != SS_ACT_NONE && p->activation != SS_ACT_SILU) return SS_ERR_UNSUPPORTED;
   if (p->batch < 0 || p->dim < 0 || p->seqlen < 0 || p->width < 1) return SS_ERR_SHAPE;
   if (p->width < 2 || p->width > 4) return SS_ERR_UNSUPPORTED;
-  if (p->batch > 65535 || p->dim > 65535 || p->seqlen > (int64_t(1) << 40)) return SS_ERR_UNSUPPORTED;
+  if (p->batch > 65535 || p->dim > 65535 || p->seqlen > (int64_t(1) << 31) - 4096) return SS_ERR_UNSUPPORTED;
   if (p->seq_idx && (p->initial_states || p->final_states)) return SS_ERR_UNSUPPORTED;
   if (p->batch * p->dim == 0) return SS_OK;
   if (!p->weight || (p->seqlen > 0 && (!p->out || !p->x))) return SS_ERR_NULL;
@@ -747,7 +747,7 @@ int launch_conv(const ss_conv1d_params *p, cudaStream_t stream) {
   // 8 steps per thread (16 steps measured the same on 8192-step rows and
   // 18% slower on 2048-step rows)
   const int ept = 8;
-  const void *fn = ssk::conv1d_kernel(p->dtype, ept, static_cast<int>(p->width));
+  const void *fn = ssk::conv1d_kernel(p->dtype, ept, static_cast<int>(p->width), p->seq_idx != nullptr);
   const int64_t gx = (p->seqlen + 256 * ept - 1) / (256 * ept);
   if (gx > 0x7fffffff) return SS_ERR_UNSUPPORTED;
   return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(p->dim),
