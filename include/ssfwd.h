@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define SS_ABI_VERSION 3
+#define SS_ABI_VERSION 4
 
 /* Element types. u, delta, z and out share `in_dtype`. */
 typedef enum ss_dtype { SS_F32 = 0, SS_F16 = 1, SS_BF16 = 2 } ss_dtype;
@@ -62,7 +62,7 @@ typedef enum ss_status {
   SS_ERR_CUDA = 8,         /* a CUDA runtime/driver call failed               */
   SS_ERR_INTERNAL = 9,     /* a device-side self-check tripped                */
   SS_ERR_VERSION = 10,     /* params->abi_version != SS_ABI_VERSION           */
-  SS_ERR_SCRATCH = 11      /* ss_fwd_noalloc: needs more than SS_NOALLOC_MAX_SCRATCH */
+  SS_ERR_SCRATCH = 11      /* ss_fwd_noalloc: needs more than SS_NOALLOC_MAX_SCRATCH; ss_bwd: workspace missing or too small */
 } ss_status;
 
 /*
@@ -306,6 +306,80 @@ typedef struct ss_conv1d_update_params {
 
 int ss_causal_conv1d_update_validate(const ss_conv1d_update_params *p);
 int ss_causal_conv1d_update(const ss_conv1d_update_params *p, void *stream);
+
+/*
+ * Backward of ss_fwd. Section 4.1 of the page routes the backward of
+ * selective_scan_fn to a CUDA kernel that returns the gradient of every input;
+ * it prints no formula. Given dout, the gradient of a scalar loss with respect
+ * to out, this computes the exact derivatives of sum(dout * out) for the
+ * forward above (reverse-mode through the recurrence; lam = dL/dx):
+ *
+ *     dy_t   = dout_t silu(z_t)                 dz_t  = dout_t y_t silu'(z_t)
+ *     lam_t  = dy_t C_t + exp(dt_{t+1} A) lam_{t+1}
+ *     du_t   = dy_t D + sum_n lam_t dt_t B_t    dD   += dy_t u_t
+ *     ddt_t  = sum_n lam_t (A exp(dt_t A) x_{t-1} + B_t u_t)
+ *     ddelta_t = ddt_t sigmoid(delta_t + delta_bias)   (ddt_t without softplus)
+ *     dA    += lam_t exp(dt_t A) x_{t-1} dt_t   dB_t += lam_t dt_t u_t
+ *     dC_t  += dy_t x_t                         ddelta_bias += ddelta_t
+ *     dinitial_state = exp(dt_0 A) lam_0
+ *
+ * with dA, dD, ddelta_bias and fixed dB/dC summed over batch and steps, and
+ * variable dB/dC summed over the channels of each group. The states x_t are
+ * recomputed from checkpoints kept in `workspace`; nothing from the forward
+ * call is needed.
+ *
+ * Inputs (the forward's operands, same shapes, dtypes and stride rules as in
+ * ss_fwd_params): u, delta, z, B, C, A, D, delta_bias, initial_state, and
+ *   dout               (batch, dim, seqlen) in_dtype, seqlen stride 1.
+ * Outputs (all written, never accumulated into; none may overlap an input,
+ * the workspace or another output):
+ *   du, ddelta         (batch, dim, seqlen) in_dtype, seqlen stride 1.
+ *   dz                 same, required when z is given (ignored otherwise).
+ *   dA                 (dim, dstate) fp32, contiguous.
+ *   dB, dC             fp32, contiguous, in B/C's shape: (dim, dstate) for
+ *                      fixed B/C, (batch, ngroups, dstate, seqlen) for variable.
+ *   dD, ddelta_bias    (dim,) fp32 contiguous, or NULL = not wanted. An absent
+ *                      D / delta_bias counts as 0, so its gradient is still
+ *                      defined.
+ *   dinitial_state     (batch, dim, dstate) fp32 contiguous, or NULL = not
+ *                      wanted: the gradient of the start state (initial_state,
+ *                      or the zero state when that is NULL).
+ *   workspace          device memory of at least ss_bwd_workspace_size bytes,
+ *                      16-byte aligned, caller-owned; contents need no
+ *                      initialisation (SS_ERR_SCRATCH if too small or NULL).
+ * dA, dB, dC, dD, ddelta_bias are reduced with fp32 atomic additions, so
+ * their last bits may differ between runs. seqlen == 0 gives zero gradients.
+ */
+typedef struct ss_bwd_params {
+  int32_t abi_version;      /* must be SS_ABI_VERSION */
+  int32_t in_dtype;         /* ss_dtype of u, delta, z, dout, du, ddelta, dz */
+  int32_t bc_dtype;         /* ss_dtype of B, C (outputs dB, dC are fp32) */
+  int32_t bc_mode;          /* ss_bc_mode */
+  int32_t delta_softplus;
+  int32_t reserved0;
+  int64_t batch, dim, seqlen, dstate, ngroups;
+  const void *u, *delta, *z, *B, *C, *dout;
+  const float *A, *D, *delta_bias, *initial_state;
+  void *du, *ddelta, *dz;
+  float *dA, *dB, *dC, *dD, *ddelta_bias, *dinitial_state;
+  int64_t u_stride[3], delta_stride[3], z_stride[3], dout_stride[3];
+  int64_t du_stride[3], ddelta_stride[3], dz_stride[3];
+  int64_t B_stride[4], C_stride[4];
+  int64_t A_stride[2];
+  int64_t initial_state_stride[3];
+  void *workspace;
+  int64_t workspace_bytes;
+} ss_bwd_params;
+
+/* Validate without launching (no CUDA call; the workspace size is checked). */
+int ss_bwd_validate(const ss_bwd_params *p);
+
+/* Bytes of workspace ss_bwd needs for `p` (validated as by ss_bwd, except
+ * for the workspace itself). */
+int ss_bwd_workspace_size(const ss_bwd_params *p, int64_t *bytes);
+
+/* The backward on device buffers, enqueued on `stream`. */
+int ss_bwd(const ss_bwd_params *p, void *stream);
 
 /*
  * Device-side error word of the library on the current device (nonzero after

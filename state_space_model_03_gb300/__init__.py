@@ -7,8 +7,8 @@ CPU fallback: the calls raise if the CUDA library is missing or no GPU is
 present.
 """
 
-__all__ = ["selective_scan_fn", "selective_scan_fn_host", "selective_state_update", "causal_conv1d_fn",
-           "causal_conv1d_update"]
+__all__ = ["selective_scan_fn", "selective_scan_fn_host", "selective_scan_bwd", "SelectiveScanFn",
+           "selective_state_update", "causal_conv1d_fn", "causal_conv1d_update"]
 
 
 def __getattr__(name):

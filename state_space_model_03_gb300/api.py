@@ -10,7 +10,9 @@ library or a CUDA device the calls raise.
 "PaddleNLP Kernel 算子库：CUDA 与 Triton 双实现的高性能 NLP GPU 算子实战指南",
 section 4.1: tensors whose last stride is not 1 are made contiguous, a 3-D
 (batch, dstate, seqlen) B/C is treated as 4-D with one group, and the result
-is ``out`` or ``(out, last_state)``. Forward only (no autograd).
+is ``out`` or ``(out, last_state)``. When an input requires a gradient the
+call goes through ``SelectiveScanFn``, whose backward runs ``ss_bwd``
+(last_state carries no gradient, as on the page).
 """
 from __future__ import annotations
 
@@ -29,7 +31,7 @@ _lib = None
 
 SS_F32, SS_F16, SS_BF16 = 0, 1, 2
 SS_BC_FIXED, SS_BC_VARIABLE = 0, 1
-SS_ABI_VERSION = 3
+SS_ABI_VERSION = 4
 _DT = {torch.float32: SS_F32, torch.float16: SS_F16, torch.bfloat16: SS_BF16}
 
 _i64x2, _i64x3, _i64x4 = ctypes.c_int64 * 2, ctypes.c_int64 * 3, ctypes.c_int64 * 4
@@ -96,6 +98,28 @@ class SSConv1dUpdateParams(ctypes.Structure):
     ]
 
 
+class SSBwdParams(ctypes.Structure):
+    """Mirror of ``ss_bwd_params``."""
+    _fields_ = [
+        ("abi_version", ctypes.c_int32), ("in_dtype", ctypes.c_int32), ("bc_dtype", ctypes.c_int32),
+        ("bc_mode", ctypes.c_int32), ("delta_softplus", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+        ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+        ("u", ctypes.c_void_p), ("delta", ctypes.c_void_p), ("z", ctypes.c_void_p),
+        ("B", ctypes.c_void_p), ("C", ctypes.c_void_p), ("dout", ctypes.c_void_p),
+        ("A", ctypes.c_void_p), ("D", ctypes.c_void_p), ("delta_bias", ctypes.c_void_p),
+        ("initial_state", ctypes.c_void_p),
+        ("du", ctypes.c_void_p), ("ddelta", ctypes.c_void_p), ("dz", ctypes.c_void_p),
+        ("dA", ctypes.c_void_p), ("dB", ctypes.c_void_p), ("dC", ctypes.c_void_p),
+        ("dD", ctypes.c_void_p), ("ddelta_bias", ctypes.c_void_p), ("dinitial_state", ctypes.c_void_p),
+        ("u_stride", _i64x3), ("delta_stride", _i64x3), ("z_stride", _i64x3), ("dout_stride", _i64x3),
+        ("du_stride", _i64x3), ("ddelta_stride", _i64x3), ("dz_stride", _i64x3),
+        ("B_stride", _i64x4), ("C_stride", _i64x4), ("A_stride", _i64x2),
+        ("initial_state_stride", _i64x3),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64),
+    ]
+
+
 SS_ACT_NONE, SS_ACT_SILU = 0, 1
 
 
@@ -147,6 +171,13 @@ def load_library():
             lib.ss_causal_conv1d_update_validate.restype = ctypes.c_int
             lib.ss_causal_conv1d_update.argtypes = [PU, vp]
             lib.ss_causal_conv1d_update.restype = ctypes.c_int
+            PB = ctypes.POINTER(SSBwdParams)
+            lib.ss_bwd_validate.argtypes = [PB]
+            lib.ss_bwd_validate.restype = ctypes.c_int
+            lib.ss_bwd_workspace_size.argtypes = [PB, ctypes.POINTER(ctypes.c_int64)]
+            lib.ss_bwd_workspace_size.restype = ctypes.c_int
+            lib.ss_bwd.argtypes = [PB, vp]
+            lib.ss_bwd.restype = ctypes.c_int
             lib.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
             lib.ss_device_error.restype = ctypes.c_int
             if lib.ss_abi_version() != SS_ABI_VERSION:
@@ -266,6 +297,22 @@ def attach_workspace(p: SSFwdParams, device) -> "torch.Tensor | None":
     return ws
 
 
+def _forward(u, delta, A, B, C, D, z, delta_bias, delta_softplus, return_last_state, initial_state):
+    """ss_fwd on normalised CUDA tensors; returns (out, last_state or None)."""
+    lib = load_library()
+    out = torch.empty(u.shape, dtype=u.dtype, device=u.device)
+    last = (torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
+            if return_last_state else None)
+    p = make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last, initial_state)
+    ws = attach_workspace(p, u.device)
+    stream = torch.cuda.current_stream(u.device)
+    with torch.cuda.device(u.device):
+        _check(lib.ss_fwd(ctypes.byref(p), stream.cuda_stream))
+    if ws is not None:
+        ws.record_stream(stream)
+    return out, last
+
+
 def selective_scan_fn(u, delta, A, B, C, D=None, z=None, delta_bias=None,
                       delta_softplus=False, return_last_state=False, initial_state=None):
     """Selective-scan forward on CUDA tensors; runs on the current stream.
@@ -275,25 +322,131 @@ def selective_scan_fn(u, delta, A, B, C, D=None, z=None, delta_bias=None,
     (batch, dstate, seqlen) / (batch, groups, dstate, seqlen) in u's dtype or
     fp32. D, delta_bias: (dim,) fp32. initial_state: optional (batch, dim,
     dstate) fp32 start state (zero if None). Returns out (u's dtype), or
-    (out, last_state) with last_state (batch, dim, dstate) fp32.
+    (out, last_state) with last_state (batch, dim, dstate) fp32. Differentiable
+    (through ss_bwd) in every input but last_state.
     """
     if not u.is_cuda:
         raise RuntimeError("selective_scan_fn needs CUDA tensors (there is no CPU path)")
-    lib = load_library()
+    ins = (u, delta, A, B, C, D, z, delta_bias, initial_state)
+    if torch.is_grad_enabled() and any(t is not None and t.requires_grad for t in ins):
+        out, last = SelectiveScanFn.apply(u, delta, A, B, C, D, z, delta_bias, bool(delta_softplus),
+                                          bool(return_last_state), initial_state)
+        return (out, last) if return_last_state else out
     u, delta, A, B, C, D, z, delta_bias = normalise(u, delta, A, B, C, D, z, delta_bias)
-    out = torch.empty(u.shape, dtype=u.dtype, device=u.device)
-    last = (torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
-            if return_last_state else None)
     if initial_state is not None:
         initial_state = _unit_last(initial_state)
-    p = make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last, initial_state)
-    ws = attach_workspace(p, u.device)  # noqa: F841 (kept alive until the launch is enqueued)
-    stream = torch.cuda.current_stream(u.device).cuda_stream
-    with torch.cuda.device(u.device):
-        _check(lib.ss_fwd(ctypes.byref(p), stream))
-    if ws is not None:
-        ws.record_stream(torch.cuda.current_stream(u.device))
+    out, last = _forward(u, delta, A, B, C, D, z, delta_bias, delta_softplus, return_last_state, initial_state)
     return (out, last) if return_last_state else out
+
+
+def make_bwd_params(dout, u, delta, A, B, C, D, z, delta_bias, delta_softplus, initial_state,
+                    du, ddelta, dz, dA, dB, dC, dD, ddelta_bias, dinitial_state) -> SSBwdParams:
+    """Fill an ss_bwd_params from normalised CUDA tensors (B/C 2-D or 4-D);
+    the workspace is attached separately (attach_bwd_workspace)."""
+    f = make_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, du, None, initial_state)
+    for name, t in (("dout", dout), ("du", du), ("ddelta", ddelta), ("dz", dz)):
+        if t is not None and (t.dtype != u.dtype or t.shape != u.shape):
+            raise TypeError(f"{name} must match u in shape and dtype")
+    p = SSBwdParams()
+    for k in ("abi_version", "in_dtype", "bc_dtype", "bc_mode", "delta_softplus", "batch", "dim", "seqlen",
+              "dstate", "ngroups", "u", "delta", "z", "B", "C", "A", "D", "delta_bias", "initial_state"):
+        setattr(p, k, getattr(f, k))
+    for k in ("u_stride", "delta_stride", "z_stride", "B_stride", "C_stride", "A_stride", "initial_state_stride"):
+        getattr(p, k)[:] = list(getattr(f, k))
+    p.dout = _ptr(dout)
+    p.du, p.ddelta, p.dz = _ptr(du), _ptr(ddelta), _ptr(dz)
+    p.dA, p.dB, p.dC = _ptr(dA), _ptr(dB), _ptr(dC)
+    p.dD, p.ddelta_bias, p.dinitial_state = _ptr(dD), _ptr(ddelta_bias), _ptr(dinitial_state)
+    p.dout_stride[:] = list(dout.stride())
+    p.du_stride[:] = list(du.stride())
+    p.ddelta_stride[:] = list(ddelta.stride())
+    p.dz_stride[:] = list(dz.stride()) if dz is not None else [0, 0, 1]
+    return p
+
+
+def attach_bwd_workspace(p: SSBwdParams, device) -> "torch.Tensor | None":
+    """Allocate (torch) and attach the checkpoint workspace ss_bwd needs."""
+    n = ctypes.c_int64(0)
+    _check(load_library().ss_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n)))
+    if n.value <= 0:
+        return None
+    ws = torch.empty(int(n.value), dtype=torch.uint8, device=device)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), int(n.value)
+    return ws
+
+
+def selective_scan_bwd(dout, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
+                       initial_state=None, want_dD=None, want_ddelta_bias=None, want_dinitial_state=None):
+    """Gradients of sum(dout * out) for selective_scan_fn (through ss_bwd), on
+    the current stream. Returns a dict: du, ddelta, dz (u's dtype), dA (fp32),
+    dB, dC (B/C's dtype and shape), dD, ddelta_bias, dinitial_state (fp32;
+    None when not wanted, by default when the input is absent)."""
+    if not u.is_cuda:
+        raise RuntimeError("selective_scan_bwd needs CUDA tensors (there is no CPU path)")
+    B_in = B
+    u, delta, A, B, C, D, z, delta_bias = normalise(u, delta, A, B, C, D, z, delta_bias)
+    dout = _unit_last(dout)
+    if initial_state is not None:
+        initial_state = _unit_last(initial_state)
+    want_dD = D is not None if want_dD is None else want_dD
+    want_ddelta_bias = delta_bias is not None if want_ddelta_bias is None else want_ddelta_bias
+    want_dinitial_state = initial_state is not None if want_dinitial_state is None else want_dinitial_state
+    dev = u.device
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[1]
+    f32 = dict(dtype=torch.float32, device=dev)
+    du, ddelta = torch.empty_like(u), torch.empty_like(u)
+    dz = torch.empty_like(u) if z is not None else None
+    dA = torch.empty((dim, dstate), **f32)
+    dB, dC = torch.empty(B.shape, **f32), torch.empty(C.shape, **f32)
+    dD = torch.empty(dim, **f32) if want_dD else None
+    ddb = torch.empty(dim, **f32) if want_ddelta_bias else None
+    dx0 = torch.empty((batch, dim, dstate), **f32) if want_dinitial_state else None
+    p = make_bwd_params(dout, u, delta, A, B, C, D, z, delta_bias, delta_softplus, initial_state,
+                        du, ddelta, dz, dA, dB, dC, dD, ddb, dx0)
+    ws = attach_bwd_workspace(p, dev)
+    stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        _check(load_library().ss_bwd(ctypes.byref(p), stream.cuda_stream))
+    if ws is not None:
+        ws.record_stream(stream)
+    if B_in.dim() == 3:
+        dB, dC = dB[:, 0], dC[:, 0]
+    return dict(du=du, ddelta=ddelta, dz=dz, dA=dA, dB=dB.to(B_in.dtype), dC=dC.to(B_in.dtype),
+                dD=dD, ddelta_bias=ddb, dinitial_state=dx0)
+
+
+class SelectiveScanFn(torch.autograd.Function):
+    """selective_scan_fn with its backward (the page's SelectiveScanFn layer):
+    forward through ss_fwd, backward through ss_bwd; last_state has no
+    gradient."""
+
+    @staticmethod
+    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, delta_softplus, return_last_state, initial_state):
+        B3 = B.dim() == 3
+        nu, nd, nA, nB, nC, nD, nz, nb = normalise(u, delta, A, B, C, D, z, delta_bias)
+        x0 = _unit_last(initial_state) if initial_state is not None else None
+        out, last = _forward(nu, nd, nA, nB, nC, nD, nz, nb, delta_softplus, return_last_state, x0)
+        ctx.save_for_backward(nu, nd, nA, nB, nC, nD, nz, nb, x0)
+        ctx.delta_softplus, ctx.B3 = delta_softplus, B3
+        ctx.dtypes = (B.dtype, C.dtype)
+        if last is not None:
+            ctx.mark_non_differentiable(last)
+        return out, last
+
+    @staticmethod
+    def backward(ctx, dout, dlast):
+        u, delta, A, B, C, D, z, bias, x0 = ctx.saved_tensors
+        need = ctx.needs_input_grad
+        g = selective_scan_bwd(dout, u, delta, A, B, C, D, z, bias, ctx.delta_softplus, x0,
+                               want_dD=D is not None and need[5],
+                               want_ddelta_bias=bias is not None and need[7],
+                               want_dinitial_state=x0 is not None and need[10])
+        dB, dC = g["dB"].to(ctx.dtypes[0]), g["dC"].to(ctx.dtypes[1])
+        if ctx.B3:
+            dB, dC = dB[:, 0], dC[:, 0]
+        return (g["du"], g["ddelta"], g["dA"], dB, dC, g["dD"], g["dz"], g["ddelta_bias"], None, None,
+                g["dinitial_state"])
 
 
 class HostRunner:

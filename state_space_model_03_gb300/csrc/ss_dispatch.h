@@ -60,4 +60,24 @@ struct ConvUpdateParams {
 const void *conv1d_kernel(int dtype, int ept, int width, bool seq);
 const void *conv1d_update_kernel(int dtype, int width);
 
+// Selective-scan backward (ss_bwd).
+struct BwdParams {
+  int batch, dim, dstate, ngroups, dpg;
+  int tiles;        // CTAs per group along the channels
+  int seqlen, nch;  // steps; chunks of bwd_chunk_steps() steps
+  int has_z, softplus;
+  int vec;          // 16-byte row accesses of u, delta, z, dout, du, ddelta, dz allowed
+  int bcvec;        // 16-byte B/C row accesses allowed (variable B/C)
+  int dbvec;        // 16-byte atomics into dB/dC allowed
+  const void *u, *delta, *z, *B, *C, *dout;
+  const float *A, *D, *bias, *init;
+  void *du, *ddelta, *dz;
+  float *dA, *dB, *dC, *dD, *dbias, *dx0;
+  float *ws;        // chunk-start states (batch, dim, nch, dstate)
+  long long su[2], sd[2], sz[2], sg[2], sdu[2], sdd[2], sdz[2], sB[3], sC[3], sA, si[2];
+};
+int bwd_chunk_steps();
+int bwd_rows_per_cta();
+const void *bwd_kernel(int in_dtype, bool bc_f32, bool fixed);
+
 }  // namespace ssk

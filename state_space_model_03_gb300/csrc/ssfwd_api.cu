@@ -811,6 +811,205 @@ int launch_conv_update(const ss_conv1d_update_params *p, cudaStream_t stream) {
              : SS_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Backward (ss_bwd)
+// ---------------------------------------------------------------------------
+int64_t bwd_chunks(int64_t seqlen) { return (seqlen + ssk::bwd_chunk_steps() - 1) / ssk::bwd_chunk_steps(); }
+
+int64_t bwd_ws_bytes(const ss_bwd_params *p) {
+  return p->batch * p->dim * bwd_chunks(p->seqlen) * p->dstate * 4;
+}
+
+// Everything except the workspace.
+int validate_bwd_operands(const ss_bwd_params *p) {
+  if (!p) return SS_ERR_NULL;
+  if (p->abi_version != SS_ABI_VERSION) return SS_ERR_VERSION;
+  if (p->in_dtype < SS_F32 || p->in_dtype > SS_BF16) return SS_ERR_DTYPE;
+  if (p->bc_dtype < SS_F32 || p->bc_dtype > SS_BF16) return SS_ERR_DTYPE;
+  if (p->bc_mode != SS_BC_FIXED && p->bc_mode != SS_BC_VARIABLE) return SS_ERR_SHAPE;
+  const bool fixed = p->bc_mode == SS_BC_FIXED;
+  if (fixed && p->bc_dtype != SS_F32) return SS_ERR_DTYPE;
+  if (!fixed && p->bc_dtype != p->in_dtype && p->bc_dtype != SS_F32) return SS_ERR_DTYPE;
+  if (p->batch < 0 || p->dim < 0 || p->seqlen < 0) return SS_ERR_SHAPE;
+  if (p->dstate < 1) return SS_ERR_SHAPE;
+  if (p->dstate > 64) return SS_ERR_UNSUPPORTED;
+  if (!fixed && (p->ngroups < 1 || (p->dim > 0 && p->dim % p->ngroups != 0))) return SS_ERR_SHAPE;
+  if (p->batch > (int64_t(1) << 24) || p->dim > (1 << 30) || p->seqlen > (int64_t(1) << 31) - 1024)
+    return SS_ERR_UNSUPPORTED;
+  if (p->batch * p->dim == 0) return SS_OK;
+  if (!p->A || !p->dA) return SS_ERR_NULL;
+  if ((fixed || p->seqlen > 0) && (!p->dB || !p->dC)) return SS_ERR_NULL;  // variable dB/dC are empty at seqlen 0
+  if (p->A_stride[1] != 1 || p->A_stride[0] < 0) return SS_ERR_STRIDE;
+  if (p->initial_state) {
+    if (p->initial_state_stride[2] != 1 || p->initial_state_stride[0] < 0 || p->initial_state_stride[1] < 0)
+      return SS_ERR_STRIDE;
+    if (!aligned(p->initial_state, 4)) return SS_ERR_ALIGN;
+  }
+  const int es = elem_size(p->in_dtype), bs = elem_size(p->bc_dtype);
+  const int64_t sz3[3] = {p->batch, p->dim, p->seqlen};
+  const int64_t sza[2] = {p->dim, p->dstate};
+  const int64_t szs[3] = {p->batch, p->dim, p->dstate};
+  const int64_t one[1] = {p->dim}, unit[1] = {1};
+  if (!aligned(p->A, 4) || !aligned(p->dA, 4) || !aligned(p->dB, 4) || !aligned(p->dC, 4)) return SS_ERR_ALIGN;
+  if ((p->D && !aligned(p->D, 4)) || (p->delta_bias && !aligned(p->delta_bias, 4)) ||
+      (p->dD && !aligned(p->dD, 4)) || (p->ddelta_bias && !aligned(p->ddelta_bias, 4)) ||
+      (p->dinitial_state && !aligned(p->dinitial_state, 4)))
+    return SS_ERR_ALIGN;
+  if (p->seqlen > 0) {
+    if (!p->u || !p->delta || !p->B || !p->C || !p->dout || !p->du || !p->ddelta) return SS_ERR_NULL;
+    if (p->z && !p->dz) return SS_ERR_NULL;
+    const int64_t *st3[7] = {p->u_stride, p->delta_stride, p->z ? p->z_stride : p->u_stride, p->dout_stride,
+                             p->du_stride, p->ddelta_stride, p->z ? p->dz_stride : p->u_stride};
+    for (auto st : st3)
+      if (st[2] != 1 || st[0] < 0 || st[1] < 0) return SS_ERR_STRIDE;
+    if (fixed) {
+      if (p->B_stride[1] != 1 || p->C_stride[1] != 1 || p->B_stride[0] < 0 || p->C_stride[0] < 0)
+        return SS_ERR_STRIDE;
+    } else {
+      for (int i = 0; i < 4; ++i)
+        if (p->B_stride[i] < 0 || p->C_stride[i] < 0) return SS_ERR_STRIDE;
+      if (p->B_stride[3] != 1 || p->C_stride[3] != 1) return SS_ERR_STRIDE;
+    }
+    if (!aligned(p->u, es) || !aligned(p->delta, es) || !aligned(p->dout, es) || !aligned(p->du, es) ||
+        !aligned(p->ddelta, es) || (p->z && (!aligned(p->z, es) || !aligned(p->dz, es))))
+      return SS_ERR_ALIGN;
+    if (!aligned(p->B, bs) || !aligned(p->C, bs)) return SS_ERR_ALIGN;
+  }
+  // outputs must not overlap inputs, the workspace or each other
+  Range ins[12], outs[10];
+  int ni = 0, no = 0;
+  const int64_t c2[2] = {p->dstate, 1};
+  const int64_t c3[3] = {p->dim * p->dstate, p->dstate, 1};
+  ins[ni++] = span(p->A, 4, sza, p->A_stride, 2);
+  if (p->D) ins[ni++] = span(p->D, 4, one, unit, 1);
+  if (p->delta_bias) ins[ni++] = span(p->delta_bias, 4, one, unit, 1);
+  if (p->initial_state) ins[ni++] = span(p->initial_state, 4, szs, p->initial_state_stride, 3);
+  outs[no++] = span(p->dA, 4, sza, c2, 2);
+  if (p->dD) outs[no++] = span(p->dD, 4, one, unit, 1);
+  if (p->ddelta_bias) outs[no++] = span(p->ddelta_bias, 4, one, unit, 1);
+  if (p->dinitial_state) outs[no++] = span(p->dinitial_state, 4, szs, c3, 3);
+  if (fixed) {
+    if (p->seqlen > 0) {
+      ins[ni++] = span(p->B, 4, sza, p->B_stride, 2);
+      ins[ni++] = span(p->C, 4, sza, p->C_stride, 2);
+    }
+    outs[no++] = span(p->dB, 4, sza, c2, 2);
+    outs[no++] = span(p->dC, 4, sza, c2, 2);
+  } else {
+    const int64_t szb[4] = {p->batch, p->ngroups, p->dstate, p->seqlen};
+    const int64_t cb[4] = {p->ngroups * p->dstate * p->seqlen, p->dstate * p->seqlen, p->seqlen, 1};
+    if (p->seqlen > 0) {
+      ins[ni++] = span(p->B, bs, szb, p->B_stride, 4);
+      ins[ni++] = span(p->C, bs, szb, p->C_stride, 4);
+    }
+    outs[no++] = span(p->dB, 4, szb, cb, 4);
+    outs[no++] = span(p->dC, 4, szb, cb, 4);
+  }
+  if (p->seqlen > 0) {
+    ins[ni++] = span(p->u, es, sz3, p->u_stride, 3);
+    ins[ni++] = span(p->delta, es, sz3, p->delta_stride, 3);
+    ins[ni++] = span(p->dout, es, sz3, p->dout_stride, 3);
+    if (p->z) ins[ni++] = span(p->z, es, sz3, p->z_stride, 3);
+    outs[no++] = span(p->du, es, sz3, p->du_stride, 3);
+    outs[no++] = span(p->ddelta, es, sz3, p->ddelta_stride, 3);
+    if (p->z) outs[no++] = span(p->dz, es, sz3, p->dz_stride, 3);
+  }
+  for (int o = 0; o < no; ++o) {
+    for (int i = 0; i < ni; ++i)
+      if (overlap(outs[o], ins[i])) return SS_ERR_ALIAS;
+    for (int q = o + 1; q < no; ++q)
+      if (overlap(outs[o], outs[q])) return SS_ERR_ALIAS;
+  }
+  if (p->workspace && p->workspace_bytes > 0) {
+    const Range ws{reinterpret_cast<uintptr_t>(p->workspace),
+                   reinterpret_cast<uintptr_t>(p->workspace) + static_cast<uintptr_t>(p->workspace_bytes)};
+    for (int i = 0; i < ni; ++i)
+      if (overlap(ws, ins[i])) return SS_ERR_ALIAS;
+    for (int o = 0; o < no; ++o)
+      if (overlap(ws, outs[o])) return SS_ERR_ALIAS;
+  }
+  return SS_OK;
+}
+
+int validate_bwd(const ss_bwd_params *p) {
+  const int st = validate_bwd_operands(p);
+  if (st != SS_OK) return st;
+  if (p->workspace_bytes < 0) return SS_ERR_SHAPE;
+  if (p->batch * p->dim == 0 || p->seqlen == 0) return SS_OK;
+  if (!p->workspace || p->workspace_bytes < bwd_ws_bytes(p)) return SS_ERR_SCRATCH;
+  if (!aligned(p->workspace, 16)) return SS_ERR_ALIGN;
+  return SS_OK;
+}
+
+int launch_bwd(const ss_bwd_params *p, cudaStream_t stream) {
+  if (p->batch * p->dim == 0) return SS_OK;
+  const bool fixed = p->bc_mode == SS_BC_FIXED;
+  if (fault_injected("launch")) return SS_ERR_CUDA;
+  // the reduced gradients are sums of atomic additions: start from zero
+  const int64_t nbc = fixed ? p->dim * p->dstate : p->batch * p->ngroups * p->dstate * p->seqlen;
+  bool ok = cudaMemsetAsync(p->dA, 0, p->dim * p->dstate * 4, stream) == cudaSuccess;
+  if (ok && nbc > 0)
+    ok = cudaMemsetAsync(p->dB, 0, nbc * 4, stream) == cudaSuccess &&
+         cudaMemsetAsync(p->dC, 0, nbc * 4, stream) == cudaSuccess;
+  if (ok && p->dD) ok = cudaMemsetAsync(p->dD, 0, p->dim * 4, stream) == cudaSuccess;
+  if (ok && p->ddelta_bias) ok = cudaMemsetAsync(p->ddelta_bias, 0, p->dim * 4, stream) == cudaSuccess;
+  if (!ok) return SS_ERR_CUDA;
+  if (p->seqlen == 0) {
+    if (p->dinitial_state &&
+        cudaMemsetAsync(p->dinitial_state, 0, p->batch * p->dim * p->dstate * 4, stream) != cudaSuccess)
+      return SS_ERR_CUDA;
+    return SS_OK;
+  }
+  ssk::BwdParams k{};
+  k.batch = static_cast<int>(p->batch);
+  k.dim = static_cast<int>(p->dim);
+  k.dstate = static_cast<int>(p->dstate);
+  k.ngroups = fixed ? 1 : static_cast<int>(p->ngroups);
+  k.dpg = k.dim / k.ngroups;
+  const int rows = ssk::bwd_rows_per_cta();
+  k.tiles = (k.dpg + rows - 1) / rows;
+  k.seqlen = static_cast<int>(p->seqlen);
+  k.nch = static_cast<int>(bwd_chunks(p->seqlen));
+  k.has_z = p->z != nullptr;
+  k.softplus = p->delta_softplus != 0;
+  k.u = p->u; k.delta = p->delta; k.z = p->z; k.B = p->B; k.C = p->C; k.dout = p->dout;
+  k.A = p->A; k.D = p->D; k.bias = p->delta_bias; k.init = p->initial_state;
+  k.du = p->du; k.ddelta = p->ddelta; k.dz = p->dz;
+  k.dA = p->dA; k.dB = p->dB; k.dC = p->dC; k.dD = p->dD; k.dbias = p->ddelta_bias; k.dx0 = p->dinitial_state;
+  k.ws = static_cast<float *>(p->workspace);
+  for (int i = 0; i < 2; ++i) {
+    k.su[i] = p->u_stride[i]; k.sd[i] = p->delta_stride[i]; k.sg[i] = p->dout_stride[i];
+    k.sz[i] = p->z ? p->z_stride[i] : 0; k.sdz[i] = p->z ? p->dz_stride[i] : 0;
+    k.sdu[i] = p->du_stride[i]; k.sdd[i] = p->ddelta_stride[i];
+    k.si[i] = p->initial_state ? p->initial_state_stride[i] : 0;
+  }
+  for (int i = 0; i < 3; ++i) { k.sB[i] = p->B_stride[i]; k.sC[i] = p->C_stride[i]; }
+  k.sA = p->A_stride[0];
+  // 16-byte accesses of 8 steps: every row start 16-byte aligned
+  const int es = elem_size(p->in_dtype), bs = elem_size(p->bc_dtype);
+  auto rows_ok = [&](const void *ptr, const int64_t *st, int esz) {
+    return aligned(ptr, 16) && (p->batch == 1 || (st[0] * esz) % 16 == 0) && (p->dim == 1 || (st[1] * esz) % 16 == 0);
+  };
+  k.vec = rows_ok(p->u, p->u_stride, es) && rows_ok(p->delta, p->delta_stride, es) &&
+          rows_ok(p->dout, p->dout_stride, es) && rows_ok(p->du, p->du_stride, es) &&
+          rows_ok(p->ddelta, p->ddelta_stride, es) &&
+          (!p->z || (rows_ok(p->z, p->z_stride, es) && rows_ok(p->dz, p->dz_stride, es)));
+  k.bcvec = !fixed && aligned(p->B, 16) && aligned(p->C, 16);
+  for (int i = 0; i < 3 && k.bcvec; ++i)
+    k.bcvec = (p->B_stride[i] * bs) % 16 == 0 && (p->C_stride[i] * bs) % 16 == 0;
+  k.dbvec = !fixed && aligned(p->dB, 16) && aligned(p->dC, 16) && p->seqlen % 4 == 0;
+  const bool bc_f32 = fixed || p->bc_dtype == SS_F32;
+  const void *fn = ssk::bwd_kernel(p->in_dtype, bc_f32, fixed);
+  const int64_t gx = static_cast<int64_t>(k.ngroups) * k.tiles;
+  const int64_t gy = std::min<int64_t>(p->batch, 65535), gz = (p->batch + gy - 1) / gy;
+  if (gx > 0x7fffffff || gz > 65535) return SS_ERR_UNSUPPORTED;
+  void *args[1] = {&k};
+  return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(gz)),
+                          dim3(rows * 32), args, 0, stream) == cudaSuccess
+             ? SS_OK
+             : SS_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -831,8 +1030,9 @@ const char *ss_status_string(int s) {
     case SS_ERR_INTERNAL: return "a device-side self-check failed";
     case SS_ERR_VERSION: return "ABI version mismatch";
     case SS_ERR_SCRATCH:
-      return "the problem needs more scratch than ss_fwd_noalloc's static buffer holds "
-             "(SS_NOALLOC_MAX_SCRATCH bytes); call ss_fwd with a workspace instead";
+      return "not enough scratch: ss_fwd_noalloc's static buffer (SS_NOALLOC_MAX_SCRATCH bytes) is too "
+             "small for the problem (call ss_fwd with a workspace), or ss_bwd's workspace is missing or "
+             "smaller than ss_bwd_workspace_size";
     default: return "unknown status";
   }
 }
@@ -935,6 +1135,22 @@ int ss_causal_conv1d_update(const ss_conv1d_update_params *p, void *stream) {
   int st = validate_conv_update(p);
   if (st != SS_OK) return st;
   return launch_conv_update(p, static_cast<cudaStream_t>(stream));
+}
+
+int ss_bwd_validate(const ss_bwd_params *p) { return validate_bwd(p); }
+
+int ss_bwd_workspace_size(const ss_bwd_params *p, int64_t *bytes) {
+  if (!bytes) return SS_ERR_NULL;
+  const int st = validate_bwd_operands(p);
+  if (st != SS_OK) return st;
+  *bytes = bwd_ws_bytes(p);
+  return SS_OK;
+}
+
+int ss_bwd(const ss_bwd_params *p, void *stream) {
+  const int st = validate_bwd(p);
+  if (st != SS_OK) return st;
+  return launch_bwd(p, static_cast<cudaStream_t>(stream));
 }
 
 int ss_device_error(int32_t *out_word, int clear) {

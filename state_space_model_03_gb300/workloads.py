@@ -133,6 +133,28 @@ def compulsory_bytes(w: Workload) -> int:
     return total
 
 
+def make_dout(w: Workload, seed: Optional[int] = None) -> torch.Tensor:
+    """The upstream gradient for the backward: dout ~ N(0, 1) of u's shape,
+    drawn with PCG64 from seed (default w.seed + 1000), stored in w.dtype."""
+    rng = np.random.default_rng(w.seed + 1000 if seed is None else seed)
+    return _cast(rng.standard_normal((w.batch, w.dim, w.seqlen), dtype=np.float32), w.dtype)
+
+
+def backward_compulsory_bytes(w: Workload) -> int:
+    """Bytes the backward must move at least once: u, delta, (z), dout read and
+    du, ddelta, (dz) written at the stored dtype; B/C read once and dB/dC
+    written once in fp32 (per (batch, group), or per channel if fixed); A, D,
+    bias read and dA, dD, ddelta_bias written in fp32."""
+    s = torch.tensor([], dtype=_TORCH_DTYPES[w.dtype]).element_size()
+    sbc = torch.tensor([], dtype=_TORCH_DTYPES[w.bc_stored_dtype()]).element_size()
+    total = s * (5 + (2 if w.has_z else 0)) * w.elems
+    nbc = w.dim * w.dstate if w.bc == "fixed" else w.batch * w.groups * w.dstate * w.seqlen
+    total += 2 * nbc * (sbc + 4)
+    total += 2 * w.dim * w.dstate * 4
+    total += 2 * w.dim * 4 * ((1 if w.D_mode != "none" else 0) + (1 if w.has_bias else 0))
+    return total
+
+
 # ---------------------------------------------------------------------------
 # Decode step (one token per sequence against a resident state)
 # ---------------------------------------------------------------------------

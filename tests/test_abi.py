@@ -32,7 +32,8 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == {"ss_abi_version", "ss_status_string", "ss_fwd_validate", "ss_fwd",
                           "ss_fwd_host", "ss_device_error", "ss_fwd_workspace_size", "ss_fwd_noalloc",
                           "ss_state_update_validate", "ss_state_update", "ss_causal_conv1d_validate",
-                          "ss_causal_conv1d", "ss_causal_conv1d_update_validate", "ss_causal_conv1d_update"}
+                          "ss_causal_conv1d", "ss_causal_conv1d_update_validate", "ss_causal_conv1d_update",
+                          "ss_bwd_validate", "ss_bwd_workspace_size", "ss_bwd"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -308,3 +309,93 @@ def test_conv1d_update_validation(lib):
     p.out = base + 12288
     p.width = 6
     assert lib.ss_causal_conv1d_update_validate(ctypes.byref(p)) == 7
+
+
+# ---------------------------------------------------------------------------
+# backward (ss_bwd): validation only (no launch on the CPU)
+# ---------------------------------------------------------------------------
+def _good_bwd(with_ws=True):
+    """A valid variable-B/C bf16 backward with fake (never dereferenced)
+    device addresses, contiguous and 256-byte aligned."""
+    b, d, l, n, g = 2, 64, 300, 16, 2
+    p = api.SSBwdParams()
+    p.abi_version = api.SS_ABI_VERSION
+    p.in_dtype = p.bc_dtype = api.SS_BF16
+    p.bc_mode = api.SS_BC_VARIABLE
+    p.delta_softplus = 1
+    p.batch, p.dim, p.seqlen, p.dstate, p.ngroups = b, d, l, n, g
+    sz3, szb = b * d * l * 2, b * g * n * l
+    cur = 1 << 40
+    for k, nbytes in (("u", sz3), ("delta", sz3), ("z", sz3), ("dout", sz3), ("B", szb * 2), ("C", szb * 2),
+                      ("A", d * n * 4), ("D", d * 4), ("delta_bias", d * 4), ("initial_state", b * d * n * 4),
+                      ("du", sz3), ("ddelta", sz3), ("dz", sz3), ("dA", d * n * 4), ("dB", szb * 4),
+                      ("dC", szb * 4), ("dD", d * 4), ("ddelta_bias", d * 4), ("dinitial_state", b * d * n * 4)):
+        setattr(p, k, cur)
+        cur += (nbytes + 255) // 256 * 256
+    for k in ("u_stride", "delta_stride", "z_stride", "dout_stride", "du_stride", "ddelta_stride", "dz_stride"):
+        getattr(p, k)[:] = [d * l, l, 1]
+    p.B_stride[:] = [g * n * l, n * l, l, 1]
+    p.C_stride[:] = [g * n * l, n * l, l, 1]
+    p.A_stride[:] = [n, 1]
+    p.initial_state_stride[:] = [d * n, n, 1]
+    if with_ws:
+        p.workspace, p.workspace_bytes = cur, b * d * 2 * n * 4  # 300 steps = 2 chunks of 256
+    return p
+
+
+def test_bwd_workspace_size(lib):
+    p = _good_bwd(with_ws=False)
+    n = ctypes.c_int64(-1)
+    assert lib.ss_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    assert n.value == 2 * 64 * 2 * 16 * 4  # batch * dim * chunks * dstate * fp32
+    assert lib.ss_bwd_workspace_size(ctypes.byref(p), None) == 1
+    assert lib.ss_bwd_validate(ctypes.byref(p)) == 11  # no workspace: SS_ERR_SCRATCH
+    assert lib.ss_bwd(ctypes.byref(p), None) == 11
+    assert lib.ss_bwd_validate(ctypes.byref(_good_bwd())) == 0
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda p: setattr(p, "abi_version", 3), 10),
+    (lambda p: setattr(p, "dout", None), 1),
+    (lambda p: setattr(p, "du", None), 1),
+    (lambda p: setattr(p, "dA", None), 1),
+    (lambda p: setattr(p, "dB", None), 1),
+    (lambda p: setattr(p, "dz", None), 1),                    # z given, dz missing
+    (lambda p: setattr(p, "dstate", 65), 7),
+    (lambda p: setattr(p, "ngroups", 3), 2),
+    (lambda p: setattr(p, "bc_dtype", api.SS_F16), 3),
+    (lambda p: p.dout_stride.__setitem__(2, 2), 4),
+    (lambda p: p.du_stride.__setitem__(2, 2), 4),
+    (lambda p: p.dz_stride.__setitem__(1, -1), 4),
+    (lambda p: setattr(p, "du", p.du + 1), 5),
+    (lambda p: setattr(p, "dB", p.dB + 2), 5),
+    (lambda p: setattr(p, "workspace", p.workspace + 8), 5),  # not 16-byte aligned
+    (lambda p: setattr(p, "du", p.u), 6),                     # gradient written over an input
+    (lambda p: setattr(p, "dA", p.A), 6),
+    (lambda p: setattr(p, "dC", p.dB + 64), 6),               # two outputs overlap
+    (lambda p: setattr(p, "dinitial_state", p.initial_state), 6),
+    (lambda p: setattr(p, "workspace", p.dA), 6),
+    (lambda p: setattr(p, "workspace_bytes", 100), 11),
+    (lambda p: setattr(p, "workspace_bytes", -1), 2),
+])
+def test_bwd_invalid_params_rejected(lib, mutate, status):
+    p = _good_bwd()
+    mutate(p)
+    assert lib.ss_bwd_validate(ctypes.byref(p)) == status
+    assert lib.ss_bwd(ctypes.byref(p), None) == status
+
+
+def test_bwd_optional_outputs_and_empty(lib):
+    p = _good_bwd()
+    for k in ("dD", "ddelta_bias", "dinitial_state", "D", "delta_bias", "initial_state"):
+        setattr(p, k, None)
+    assert lib.ss_bwd_validate(ctypes.byref(p)) == 0
+    p.z = None
+    p.dz = None
+    assert lib.ss_bwd_validate(ctypes.byref(p)) == 0
+    q = _good_bwd(with_ws=False)
+    q.seqlen = 0  # zero gradients, no workspace needed
+    assert lib.ss_bwd_validate(ctypes.byref(q)) == 0
+    q = _good_bwd(with_ws=False)
+    q.batch = 0
+    assert lib.ss_bwd_validate(ctypes.byref(q)) == 0
