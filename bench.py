@@ -64,6 +64,7 @@ KERNEL_SOURCES = {
     "scan": ("ss_fwd_kernel.cuh", "ss_fwd_f32.cu", "ss_fwd_f16.cu", "ss_fwd_bf16.cu"),
     "state_update": ("ss_state_update.cu",),
     "conv1d": ("ss_conv1d.cu",),
+    "bwd": ("ss_bwd.cu",),
 }
 
 
@@ -619,14 +620,181 @@ def run_conv(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+BWD_METRIC = "selective-scan bwd HBM GB/s (compulsory bytes / kernel time)"
+# Algorithmic fp32 operations of the backward per (batch, channel, state, step):
+# state recompute (dt*A, a*h + (dt u)*B: 3), y += C h (1), adjoint
+# lam = a*lam' + dy*C (2), du += (lam dt)*B (2), ddt += lam (A (a h_prev) + B u)
+# (4), dA += (lam dt)(a h_prev) (1), dB term (1), dC term (1); plus one exp.
+BWD_OPS_PER_PAIR = 15
+FP32_LANES_PER_SM = 128
+
+
+def _bwd_rate_oracle(w, x, dout, budget_s):
+    """The numpy fp64 backward oracle on sampled (batch, channel) rows for about
+    budget_s seconds; returns (GB/s in the bench metric, seconds, rows)."""
+    import numpy as np
+    from oracle import backward as bwd_oracle
+    cb = workloads.backward_compulsory_bytes(w)
+    nrows = w.batch * w.dim
+    rng = np.random.default_rng(0)
+    # the stored inputs widened to fp64 once (the oracle's own first step), outside the timing
+    f64 = {k: (None if x[k] is None else x[k].double().numpy()) for k in NAMES}
+    g64 = dout.double().numpy()
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        r = int(rng.integers(nrows))
+        bwd_oracle.selective_scan_bwd_rows([(r // w.dim, r % w.dim)], g64, **f64,
+                                           delta_softplus=x["delta_softplus"])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= nrows:
+            return cb / nrows * n / el / 1e9, el, n
+
+
+def run_bwd(args, rank, world, local_rank):
+    """One selective-scan backward (ss_bwd: the zero fill of the reduced
+    gradients and the kernel) per bench step."""
+    import torch
+    from state_space_model_03_gb300 import api
+
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w)
+    dout_h = workloads.make_dout(w)
+    cb = workloads.backward_compulsory_bytes(w)
+    pairs = w.elems * w.dstate
+    base_cfg = {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": w.dstate,
+                "groups": w.groups, "bc": w.bc, "has_z": w.has_z}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        gbs, el, n = _bwd_rate_oracle(w, x, dout_h, max(1.0, args.cpu_budget))
+        cpu = {"value": gbs, "unit": "GB/s", "kind": "oracle", "cores": 1,
+               "sample": f"{n} of {w.batch * w.dim} rows of {w.name}, numpy fp64 backward oracle, {el:.1f} s"}
+        print(json.dumps({"impl": "reference", "metric": BWD_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1,
+                          "steps": 1, "warmup": 0, "ms_per_step": cb / (gbs * 1e9) * 1e3, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic (seeded, Mamba-layer shapes)", "config": base_cfg,
+                          "cpu_baseline": cpu,
+                          "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = api.load_library()
+    d = {k: (None if x[k] is None else x[k].to(dev)) for k in NAMES}
+    u, delta, A, B, C, D, z, bias = api.normalise(*(d[k] for k in NAMES))
+    dout = dout_h.to(dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    du, ddelta = torch.empty_like(u), torch.empty_like(u)
+    dz = torch.empty_like(u) if z is not None else None
+    dA, dB, dC = torch.empty(A.shape, **f32), torch.empty(B.shape, **f32), torch.empty(C.shape, **f32)
+    dD = torch.empty(w.dim, **f32) if D is not None else None
+    ddb = torch.empty(w.dim, **f32) if bias is not None else None
+    params = api.make_bwd_params(dout, u, delta, A, B, C, D, z, bias, x["delta_softplus"], None,
+                                 du, ddelta, dz, dA, dB, dC, dD, ddb, None)
+    ws = api.attach_bwd_workspace(params, dev)  # noqa: F841 (kept alive for the calls below)
+    pref = ctypes.byref(params)
+    stream = torch.cuda.Stream(device=dev)
+    sptr = stream.cuda_stream
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def step():
+        st = lib.ss_bwd(pref, sptr)
+        if st != 0:
+            raise RuntimeError(api.status_string(st))
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            flush_buf.fill_(i & 0xFF)
+            step()
+    stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk, torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush_buf.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    if api.device_error() != 0:
+        raise RuntimeError("device-side error word set")
+    kms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+    ms = max_over_ranks([sum(kms) / len(kms)], world, dev)[0]
+    gbs = job_rate(cb, world, ms) / 1e9
+    clocks = clk.summary()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = nsm * FP32_LANES_PER_SM * 2070e6 / 1e9  # Gop/s at the maximum SM clock
+    achieved = BWD_OPS_PER_PAIR * pairs / (ms * 1e-3) / 1e9
+    # end to end: inputs from pinned host memory, every gradient back to pinned host memory
+    hin = {k: (None if t is None else t.pin_memory()) for k, t in
+           (("u", x["u"]), ("delta", x["delta"]), ("z", x["z"]), ("B", x["B"]), ("C", x["C"]), ("dout", dout_h))}
+    dins = {"u": u, "delta": delta, "z": z, "B": B, "C": C, "dout": dout}
+    outs = [t for t in (du, ddelta, dz, dA, dB, dC, dD, ddb) if t is not None]
+    houts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in hin.values() if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in houts)
+    e2e_steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for k, t in hin.items():
+                if t is not None:
+                    dins[k].copy_(t.view(dins[k].shape), non_blocking=True)
+            step()
+            for ho, do in zip(houts, outs):
+                ho.copy_(do, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], world, dev)[0]
+    if rank != 0:
+        return
+    line = {
+        "metric": BWD_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {"fp32": "f32", "fp16": "f16", "bf16": "bf16"}[w.dtype],
+        "data": "synthetic (seeded, Mamba-layer shapes)",
+        "config": dict(base_cfg, parallelism=f"independent x{world}",
+                       l2=f"flushed before every step ({2 * l2 >> 20} MiB write, outside the kernel interval)"),
+        "elems_per_s": job_rate(w.elems, world, ms),
+        "compulsory_bytes_per_step": cb,
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "Gop/s",
+                     "frac": achieved / alu_peak,
+                     "peak_source": f"derived: {nsm} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2070 MHz",
+                     "ops_per_pair": BWD_OPS_PER_PAIR, "traffic": _traffic(w.name + ":bwd", "bwd")},
+        "hbm": {"achieved_gbs": gbs, "peak": _peaks()[0], "frac": gbs / _peaks()[0]},
+        "e2e": {"value": job_rate(cb, world, e2e_ms) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "memsets_per_step": 3 + (D is not None) + (bias is not None),
+        "clocks": clocks,
+        "kernel_hash": _kernel_hash("bwd"),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        gbs_cpu, el, n = _bwd_rate_oracle(w, x, dout_h, min(args.cpu_budget, 10.0))
+        line["cpu_baseline"] = {"value": gbs_cpu, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n} of {w.batch * w.dim} rows of {w.name}, numpy fp64 backward "
+                                          f"oracle, {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--op", default="scan", choices=["scan", "state_update", "conv1d"],
+    ap.add_argument("--op", default="scan", choices=["scan", "state_update", "conv1d", "bwd"],
                     help="scan: the selective-scan forward (the headline); state_update: one decode step; "
-                         "conv1d: the causal conv1d forward")
+                         "conv1d: the causal conv1d forward; bwd: the selective-scan backward")
     ap.add_argument("--workload", default=None,
                     choices=sorted(workloads.WORKLOADS) + sorted(workloads.DECODE_WORKLOADS)
                     + sorted(workloads.CONV_WORKLOADS))
@@ -668,7 +836,19 @@ def main():
     if args.workload is None:
         args.workload = DEFAULT_WORKLOAD
     elif args.workload not in workloads.WORKLOADS:
-        ap.error("--op scan takes a forward workload")
+        ap.error(f"--op {args.op} takes a scan workload")
+    if args.op == "bwd":
+        if world > 1 and args.impl == "ours":
+            import torch
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl")
+        try:
+            run_bwd(args, rank, world, local_rank)
+        finally:
+            if world > 1 and args.impl == "ours":
+                import torch
+                torch.distributed.destroy_process_group()
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

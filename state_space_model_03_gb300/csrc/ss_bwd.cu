@@ -29,9 +29,13 @@ namespace ssk {
 
 namespace {
 
-constexpr int kBwdWarps = 8;
+#ifndef SSB_WARPS
+#define SSB_WARPS 8
+#endif
+constexpr int kBwdWarps = SSB_WARPS;  // rows (warps) per CTA
 constexpr int kE = 8;          // steps per lane
 constexpr int kCH = 32 * kE;   // steps per chunk
+static_assert(kE == 8, "the dB/dC reduction splits a lane's run into two quads");
 constexpr int kMaxN = 64;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -105,13 +109,31 @@ __device__ __forceinline__ void scan_down(float &P, float &Q, int lane) {
   }
 }
 
+constexpr int kNB = 16;  // states of variable B/C staged in shared memory at a time
+
+// Shared-memory carve-up (bytes), per instantiation.
+template <typename BCT, bool FIXED>
+struct BwdSmem {
+  static constexpr int kRows = kBwdWarps * kMaxN;                     // per-row, per-state floats
+  static constexpr int kRed = FIXED ? 0 : 2 * 2 * kBwdWarps * kCH;    // dB/dC terms, double-buffered
+  static constexpr int kStage = FIXED ? 0 : 2 * kNB * kCH * (int)sizeof(BCT);  // B, C of kNB states
+  static constexpr int kSmall = (FIXED ? 7 : 3) * kRows;             // carry, dA, A (+ dB, dC sums, B, C values)
+  static constexpr int kBytes = kRed * 4 + kStage + kSmall * 4;
+};
+
 template <typename T, typename BCT, bool FIXED>
 __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_constant__ BwdParams p) {
-  __shared__ __align__(16) float sred[2][2][kBwdWarps][kCH];  // variable dB/dC terms, double-buffered
-  __shared__ float scar[kBwdWarps][kMaxN];                    // state / adjoint carry per row and state
-  __shared__ float sdA[kBwdWarps][kMaxN];
-  __shared__ float sdB[kBwdWarps][kMaxN];                     // fixed B/C: per-row sums
-  __shared__ float sdC[kBwdWarps][kMaxN];
+  using SM = BwdSmem<BCT, FIXED>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  float *sred = reinterpret_cast<float *>(smem);                                  // [2][2][K][kCH]
+  BCT *sbc = reinterpret_cast<BCT *>(smem + SM::kRed * 4);                          // [2][kNB][kCH]
+  float *small = reinterpret_cast<float *>(smem + SM::kRed * 4 + SM::kStage);
+  float *scar = small;                      // [K][kMaxN] state / adjoint carry
+  float *sdA = small + SM::kRows;           // [K][kMaxN]
+  float *sAr = small + 2 * SM::kRows;       // [K][kMaxN] A of the row
+  float *sdB = small + 3 * SM::kRows;       // fixed: [K][kMaxN] dB, dC sums and B, C values
+  float *sdC = small + 4 * SM::kRows;
+  float *sBf = small + 5 * SM::kRows;       // fixed: [2][K][kMaxN] B then C values of the rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.dstate, L = p.seqlen, nch = p.nch;
@@ -127,7 +149,6 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_
   const T *dl_row = static_cast<const T *>(p.delta) + b * p.sd[0] + d * p.sd[1];
   const T *z_row = p.has_z ? static_cast<const T *>(p.z) + b * p.sz[0] + d * p.sz[1] : nullptr;
   const T *g_row = static_cast<const T *>(p.dout) + b * p.sg[0] + d * p.sg[1];
-  const float *a_row = p.A + d * p.sA;
   const float bias = p.bias ? p.bias[d] : 0.f;
   const float Dd = p.D ? p.D[d] : 0.f;
   float *ws_row = p.ws + row * nch * N;
@@ -135,14 +156,50 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_
                             : static_cast<const BCT *>(p.B) + b * p.sB[0] + g * p.sB[1];
   const BCT *C_base = FIXED ? static_cast<const BCT *>(p.C) + d * p.sC[0]
                             : static_cast<const BCT *>(p.C) + b * p.sC[0] + g * p.sC[1];
+  float *const my_car = scar + warp * kMaxN;
+  float *const my_dA = sdA + warp * kMaxN;
+  float *const my_A = sAr + warp * kMaxN;
 
   for (int n = lane; n < N; n += 32) {
-    scar[warp][n] = (p.init && active) ? p.init[b * p.si[0] + d * p.si[1] + n] : 0.f;
-    sdA[warp][n] = 0.f;
-    sdB[warp][n] = 0.f;
-    sdC[warp][n] = 0.f;
+    my_car[n] = (p.init && active) ? p.init[b * p.si[0] + d * p.si[1] + n] : 0.f;
+    my_dA[n] = 0.f;
+    my_A[n] = p.A[d * p.sA + n];
+    if constexpr (FIXED) {
+      sdB[warp * kMaxN + n] = 0.f;
+      sdC[warp * kMaxN + n] = 0.f;
+      sBf[warp * kMaxN + n] = to_f<BCT>(B_base[n]);
+      sBf[kBwdWarps * kMaxN + warp * kMaxN + n] = to_f<BCT>(C_base[n]);  // C values follow B's
+    }
   }
   __syncwarp();
+
+  // Variable B/C: copy states [n0, n0 + nb) of chunk c into shared memory
+  // (B only when !with_c); zeros past the end of the row. Whole CTA.
+  auto stage = [&](int c, int n0, int nb, bool with_c) {
+    __syncthreads();  // earlier readers of the stage are done
+    constexpr int G = 16 / (int)sizeof(BCT);  // elements per 16-byte group
+    const int per_mat = nb * (kCH / G);
+    const int total = (with_c ? 2 : 1) * per_mat;
+    for (int e = threadIdx.x; e < total; e += kBwdWarps * 32) {
+      const int which = e >= per_mat;
+      const int rem = e - which * per_mat;
+      const int nn = rem / (kCH / G), tg = (rem - nn * (kCH / G)) * G;
+      const int t = c * kCH + tg;
+      const BCT *src = (which ? C_base + (n0 + nn) * p.sC[2] : B_base + (n0 + nn) * p.sB[2]) + t;
+      BCT *dst = sbc + (which * kNB + nn) * kCH + tg;
+      if (p.bcvec && t + G <= L) {
+        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+      } else {
+#pragma unroll
+        for (int j = 0; j < G; ++j) dst[j] = t + j < L ? src[j] : from_f<BCT>(0.f);
+      }
+    }
+    __syncthreads();
+  };
+  // the lane's kE values of state n (relative to the staged block) of B (which 0) or C (1)
+  auto staged = [&](int which, int nn, float (&v)[kE]) {
+    load_steps<BCT>(sbc + (which * kNB + nn) * kCH + lane * kE, true, kE, v);
+  };
 
   // dt and dt*u of this lane's steps of chunk c (0 past the end of the row)
   auto load_dt = [&](int c, float (&dt)[kE], float (&uu)[kE], float (&v)[kE], int &valid, int &t0) {
@@ -162,36 +219,41 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_
     float dt[kE], uu[kE], v[kE];
     int valid, t0;
     load_dt(c, dt, uu, v, valid, t0);
-    for (int n = 0; n < N; ++n) {
-      const float A2 = a_row[n] * kLog2e;
-      float Bv[kE];
-      if constexpr (FIXED) {
-        const float bf = to_f<BCT>(B_base[n]);
+    for (int n0 = 0; n0 < N; n0 += kNB) {
+      const int nb = min(kNB, N - n0);
+      if constexpr (!FIXED) stage(c, n0, nb, false);
+      for (int nn = 0; nn < nb; ++nn) {
+        const int n = n0 + nn;
+        const float A2 = my_A[n] * kLog2e;
+        float Bv[kE];
+        if constexpr (FIXED) {
+          const float bf = sBf[warp * kMaxN + n];
 #pragma unroll
-        for (int i = 0; i < kE; ++i) Bv[i] = bf;
-      } else {
-        load_steps<BCT>(B_base + n * p.sB[2] + t0, p.bcvec, valid, Bv);
-      }
-      float P = 1.f, Q = 0.f;
+          for (int i = 0; i < kE; ++i) Bv[i] = bf;
+        } else {
+          staged(0, nn, Bv);
+        }
+        float P = 1.f, Q = 0.f;
 #pragma unroll
-      for (int i = 0; i < kE; ++i) {
-        const float a = ex2(dt[i] * A2);
-        Q = fmaf(a, Q, dt[i] * uu[i] * Bv[i]);
-        P *= a;
-      }
-      scan_up(P, Q, lane);
-      const float Pc = __shfl_sync(kFull, P, 31), Qc = __shfl_sync(kFull, Q, 31);
-      if (lane == 0) {
-        const float h = scar[warp][n];
-        if (active) ws_row[(long long)c * N + n] = h;
-        scar[warp][n] = fmaf(Pc, h, Qc);
+        for (int i = 0; i < kE; ++i) {
+          const float a = ex2(dt[i] * A2);
+          Q = fmaf(a, Q, dt[i] * uu[i] * Bv[i]);
+          P *= a;
+        }
+        scan_up(P, Q, lane);
+        const float Pc = __shfl_sync(kFull, P, 31), Qc = __shfl_sync(kFull, Q, 31);
+        if (lane == 0) {
+          const float h = my_car[n];
+          if (active) ws_row[(long long)c * N + n] = h;
+          my_car[n] = fmaf(Pc, h, Qc);
+        }
       }
     }
     __syncwarp();
   }
 
   // ---- 2. backward, last chunk first ---------------------------------------
-  for (int n = lane; n < N; n += 32) scar[warp][n] = 0.f;  // adjoint entering the row's end
+  for (int n = lane; n < N; n += 32) my_car[n] = 0.f;  // adjoint entering the row's end
   __syncwarp();
   float dD_acc = 0.f, dbias_acc = 0.f;
   int it = 0;  // state-loop iterations so far: parity of the dB/dC buffer
@@ -206,7 +268,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_
       for (int i = 0; i < kE; ++i) {
         const float s = rcp(1.f + ex2(-gz[i] * kLog2e));
         const float go = dy[i];
-        dy[i] = go * gz[i] * s;                    // dout silu(z)
+        dy[i] = go * gz[i] * s;                      // dout silu(z)
         gz[i] = go * s * fmaf(gz[i], 1.f - s, 1.f);  // dout silu'(z)
       }
     }
@@ -219,113 +281,117 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_
       ddt[i] = 0.f;
       yv[i] = 0.f;
     }
+    // chunk-start states of this row: state n in lane n % 32 (n < 32) / (n >= 32)
+    const float hcA = (active && lane < N) ? ws_row[(long long)c * N + lane] : 0.f;
+    const float hcB = (active && lane + 32 < N) ? ws_row[(long long)c * N + lane + 32] : 0.f;
 
-    for (int n = 0; n < N; ++n, ++it) {
-      const float An = a_row[n], A2 = An * kLog2e;
-      float Bv[kE], Cv[kE], a[kE], h[kE];
-      if constexpr (FIXED) {
-        const float bf = to_f<BCT>(B_base[n]), cf = to_f<BCT>(C_base[n]);
+    for (int n0 = 0; n0 < N; n0 += kNB) {
+      const int nb = min(kNB, N - n0);
+      if constexpr (!FIXED) stage(c, n0, nb, true);
+      for (int nn = 0; nn < nb; ++nn, ++it) {
+        const int n = n0 + nn;
+        const float An = my_A[n], A2 = An * kLog2e;
+        float Bv[kE], Cv[kE], a[kE], h[kE];
+        if constexpr (FIXED) {
+          const float bf = sBf[warp * kMaxN + n], cf = sBf[kBwdWarps * kMaxN + warp * kMaxN + n];
+#pragma unroll
+          for (int i = 0; i < kE; ++i) {
+            Bv[i] = bf;
+            Cv[i] = cf;
+          }
+        } else {
+          staged(0, nn, Bv);
+          staged(1, nn, Cv);
+        }
+        // the lane's affine map x -> P x + Q over its steps
+        float P = 1.f, Q = 0.f;
 #pragma unroll
         for (int i = 0; i < kE; ++i) {
-          Bv[i] = bf;
-          Cv[i] = cf;
+          a[i] = ex2(dt[i] * A2);
+          Q = fmaf(a[i], Q, dt[i] * uu[i] * Bv[i]);
+          P *= a[i];
         }
-      } else {
-        load_steps<BCT>(B_base + n * p.sB[2] + t0, p.bcvec, valid, Bv);
-        load_steps<BCT>(C_base + n * p.sC[2] + t0, p.bcvec, valid, Cv);
-      }
-      // the lane's affine map x -> P x + Q over its steps
-      float P = 1.f, Q = 0.f;
+        const float Plane = P;
+        // states: chunk-start checkpoint through the lanes up to this one
+        scan_up(P, Q, lane);
+        const float hc = __shfl_sync(kFull, n < 32 ? hcA : hcB, n & 31);
+        float h0 = __shfl_up_sync(kFull, fmaf(P, hc, Q), 1);  // state before the lane's first step
+        if (lane == 0) h0 = hc;
+        float hp = h0;
 #pragma unroll
-      for (int i = 0; i < kE; ++i) {
-        a[i] = ex2(dt[i] * A2);
-        Q = fmaf(a[i], Q, dt[i] * uu[i] * Bv[i]);
-        P *= a[i];
-      }
-      const float Plane = P;
-      // states: chunk-start checkpoint through the lanes to the left
-      scan_up(P, Q, lane);
-      float Pe = __shfl_up_sync(kFull, P, 1), Qe = __shfl_up_sync(kFull, Q, 1);
-      if (lane == 0) {
-        Pe = 1.f;
-        Qe = 0.f;
-      }
-      const float hc = active ? ws_row[(long long)c * N + n] : 0.f;
-      const float h0 = fmaf(Pe, hc, Qe);  // state before the lane's first step
-      float hp = h0;
-#pragma unroll
-      for (int i = 0; i < kE; ++i) {
-        h[i] = fmaf(a[i], hp, dt[i] * uu[i] * Bv[i]);
-        hp = h[i];
-        yv[i] = fmaf(Cv[i], h[i], yv[i]);
-      }
-      // adjoint: the lane's map mu -> Plane mu + Qr (mu = a lam, passed to the left)
-      float Qr = 0.f;
-#pragma unroll
-      for (int i = kE - 1; i >= 0; --i) Qr = a[i] * fmaf(dy[i], Cv[i], Qr);
-      float Pr = Plane;
-      scan_down(Pr, Qr, lane);
-      float Pn = __shfl_down_sync(kFull, Pr, 1), Qn = __shfl_down_sync(kFull, Qr, 1);
-      if (lane == 31) {
-        Pn = 1.f;
-        Qn = 0.f;
-      }
-      float mu = fmaf(Pn, scar[warp][n], Qn);  // adjoint entering the lane's last step from the right
-      float dA_acc = 0.f, dBs = 0.f, dCs = 0.f;
-      float *rb = &sred[it & 1][0][warp][lane * kE];
-      float *rc = &sred[it & 1][1][warp][lane * kE];
-#pragma unroll
-      for (int i = kE - 1; i >= 0; --i) {
-        const float lam = fmaf(dy[i], Cv[i], mu);
-        const float ah = a[i] * (i > 0 ? h[i - 1] : h0);
-        const float ld = lam * dt[i];
-        du[i] = fmaf(ld, Bv[i], du[i]);
-        ddt[i] = fmaf(lam, fmaf(An, ah, Bv[i] * uu[i]), ddt[i]);
-        dA_acc = fmaf(ld, ah, dA_acc);
-        if constexpr (FIXED) {
-          dBs = fmaf(ld, uu[i], dBs);
-          dCs = fmaf(dy[i], h[i], dCs);
-        } else {
-          rb[i] = ld * uu[i];
-          rc[i] = dy[i] * h[i];
+        for (int i = 0; i < kE; ++i) {
+          h[i] = fmaf(a[i], hp, dt[i] * uu[i] * Bv[i]);
+          hp = h[i];
+          yv[i] = fmaf(Cv[i], h[i], yv[i]);
         }
-        mu = a[i] * lam;
-      }
-      __syncwarp();
-      if (lane == 0) scar[warp][n] = mu;  // leaves the chunk to the left
-      dA_acc = warp_sum(dA_acc);
-      if (lane == 0) sdA[warp][n] += dA_acc;
-      if constexpr (FIXED) {
-        dBs = warp_sum(dBs);
-        dCs = warp_sum(dCs);
-        if (lane == 0) {
-          sdB[warp][n] += dBs;
-          sdC[warp][n] += dCs;
-        }
-      } else {
-        // group sum over the CTA's rows, then one atomic per step and state
-        __syncthreads();
-        if (threadIdx.x < 2 * kCH / 4) {
-          const int which = threadIdx.x / (kCH / 4);
-          const int col = (threadIdx.x % (kCH / 4)) * 4;
-          float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        // adjoint: the lane's map mu -> Plane mu + Qr (mu = a lam, passed to the left)
+        float Qr = 0.f;
 #pragma unroll
-          for (int k = 0; k < kBwdWarps; ++k) {
-            const float4 q = *reinterpret_cast<const float4 *>(&sred[it & 1][which][k][col]);
-            s.x += q.x;
-            s.y += q.y;
-            s.z += q.z;
-            s.w += q.w;
-          }
-          const int t = c * kCH + col;
-          float *dst = (which ? p.dC : p.dB) + (((long long)b * p.ngroups + g) * N + n) * L + t;
-          if (p.dbvec && t + 4 <= L) {
-            atomicAdd(reinterpret_cast<float4 *>(dst), s);
+        for (int i = kE - 1; i >= 0; --i) Qr = a[i] * fmaf(dy[i], Cv[i], Qr);
+        float Pr = Plane;
+        scan_down(Pr, Qr, lane);
+        const float mc = my_car[n];
+        float mu = __shfl_down_sync(kFull, fmaf(Pr, mc, Qr), 1);  // adjoint entering the lane's last step
+        if (lane == 31) mu = mc;
+        float dA_acc = 0.f, dBs = 0.f, dCs = 0.f;
+        // dB/dC terms, step-major within the row: [i][lane] (conflict-free stores)
+        float *rb = sred + (((it & 1) * 2 + 0) * kBwdWarps + warp) * kCH + lane;
+        float *rc = sred + (((it & 1) * 2 + 1) * kBwdWarps + warp) * kCH + lane;
+#pragma unroll
+        for (int i = kE - 1; i >= 0; --i) {
+          const float lam = fmaf(dy[i], Cv[i], mu);
+          const float ah = a[i] * (i > 0 ? h[i - 1] : h0);
+          const float ld = lam * dt[i];
+          du[i] = fmaf(ld, Bv[i], du[i]);
+          ddt[i] = fmaf(lam, fmaf(An, ah, Bv[i] * uu[i]), ddt[i]);
+          dA_acc = fmaf(ld, ah, dA_acc);
+          if constexpr (FIXED) {
+            dBs = fmaf(ld, uu[i], dBs);
+            dCs = fmaf(dy[i], h[i], dCs);
           } else {
-            const float sv[4] = {s.x, s.y, s.z, s.w};
+            rb[i * 32] = ld * uu[i];
+            rc[i * 32] = dy[i] * h[i];
+          }
+          mu = a[i] * lam;
+        }
+        __syncwarp();
+        if (lane == 0) my_car[n] = mu;  // leaves the chunk to the left
+        dA_acc = warp_sum(dA_acc);
+        if (lane == 0) my_dA[n] += dA_acc;
+        if constexpr (FIXED) {
+          dBs = warp_sum(dBs);
+          dCs = warp_sum(dCs);
+          if (lane == 0) {
+            sdB[warp * kMaxN + n] += dBs;
+            sdC[warp * kMaxN + n] += dCs;
+          }
+        } else {
+          // group sum over the CTA's rows, then one atomic per step and state
+          __syncthreads();
+          if (threadIdx.x < 2 * kCH / 4) {
+            // thread: B or C, steps 4q .. 4q+3 of lane l's run of kE steps
+            const int which = threadIdx.x / (kCH / 4);
+            const int r = threadIdx.x % (kCH / 4);
+            const int l = r & 31, i0 = (r >> 5) * 4;
+            const float *src = sred + ((it & 1) * 2 + which) * kBwdWarps * kCH + i0 * 32 + l;
+            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (t + j < L) atomicAdd(dst + j, sv[j]);
+            for (int k = 0; k < kBwdWarps; ++k) {
+              s.x += src[k * kCH];
+              s.y += src[k * kCH + 32];
+              s.z += src[k * kCH + 64];
+              s.w += src[k * kCH + 96];
+            }
+            const int t = c * kCH + l * kE + i0;
+            float *dst = (which ? p.dC : p.dB) + (((long long)b * p.ngroups + g) * N + n) * L + t;
+            if (p.dbvec && t + 4 <= L) {
+              atomicAdd(reinterpret_cast<float4 *>(dst), s);
+            } else {
+              const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (t + j < L) atomicAdd(dst + j, sv[j]);
+            }
           }
         }
       }
@@ -356,29 +422,35 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_
     if (p.dbias) atomicAdd(p.dbias + d, dbias_acc);
   }
   for (int n = lane; n < N; n += 32) {
-    atomicAdd(p.dA + (long long)d * N + n, sdA[warp][n]);
+    atomicAdd(p.dA + (long long)d * N + n, my_dA[n]);
     if constexpr (FIXED) {
-      atomicAdd(p.dB + (long long)d * N + n, sdB[warp][n]);
-      atomicAdd(p.dC + (long long)d * N + n, sdC[warp][n]);
+      atomicAdd(p.dB + (long long)d * N + n, sdB[warp * kMaxN + n]);
+      atomicAdd(p.dC + (long long)d * N + n, sdC[warp * kMaxN + n]);
     }
-    if (p.dx0) p.dx0[row * N + n] = scar[warp][n];
+    if (p.dx0) p.dx0[row * N + n] = my_car[n];
   }
 }
 
+template <typename T, typename BCT, bool FIXED>
+BwdKernel info() {
+  return {(const void *)&ss_bwd_kernel<T, BCT, FIXED>, BwdSmem<BCT, FIXED>::kBytes};
+}
+
 template <typename T, typename BCT>
-const void *pick(bool fixed) {
+BwdKernel pick(bool fixed) {
   if constexpr (sizeof(BCT) == 4) {
-    if (fixed) return (const void *)&ss_bwd_kernel<T, float, true>;
+    if (fixed) return info<T, float, true>();
   }
-  return (const void *)&ss_bwd_kernel<T, BCT, false>;
+  return info<T, BCT, false>();
 }
 
 }  // namespace
 
 int bwd_chunk_steps() { return kCH; }
 int bwd_rows_per_cta() { return kBwdWarps; }
+int bwd_threads() { return kBwdWarps * 32; }
 
-const void *bwd_kernel(int in_dtype, bool bc_f32, bool fixed) {
+BwdKernel bwd_kernel(int in_dtype, bool bc_f32, bool fixed, int /*dstate: one kernel serves 1..64 states*/) {
   switch (in_dtype) {
     case 0: return pick<float, float>(fixed);
     case 1: return bc_f32 ? pick<__half, float>(fixed) : pick<__half, __half>(false);

@@ -76,8 +76,13 @@ struct BwdParams {
   float *ws;        // chunk-start states (batch, dim, nch, dstate)
   long long su[2], sd[2], sz[2], sg[2], sdu[2], sdd[2], sdz[2], sB[3], sC[3], sA, si[2];
 };
-int bwd_chunk_steps();
-int bwd_rows_per_cta();
-const void *bwd_kernel(int in_dtype, bool bc_f32, bool fixed);
+int bwd_chunk_steps();   // steps per chunk (checkpoint interval)
+int bwd_rows_per_cta();  // channels per CTA
+int bwd_threads();       // threads per CTA
+struct BwdKernel {
+  const void *fn;
+  int smem;  // dynamic shared memory bytes
+};
+BwdKernel bwd_kernel(int in_dtype, bool bc_f32, bool fixed, int dstate);
 
 }  // namespace ssk

@@ -26,6 +26,7 @@ std::mutex g_mu;
 int32_t *g_err_ptr[kMaxDevices] = {};
 bool g_attr_done[kMaxDevices][3][5][2][2][2][2][2][2] = {};
 int g_occupancy[kMaxDevices][3][5][2][2][3] = {};  // CTAs/SM of the TMA forward variants 0, 1, 2
+bool g_bwd_attr_done[kMaxDevices][3][2][2] = {};     // dynamic shared memory attribute set for ss_bwd
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -999,13 +1000,24 @@ int launch_bwd(const ss_bwd_params *p, cudaStream_t stream) {
     k.bcvec = (p->B_stride[i] * bs) % 16 == 0 && (p->C_stride[i] * bs) % 16 == 0;
   k.dbvec = !fixed && aligned(p->dB, 16) && aligned(p->dC, 16) && p->seqlen % 4 == 0;
   const bool bc_f32 = fixed || p->bc_dtype == SS_F32;
-  const void *fn = ssk::bwd_kernel(p->in_dtype, bc_f32, fixed);
+  const ssk::BwdKernel ki = ssk::bwd_kernel(p->in_dtype, bc_f32, fixed, k.dstate);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SS_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    bool &done = g_bwd_attr_done[dev][p->in_dtype][bc_f32][fixed];
+    if (!done && ki.smem > 0) {
+      if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) != cudaSuccess)
+        return SS_ERR_CUDA;
+      done = true;
+    }
+  }
   const int64_t gx = static_cast<int64_t>(k.ngroups) * k.tiles;
   const int64_t gy = std::min<int64_t>(p->batch, 65535), gz = (p->batch + gy - 1) / gy;
   if (gx > 0x7fffffff || gz > 65535) return SS_ERR_UNSUPPORTED;
   void *args[1] = {&k};
-  return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(gz)),
-                          dim3(rows * 32), args, 0, stream) == cudaSuccess
+  return cudaLaunchKernel(ki.fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(gz)),
+                          dim3(ssk::bwd_threads()), args, ki.smem, stream) == cudaSuccess
              ? SS_OK
              : SS_ERR_CUDA;
 }
