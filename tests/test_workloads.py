@@ -68,3 +68,17 @@ def test_compulsory_bytes_table():
     }
     for k, v in expect.items():
         assert workloads.compulsory_bytes(workloads.WORKLOADS[k]) == v, k
+
+
+def test_dout_and_backward_bytes():
+    """The backward's upstream gradient is seeded and shaped like u; the
+    backward's compulsory bytes follow the formula in its docstring."""
+    w = workloads.WORKLOADS["mamba130m_bf16"]
+    small = workloads.Workload("s", 2, 8, 40, 16, dtype="bf16", seed=5)
+    a, b = workloads.make_dout(small), workloads.make_dout(small)
+    assert a.shape == (2, 8, 40) and a.dtype == torch.bfloat16 and torch.equal(a, b)
+    assert not torch.equal(a, workloads.make_dout(small, seed=6))
+    # u, delta, z, dout read and du, ddelta, dz written (2 bytes); B, C read (2) and dB, dC written (4);
+    # A read and dA written; D, bias read and their gradients written
+    want = (2 * 7 * 8 * 1536 * 2048 + 2 * 8 * 16 * 2048 * (2 + 4) + 2 * 1536 * 16 * 4 + 2 * 1536 * 4 * 2)
+    assert workloads.backward_compulsory_bytes(w) == want
