@@ -22,6 +22,7 @@ import ctypes
 import glob
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -65,6 +66,7 @@ KERNEL_SOURCES = {
     "state_update": ("ss_state_update.cu",),
     "conv1d": ("ss_conv1d.cu",),
     "bwd": ("ss_bwd.cu",),
+    "complex": ("ss_fwd_complex.cu",),
 }
 
 
@@ -787,14 +789,182 @@ def run_bwd(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+CX_METRIC = "complex-A selective-scan fwd HBM GB/s (compulsory bytes / kernel time)"
+# Algorithmic fp32 operations of the complex-A forward per (batch, channel,
+# state, step): dt Re A, dt Im A (2), the decay's two parts e cos, e sin (2),
+# x <- a x + (dt u) B (5), y += C Re x (1); plus exp, sin and cos.
+CX_OPS_PER_PAIR = 10
+
+
+def _complex_A(w):
+    """An S4D-Lin-like complex A: -1/2 + i pi n for state n, every channel."""
+    import torch
+    n = torch.arange(w.dstate, dtype=torch.float32)
+    return torch.complex(torch.full((w.dim, w.dstate), -0.5), (math.pi * n).expand(w.dim, w.dstate).contiguous())
+
+
+def _cx_rate_oracle(w, x, budget_s):
+    """The complex-A fp64 oracle on sampled (batch, channel) rows for about
+    budget_s seconds; returns (GB/s in the bench metric, seconds, rows)."""
+    import numpy as np
+    from oracle import complex_a
+    cb = workloads.compulsory_bytes(w) + w.dim * w.dstate * 4  # A is twice as wide
+    nrows = w.batch * w.dim
+    rng = np.random.default_rng(0)
+    f64 = {k: (None if x[k] is None else (x[k].numpy() if x[k].is_complex() else x[k].double().numpy()))
+           for k in NAMES}
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        r = int(rng.integers(nrows))
+        b, d = r // w.dim, r % w.dim
+        sl = {k: (f64[k][b:b + 1, d:d + 1] if k in ("u", "delta", "z") and f64[k] is not None else f64[k])
+              for k in NAMES}
+        sl["A"] = f64["A"][d:d + 1]
+        sl["D"] = None if f64["D"] is None else f64["D"][d:d + 1]
+        sl["delta_bias"] = None if f64["delta_bias"] is None else f64["delta_bias"][d:d + 1]
+        if f64["B"].ndim == 2:
+            sl["B"], sl["C"] = f64["B"][d:d + 1], f64["C"][d:d + 1]
+        elif f64["B"].ndim == 3:
+            sl["B"], sl["C"] = f64["B"][b:b + 1], f64["C"][b:b + 1]
+        else:
+            gi = d // (w.dim // f64["B"].shape[1])
+            sl["B"], sl["C"] = f64["B"][b:b + 1, gi:gi + 1], f64["C"][b:b + 1, gi:gi + 1]
+        complex_a.selective_scan_complex_ref(**sl, delta_softplus=x["delta_softplus"])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= nrows:
+            return cb / nrows * n / el / 1e9, el, n
+
+
+def run_complex(args, rank, world, local_rank):
+    """One complex-A forward (ss_fwd_complex) per bench step."""
+    import torch
+    from state_space_model_03_gb300 import api
+
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w)
+    x["A"] = _complex_A(w)
+    cb = workloads.compulsory_bytes(w) + w.dim * w.dstate * 4
+    pairs = w.elems * w.dstate
+    base_cfg = {"workload": w.name + " (complex A = -1/2 + i pi n)", "batch": w.batch, "dim": w.dim,
+                "seqlen": w.seqlen, "dstate": w.dstate, "groups": w.groups, "bc": w.bc, "has_z": w.has_z}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        gbs, el, n = _cx_rate_oracle(w, x, max(1.0, args.cpu_budget))
+        cpu = {"value": gbs, "unit": "GB/s", "kind": "oracle", "cores": 1,
+               "sample": f"{n} of {w.batch * w.dim} rows, numpy fp64 complex-A oracle, {el:.1f} s"}
+        print(json.dumps({"impl": "reference", "metric": CX_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1,
+                          "steps": 1, "warmup": 0, "ms_per_step": cb / (gbs * 1e9) * 1e3, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic (seeded, Mamba-layer shapes)", "config": base_cfg,
+                          "cpu_baseline": cpu,
+                          "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = api.load_library()
+    d = {k: (None if x[k] is None else x[k].to(dev)) for k in NAMES}
+    u, delta, A, B, C, D, z, bias = api.normalise(*(d[k] for k in NAMES))
+    out = torch.empty_like(u)
+    params = api.make_complex_params(u, delta, A, B, C, D, z, bias, x["delta_softplus"], out, None)
+    pref = ctypes.byref(params)
+    stream = torch.cuda.Stream(device=dev)
+    sptr = stream.cuda_stream
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def step():
+        st = lib.ss_fwd_complex(pref, sptr)
+        if st != 0:
+            raise RuntimeError(api.status_string(st))
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            flush_buf.fill_(i & 0xFF)
+            step()
+    stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk, torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush_buf.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    kms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+    ms = max_over_ranks([sum(kms) / len(kms)], world, dev)[0]
+    gbs = job_rate(cb, world, ms) / 1e9
+    clocks = clk.summary()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = nsm * FP32_LANES_PER_SM * 2070e6 / 1e9
+    achieved = CX_OPS_PER_PAIR * pairs / (ms * 1e-3) / 1e9
+    # end to end: inputs from pinned host memory, out back to pinned host memory
+    hin = {k: t.pin_memory() for k, t in (("u", x["u"]), ("delta", x["delta"]), ("z", x["z"]), ("B", x["B"]),
+                                          ("C", x["C"])) if t is not None}
+    dins = {"u": u, "delta": delta, "z": z, "B": B, "C": C}
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for k, t in hin.items():
+                dins[k].copy_(t.view(dins[k].shape), non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], world, dev)[0]
+    if rank != 0:
+        return
+    line = {
+        "metric": CX_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {"fp32": "f32", "fp16": "f16", "bf16": "bf16"}[w.dtype],
+        "data": "synthetic (seeded, Mamba-layer shapes)",
+        "config": dict(base_cfg, parallelism=f"independent x{world}",
+                       l2=f"flushed before every step ({2 * l2 >> 20} MiB write, outside the kernel interval)"),
+        "elems_per_s": job_rate(w.elems, world, ms),
+        "compulsory_bytes_per_step": cb,
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "Gop/s",
+                     "frac": achieved / alu_peak,
+                     "peak_source": f"derived: {nsm} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2070 MHz",
+                     "ops_per_pair": CX_OPS_PER_PAIR, "traffic": _traffic(w.name + ":complex", "complex")},
+        "hbm": {"achieved_gbs": gbs, "peak": _peaks()[0], "frac": gbs / _peaks()[0]},
+        "e2e": {"value": job_rate(cb, world, e2e_ms) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
+                "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "kernel_hash": _kernel_hash("complex"),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        gbs_cpu, el, n = _cx_rate_oracle(w, x, min(args.cpu_budget, 10.0))
+        line["cpu_baseline"] = {"value": gbs_cpu, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n} of {w.batch * w.dim} rows of {w.name}, numpy fp64 complex-A "
+                                          f"oracle, {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--op", default="scan", choices=["scan", "state_update", "conv1d", "bwd"],
+    ap.add_argument("--op", default="scan", choices=["scan", "state_update", "conv1d", "bwd", "complex"],
                     help="scan: the selective-scan forward (the headline); state_update: one decode step; "
-                         "conv1d: the causal conv1d forward; bwd: the selective-scan backward")
+                         "conv1d: the causal conv1d forward; bwd: the selective-scan backward; "
+                         "complex: the complex-A forward")
     ap.add_argument("--workload", default=None,
                     choices=sorted(workloads.WORKLOADS) + sorted(workloads.DECODE_WORKLOADS)
                     + sorted(workloads.CONV_WORKLOADS))
@@ -837,13 +1007,13 @@ def main():
         args.workload = DEFAULT_WORKLOAD
     elif args.workload not in workloads.WORKLOADS:
         ap.error(f"--op {args.op} takes a scan workload")
-    if args.op == "bwd":
+    if args.op in ("bwd", "complex"):
         if world > 1 and args.impl == "ours":
             import torch
             torch.cuda.set_device(local_rank)
             torch.distributed.init_process_group("nccl")
         try:
-            run_bwd(args, rank, world, local_rank)
+            (run_bwd if args.op == "bwd" else run_complex)(args, rank, world, local_rank)
         finally:
             if world > 1 and args.impl == "ours":
                 import torch

@@ -382,6 +382,53 @@ int ss_bwd_workspace_size(const ss_bwd_params *p, int64_t *bytes);
 int ss_bwd(const ss_bwd_params *p, void *stream);
 
 /*
+ * Complex-A variant of ss_fwd. Section 4.1 of the page says that A (dim,
+ * dstate) may be real or complex and gives B and C only their real shapes.
+ * With complex A the state is complex and the real output takes the real part
+ * of the contraction, per (batch b, channel d, state n, step t):
+ *
+ *     x[n] = exp(dt * A[d,n]) * x[n] + dt * B[n,t] * u[b,d,t]     (complex A, x)
+ *     y    = Re(sum_n C[n,t] * x[n]) + D[d] * u[b,d,t]
+ *     out  = y * silu(z[b,d,t])  if z is given, else y
+ *
+ * with dt, B, C, D, z and delta_bias as for ss_fwd (real).
+ *
+ * Layout as in ss_fwd_params, except:
+ *   A                  (dim, dstate) complex64: interleaved (re, im) fp32
+ *                      pairs, 8-byte aligned; A_stride in complex elements,
+ *                      state stride 1.
+ *   last_state         (batch, dim, dstate) complex64 interleaved, strides in
+ *                      complex elements, state stride 1, 8-byte aligned; NULL =
+ *                      not returned (zeros for seqlen == 0).
+ *   initial_state      same layout, NULL = zero start; may be last_state itself
+ *                      with the same strides.
+ * Sizes: 1 <= dstate <= 64. Validation, errors and streams as for ss_fwd; no
+ * workspace is used.
+ */
+typedef struct ss_fwd_complex_params {
+  int32_t abi_version;      /* must be SS_ABI_VERSION */
+  int32_t in_dtype;         /* ss_dtype of u, delta, z, out */
+  int32_t bc_dtype;         /* ss_dtype of B, C */
+  int32_t bc_mode;          /* ss_bc_mode */
+  int32_t delta_softplus;
+  int32_t reserved0;
+  int64_t batch, dim, seqlen, dstate, ngroups;
+  const void *u, *delta, *z, *B, *C;
+  const float *A;           /* complex64, interleaved */
+  const float *D, *delta_bias;
+  void *out;
+  float *last_state;        /* complex64, interleaved */
+  const float *initial_state;
+  int64_t u_stride[3], delta_stride[3], z_stride[3], out_stride[3];
+  int64_t B_stride[4], C_stride[4];
+  int64_t A_stride[2];
+  int64_t last_state_stride[3], initial_state_stride[3];
+} ss_fwd_complex_params;
+
+int ss_fwd_complex_validate(const ss_fwd_complex_params *p);
+int ss_fwd_complex(const ss_fwd_complex_params *p, void *stream);
+
+/*
  * Device-side error word of the library on the current device (nonzero after
  * a kernel gave up on a bounded wait or tripped a self-check; 0 otherwise).
  * Reading it synchronises with the device. `clear` nonzero resets it to 0.

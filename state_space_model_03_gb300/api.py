@@ -98,6 +98,23 @@ class SSConv1dUpdateParams(ctypes.Structure):
     ]
 
 
+class SSFwdComplexParams(ctypes.Structure):
+    """Mirror of ``ss_fwd_complex_params``."""
+    _fields_ = [
+        ("abi_version", ctypes.c_int32), ("in_dtype", ctypes.c_int32), ("bc_dtype", ctypes.c_int32),
+        ("bc_mode", ctypes.c_int32), ("delta_softplus", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+        ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+        ("u", ctypes.c_void_p), ("delta", ctypes.c_void_p), ("z", ctypes.c_void_p),
+        ("B", ctypes.c_void_p), ("C", ctypes.c_void_p),
+        ("A", ctypes.c_void_p), ("D", ctypes.c_void_p), ("delta_bias", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("last_state", ctypes.c_void_p), ("initial_state", ctypes.c_void_p),
+        ("u_stride", _i64x3), ("delta_stride", _i64x3), ("z_stride", _i64x3), ("out_stride", _i64x3),
+        ("B_stride", _i64x4), ("C_stride", _i64x4), ("A_stride", _i64x2),
+        ("last_state_stride", _i64x3), ("initial_state_stride", _i64x3),
+    ]
+
+
 class SSBwdParams(ctypes.Structure):
     """Mirror of ``ss_bwd_params``."""
     _fields_ = [
@@ -171,6 +188,11 @@ def load_library():
             lib.ss_causal_conv1d_update_validate.restype = ctypes.c_int
             lib.ss_causal_conv1d_update.argtypes = [PU, vp]
             lib.ss_causal_conv1d_update.restype = ctypes.c_int
+            PX = ctypes.POINTER(SSFwdComplexParams)
+            lib.ss_fwd_complex_validate.argtypes = [PX]
+            lib.ss_fwd_complex_validate.restype = ctypes.c_int
+            lib.ss_fwd_complex.argtypes = [PX, vp]
+            lib.ss_fwd_complex.restype = ctypes.c_int
             PB = ctypes.POINTER(SSBwdParams)
             lib.ss_bwd_validate.argtypes = [PB]
             lib.ss_bwd_validate.restype = ctypes.c_int
@@ -207,9 +229,10 @@ def _unit_last(t):
 
 def normalise(u, delta, A, B, C, D=None, z=None, delta_bias=None):
     """Layout handling of the page's selective_scan_fn: unit last stride (else
-    .contiguous()), 3-D B/C -> 4-D with one group. Returns the tensors."""
-    if A.is_complex():
-        raise NotImplementedError("complex A is not supported (real A only)")
+    .contiguous()), 3-D B/C -> 4-D with one group. Returns the tensors. A
+    complex A becomes complex64 (the complex-A variant, ss_fwd_complex)."""
+    if A.is_complex() and A.dtype != torch.complex64:
+        A = A.to(torch.complex64)
     u, delta, z, B, C, A = (_unit_last(t) for t in (u, delta, z, B, C, A))
     if B.dim() == 3:
         B = B.unsqueeze(1)
@@ -313,6 +336,44 @@ def _forward(u, delta, A, B, C, D, z, delta_bias, delta_softplus, return_last_st
     return out, last
 
 
+def make_complex_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last_state,
+                        initial_state=None) -> SSFwdComplexParams:
+    """Fill an ss_fwd_complex_params from normalised tensors; A, last_state and
+    initial_state are complex64 (interleaved (re, im) in memory)."""
+    if A.dtype != torch.complex64 or A.dim() != 2:
+        raise TypeError("complex A must be complex64 (dim, dstate)")
+    # the real-A filler checks every other operand; A's real view stands in for it
+    f = make_params(u, delta, torch.view_as_real(A)[..., 0], B, C, D, z, delta_bias, delta_softplus, out, None)
+    p = SSFwdComplexParams()
+    for k in ("abi_version", "in_dtype", "bc_dtype", "bc_mode", "delta_softplus", "batch", "dim", "seqlen",
+              "dstate", "ngroups", "u", "delta", "z", "B", "C", "D", "delta_bias", "out"):
+        setattr(p, k, getattr(f, k))
+    for k in ("u_stride", "delta_stride", "z_stride", "out_stride", "B_stride", "C_stride"):
+        getattr(p, k)[:] = list(getattr(f, k))
+    p.A = A.data_ptr()
+    p.A_stride[:] = list(A.stride())
+    shape = (f.batch, f.dim, f.dstate)
+    for name, t in (("last_state", last_state), ("initial_state", initial_state)):
+        if t is not None:
+            if t.dtype != torch.complex64 or tuple(t.shape) != shape:
+                raise TypeError(f"{name} must be complex64 (batch, dim, dstate)")
+            setattr(p, name, t.data_ptr())
+            getattr(p, name + "_stride")[:] = list(t.stride())
+        else:
+            getattr(p, name + "_stride")[:] = [0, 0, 1]
+    return p
+
+
+def _forward_complex(u, delta, A, B, C, D, z, delta_bias, delta_softplus, return_last_state, initial_state):
+    out = torch.empty(u.shape, dtype=u.dtype, device=u.device)
+    last = (torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.complex64, device=u.device)
+            if return_last_state else None)
+    p = make_complex_params(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, last, initial_state)
+    with torch.cuda.device(u.device):
+        _check(load_library().ss_fwd_complex(ctypes.byref(p), torch.cuda.current_stream(u.device).cuda_stream))
+    return out, last
+
+
 def selective_scan_fn(u, delta, A, B, C, D=None, z=None, delta_bias=None,
                       delta_softplus=False, return_last_state=False, initial_state=None):
     """Selective-scan forward on CUDA tensors; runs on the current stream.
@@ -323,11 +384,23 @@ def selective_scan_fn(u, delta, A, B, C, D=None, z=None, delta_bias=None,
     fp32. D, delta_bias: (dim,) fp32. initial_state: optional (batch, dim,
     dstate) fp32 start state (zero if None). Returns out (u's dtype), or
     (out, last_state) with last_state (batch, dim, dstate) fp32. Differentiable
-    (through ss_bwd) in every input but last_state.
+    (through ss_bwd) in every input but last_state. A complex A (complex64,
+    real B/C) runs the complex-A variant (ss_fwd_complex; forward only): the
+    state and last_state are complex, out takes the real part of the
+    contraction.
     """
     if not u.is_cuda:
         raise RuntimeError("selective_scan_fn needs CUDA tensors (there is no CPU path)")
     ins = (u, delta, A, B, C, D, z, delta_bias, initial_state)
+    if A.is_complex():
+        if torch.is_grad_enabled() and any(t is not None and t.requires_grad for t in ins):
+            raise NotImplementedError("the complex-A variant is forward only")
+        u, delta, A, B, C, D, z, delta_bias = normalise(u, delta, A, B, C, D, z, delta_bias)
+        if initial_state is not None:
+            initial_state = _unit_last(initial_state.to(torch.complex64))
+        out, last = _forward_complex(u, delta, A, B, C, D, z, delta_bias, delta_softplus, return_last_state,
+                                     initial_state)
+        return (out, last) if return_last_state else out
     if torch.is_grad_enabled() and any(t is not None and t.requires_grad for t in ins):
         out, last = SelectiveScanFn.apply(u, delta, A, B, C, D, z, delta_bias, bool(delta_softplus),
                                           bool(return_last_state), initial_state)

@@ -85,4 +85,20 @@ struct BwdKernel {
 };
 BwdKernel bwd_kernel(int in_dtype, bool bc_f32, bool fixed, int dstate);
 
+// Complex-A forward (ss_fwd_complex).
+struct CxParams {
+  int batch, dim, dstate, ngroups, dpg, tiles;  // tiles: CTAs per group along the channels
+  int seqlen, nseg;                             // steps; segments of cx_segment_steps() steps
+  int has_z, softplus;
+  const void *u, *delta, *z, *B, *C;
+  const float *A, *D, *bias, *init;  // A, init: complex64 interleaved
+  void *out;
+  float *last;                       // complex64 interleaved
+  long long su[2], sd[2], sz[2], so[2], sB[3], sC[3], sA, si[2], sl[2];
+};
+int cx_segment_steps();
+int cx_channels_per_cta();
+int cx_threads();
+const void *cx_kernel(int in_dtype, bool bc_f32, bool fixed, int dstate);
+
 }  // namespace ssk

@@ -1,0 +1,192 @@
+// Complex-A selective-scan forward (section 4.1 of the page "PaddleNLP Kernel
+// 算子库：CUDA 与 Triton 双实现的高性能 NLP GPU 算子实战指南": A "real or complex").
+// Per (batch b, channel d, state n, step t), with complex A and state x:
+//   a = exp(dt A) = e^{dt Re A} (cos(dt Im A) + i sin(dt Im A))
+//   x = a x + dt B u,   y = Re(sum_n C x) + D u,   out = y silu(z)
+//
+// Schedule. A thread owns one (batch, channel, state) recurrence (two fp32
+// registers); the 16 lanes of a half-warp hold the states of one channel (with
+// more than 16 states a lane loops over n = j, j + 16, ...). The row is walked
+// in segments of kT steps: lane j prepares step t0 + j of the channel (dt,
+// dt u, the gate) into shared memory, every lane walks the segment for its
+// state(s) accumulating its part of y per step, and a reduce-scatter over the
+// 16 lanes leaves lane j with step t0 + j's sum, which it gates and stores.
+// There is no cross-warp communication, so warps run independently.
+#include "ss_dispatch.h"
+#include "ss_fwd_kernel.cuh"
+
+namespace ssk {
+
+namespace {
+
+constexpr int kW = 8;         // warps per CTA
+constexpr int kT = 16;        // steps per segment
+constexpr int kCPC = 2 * kW;  // channels per CTA
+constexpr unsigned kFull = 0xffffffffu;
+
+// afterwards v[0] of lane j holds the sum over the half-warp's 16 lanes of their v[j]
+__device__ __forceinline__ void reduce_scatter16(float (&v)[kT], int lane) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < o; ++k) {
+      const float send = upper ? v[k] : v[k + o];
+      const float keep = upper ? v[k + o] : v[k];
+      v[k] = keep + __shfl_xor_sync(kFull, send, o);
+    }
+  }
+}
+
+// kT values of one B/C row starting at step t (zeros past the end)
+template <typename BCT>
+__device__ __forceinline__ void load_row(const BCT *src, int t, int L, float (&v)[kT]) {
+#pragma unroll
+  for (int i = 0; i < kT; ++i) v[i] = t + i < L ? to_f<BCT>(src[t + i]) : 0.f;
+}
+
+template <typename T, typename BCT, bool FIXED, int SPL>
+__global__ void __launch_bounds__(kW * 32) ss_fwd_complex_kernel(const __grid_constant__ CxParams p) {
+  __shared__ __align__(16) float s_ch[kCPC][2][kT];  // dt, dt*u per channel and step
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, j = lane & 15;
+  const int chl = warp * 2 + half;
+  const int N = p.dstate, L = p.seqlen;
+  const int g = blockIdx.x / p.tiles;
+  const int dl = (blockIdx.x - g * p.tiles) * kCPC + chl;
+  const bool active = dl < p.dpg;
+  const int d = g * p.dpg + (active ? dl : 0);
+  const int b = blockIdx.y + gridDim.y * blockIdx.z;
+  if (b >= p.batch) return;  // the last batch slab of a folded grid (whole CTA)
+
+  const T *u_row = static_cast<const T *>(p.u) + b * p.su[0] + d * p.su[1];
+  const T *dl_row = static_cast<const T *>(p.delta) + b * p.sd[0] + d * p.sd[1];
+  const T *z_row = p.has_z ? static_cast<const T *>(p.z) + b * p.sz[0] + d * p.sz[1] : nullptr;
+  T *o_row = static_cast<T *>(p.out) + b * p.so[0] + d * p.so[1];
+  const float bias = p.bias ? p.bias[d] : 0.f;
+  const float Dd = p.D ? p.D[d] : 0.f;
+  const BCT *B_base = FIXED ? static_cast<const BCT *>(p.B) + d * p.sB[0]
+                            : static_cast<const BCT *>(p.B) + b * p.sB[0] + g * p.sB[1];
+  const BCT *C_base = FIXED ? static_cast<const BCT *>(p.C) + d * p.sC[0]
+                            : static_cast<const BCT *>(p.C) + b * p.sC[0] + g * p.sC[1];
+
+  float Ar2[SPL], Ai[SPL], xr[SPL], xi[SPL], Bf[SPL], Cf[SPL];
+#pragma unroll
+  for (int s = 0; s < SPL; ++s) {
+    const int n = 16 * s + j;
+    const bool ok = n < N;
+    Ar2[s] = ok ? p.A[2 * (d * p.sA + n)] * kLog2e : 0.f;
+    Ai[s] = ok ? p.A[2 * (d * p.sA + n) + 1] : 0.f;
+    const long long ii = 2 * (b * p.si[0] + d * p.si[1] + n);
+    xr[s] = (ok && active && p.init) ? p.init[ii] : 0.f;
+    xi[s] = (ok && active && p.init) ? p.init[ii + 1] : 0.f;
+    Bf[s] = (FIXED && ok) ? to_f<BCT>(B_base[n]) : 0.f;
+    Cf[s] = (FIXED && ok) ? to_f<BCT>(C_base[n]) : 0.f;
+  }
+  float *const ch = &s_ch[chl][0][0];
+
+  for (int t0 = 0; t0 < L; t0 += kT) {
+    // lane j prepares step t0 + j
+    const bool vj = active && t0 + j < L;
+    float uj = 0.f, dtj = 0.f, gate = 1.f;
+    if (vj) {
+      uj = to_f<T>(u_row[t0 + j]);
+      const float v = to_f<T>(dl_row[t0 + j]) + bias;
+      dtj = p.softplus ? softplus_f(v) : v;
+      if (p.has_z) gate = silu_f(to_f<T>(z_row[t0 + j]));
+    }
+    ch[j] = dtj;
+    ch[kT + j] = dtj * uj;
+    __syncwarp();
+
+    float yv[kT];
+#pragma unroll
+    for (int i = 0; i < kT; ++i) yv[i] = 0.f;
+#pragma unroll
+    for (int s = 0; s < SPL; ++s) {
+      const int n = 16 * s + j;
+      float Bv[kT], Cv[kT];
+      if constexpr (FIXED) {
+#pragma unroll
+        for (int i = 0; i < kT; ++i) {
+          Bv[i] = Bf[s];
+          Cv[i] = Cf[s];
+        }
+      } else {
+        const bool ok = active && n < N;
+        load_row<BCT>(B_base + n * p.sB[2], t0, ok ? L : 0, Bv);
+        load_row<BCT>(C_base + n * p.sC[2], t0, ok ? L : 0, Cv);
+      }
+      float r = xr[s], im = xi[s];
+#pragma unroll
+      for (int i = 0; i < kT; i += 4) {
+        const float4 dt4 = *reinterpret_cast<const float4 *>(ch + i);
+        const float4 du4 = *reinterpret_cast<const float4 *>(ch + kT + i);
+        const float dtv[4] = {dt4.x, dt4.y, dt4.z, dt4.w}, duv[4] = {du4.x, du4.y, du4.z, du4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float e = ex2(dtv[q] * Ar2[s]);
+          float sn, cs;
+          sincosf(dtv[q] * Ai[s], &sn, &cs);
+          const float ar = e * cs, ai = e * sn;
+          const float nr = fmaf(ar, r, fmaf(-ai, im, duv[q] * Bv[i + q]));
+          im = fmaf(ar, im, ai * r);
+          r = nr;
+          yv[i + q] = fmaf(Cv[i + q], r, yv[i + q]);
+        }
+      }
+      xr[s] = r;
+      xi[s] = im;
+    }
+    // y of step t0 + j in lane j
+    reduce_scatter16(yv, lane);
+    if (vj) o_row[t0 + j] = from_f<T>(fmaf(Dd, uj, yv[0]) * gate);
+    __syncwarp();  // the channel's step values are read before the next segment overwrites them
+  }
+
+  if (!active || !p.last) return;
+#pragma unroll
+  for (int s = 0; s < SPL; ++s) {
+    const int n = 16 * s + j;
+    if (n >= N) continue;
+    const long long li = 2 * (b * p.sl[0] + d * p.sl[1] + n);
+    p.last[li] = xr[s];
+    p.last[li + 1] = xi[s];
+  }
+}
+
+template <typename T, typename BCT, bool FIXED>
+const void *by_states(int spl) {
+  switch (spl) {
+    case 1: return (const void *)&ss_fwd_complex_kernel<T, BCT, FIXED, 1>;
+    case 2: return (const void *)&ss_fwd_complex_kernel<T, BCT, FIXED, 2>;
+    case 3: return (const void *)&ss_fwd_complex_kernel<T, BCT, FIXED, 3>;
+    default: return (const void *)&ss_fwd_complex_kernel<T, BCT, FIXED, 4>;
+  }
+}
+
+template <typename T, typename BCT>
+const void *pick(bool fixed, int spl) {
+  if constexpr (sizeof(BCT) == 4) {
+    if (fixed) return by_states<T, float, true>(spl);
+  }
+  return by_states<T, BCT, false>(spl);
+}
+
+}  // namespace
+
+int cx_segment_steps() { return kT; }
+int cx_channels_per_cta() { return kCPC; }
+int cx_threads() { return kW * 32; }
+
+const void *cx_kernel(int in_dtype, bool bc_f32, bool fixed, int dstate) {
+  const int spl = (dstate + 15) / 16;
+  switch (in_dtype) {
+    case 0: return pick<float, float>(fixed, spl);
+    case 1: return bc_f32 ? pick<__half, float>(fixed, spl) : pick<__half, __half>(false, spl);
+    default: return bc_f32 ? pick<__nv_bfloat16, float>(fixed, spl) : pick<__nv_bfloat16, __nv_bfloat16>(false, spl);
+  }
+}
+
+}  // namespace ssk

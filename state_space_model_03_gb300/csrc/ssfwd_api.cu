@@ -1022,6 +1022,145 @@ int launch_bwd(const ss_bwd_params *p, cudaStream_t stream) {
              : SS_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Complex-A forward (ss_fwd_complex)
+// ---------------------------------------------------------------------------
+int validate_cx(const ss_fwd_complex_params *p) {
+  if (!p) return SS_ERR_NULL;
+  if (p->abi_version != SS_ABI_VERSION) return SS_ERR_VERSION;
+  if (p->in_dtype < SS_F32 || p->in_dtype > SS_BF16) return SS_ERR_DTYPE;
+  if (p->bc_dtype < SS_F32 || p->bc_dtype > SS_BF16) return SS_ERR_DTYPE;
+  if (p->bc_mode != SS_BC_FIXED && p->bc_mode != SS_BC_VARIABLE) return SS_ERR_SHAPE;
+  const bool fixed = p->bc_mode == SS_BC_FIXED;
+  if (fixed && p->bc_dtype != SS_F32) return SS_ERR_DTYPE;
+  if (!fixed && p->bc_dtype != p->in_dtype && p->bc_dtype != SS_F32) return SS_ERR_DTYPE;
+  if (p->batch < 0 || p->dim < 0 || p->seqlen < 0) return SS_ERR_SHAPE;
+  if (p->dstate < 1) return SS_ERR_SHAPE;
+  if (p->dstate > 64) return SS_ERR_UNSUPPORTED;
+  if (!fixed && (p->ngroups < 1 || (p->dim > 0 && p->dim % p->ngroups != 0))) return SS_ERR_SHAPE;
+  if (p->batch > (int64_t(1) << 24) || p->dim > (1 << 30) || p->seqlen > (int64_t(1) << 31) - 1024)
+    return SS_ERR_UNSUPPORTED;
+  if (p->batch * p->dim == 0) return SS_OK;
+  const int64_t szl[3] = {p->batch, p->dim, p->dstate};
+  Range last{0, 0}, init{0, 0};
+  if (p->last_state) {
+    if (p->last_state_stride[2] != 1 || p->last_state_stride[0] < 0 || p->last_state_stride[1] < 0)
+      return SS_ERR_STRIDE;
+    if (!aligned(p->last_state, 8)) return SS_ERR_ALIGN;
+    last = span(p->last_state, 8, szl, p->last_state_stride, 3);
+  }
+  if (p->initial_state) {
+    if (p->initial_state_stride[2] != 1 || p->initial_state_stride[0] < 0 || p->initial_state_stride[1] < 0)
+      return SS_ERR_STRIDE;
+    if (!aligned(p->initial_state, 8)) return SS_ERR_ALIGN;
+    init = span(p->initial_state, 8, szl, p->initial_state_stride, 3);
+    const bool same = p->last_state == p->initial_state && p->last_state_stride[0] == p->initial_state_stride[0] &&
+                      p->last_state_stride[1] == p->initial_state_stride[1];
+    if (!same && overlap(init, last)) return SS_ERR_ALIAS;
+  }
+  if (p->seqlen == 0) return SS_OK;
+  if (!p->u || !p->delta || !p->A || !p->B || !p->C || !p->out) return SS_ERR_NULL;
+  const int64_t *st3[4] = {p->u_stride, p->delta_stride, p->z ? p->z_stride : p->u_stride, p->out_stride};
+  for (auto st : st3)
+    if (st[2] != 1 || st[0] < 0 || st[1] < 0) return SS_ERR_STRIDE;
+  if (p->A_stride[1] != 1 || p->A_stride[0] < 0) return SS_ERR_STRIDE;
+  if (fixed) {
+    if (p->B_stride[1] != 1 || p->C_stride[1] != 1 || p->B_stride[0] < 0 || p->C_stride[0] < 0) return SS_ERR_STRIDE;
+  } else {
+    for (int i = 0; i < 4; ++i)
+      if (p->B_stride[i] < 0 || p->C_stride[i] < 0) return SS_ERR_STRIDE;
+    if (p->B_stride[3] != 1 || p->C_stride[3] != 1) return SS_ERR_STRIDE;
+  }
+  const int es = elem_size(p->in_dtype), bs = elem_size(p->bc_dtype);
+  if (!aligned(p->u, es) || !aligned(p->delta, es) || !aligned(p->out, es) || (p->z && !aligned(p->z, es)))
+    return SS_ERR_ALIGN;
+  if (!aligned(p->B, bs) || !aligned(p->C, bs) || !aligned(p->A, 8)) return SS_ERR_ALIGN;
+  if ((p->D && !aligned(p->D, 4)) || (p->delta_bias && !aligned(p->delta_bias, 4))) return SS_ERR_ALIGN;
+  const int64_t sz3[3] = {p->batch, p->dim, p->seqlen};
+  Range out = span(p->out, es, sz3, p->out_stride, 3);
+  Range ins[9];
+  int ni = 0;
+  ins[ni++] = span(p->u, es, sz3, p->u_stride, 3);
+  ins[ni++] = span(p->delta, es, sz3, p->delta_stride, 3);
+  if (p->z) ins[ni++] = span(p->z, es, sz3, p->z_stride, 3);
+  const int64_t sza[2] = {p->dim, p->dstate};
+  ins[ni++] = span(p->A, 8, sza, p->A_stride, 2);
+  if (fixed) {
+    ins[ni++] = span(p->B, 4, sza, p->B_stride, 2);
+    ins[ni++] = span(p->C, 4, sza, p->C_stride, 2);
+  } else {
+    const int64_t szb[4] = {p->batch, p->ngroups, p->dstate, p->seqlen};
+    ins[ni++] = span(p->B, bs, szb, p->B_stride, 4);
+    ins[ni++] = span(p->C, bs, szb, p->C_stride, 4);
+  }
+  const int64_t one[1] = {p->dim}, unit[1] = {1};
+  if (p->D) ins[ni++] = span(p->D, 4, one, unit, 1);
+  if (p->delta_bias) ins[ni++] = span(p->delta_bias, 4, one, unit, 1);
+  for (int i = 0; i < ni; ++i)
+    if (overlap(out, ins[i]) || overlap(last, ins[i])) return SS_ERR_ALIAS;
+  if (overlap(out, last) || overlap(out, init)) return SS_ERR_ALIAS;
+  return SS_OK;
+}
+
+__global__ void complex_empty_state(float *last, const float *init, long long s0, long long s1, long long s2i0,
+                                    long long s2i1, int batch, int dim, int dstate) {
+  const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (i >= (long long)batch * dim * dstate) return;
+  const int n = i % dstate, d = (i / dstate) % dim, b = i / ((long long)dstate * dim);
+  const long long o = 2 * (b * s0 + d * s1 + n);
+  const long long q = 2 * (b * s2i0 + d * s2i1 + n);
+  last[o] = init ? init[q] : 0.f;
+  last[o + 1] = init ? init[q + 1] : 0.f;
+}
+
+int launch_cx(const ss_fwd_complex_params *p, cudaStream_t stream) {
+  if (p->batch * p->dim == 0) return SS_OK;
+  if (fault_injected("launch")) return SS_ERR_CUDA;
+  if (p->seqlen == 0) {
+    if (!p->last_state || p->last_state == p->initial_state) return SS_OK;
+    const long long n = p->batch * p->dim * p->dstate;
+    complex_empty_state<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+        p->last_state, p->initial_state, p->last_state_stride[0], p->last_state_stride[1],
+        p->initial_state ? p->initial_state_stride[0] : 0, p->initial_state ? p->initial_state_stride[1] : 0,
+        static_cast<int>(p->batch), static_cast<int>(p->dim), static_cast<int>(p->dstate));
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  }
+  const bool fixed = p->bc_mode == SS_BC_FIXED;
+  ssk::CxParams k{};
+  k.batch = static_cast<int>(p->batch);
+  k.dim = static_cast<int>(p->dim);
+  k.dstate = static_cast<int>(p->dstate);
+  k.ngroups = fixed ? 1 : static_cast<int>(p->ngroups);
+  k.dpg = k.dim / k.ngroups;
+  const int cpc = ssk::cx_channels_per_cta();
+  k.tiles = (k.dpg + cpc - 1) / cpc;
+  k.seqlen = static_cast<int>(p->seqlen);
+  k.nseg = static_cast<int>((p->seqlen + ssk::cx_segment_steps() - 1) / ssk::cx_segment_steps());
+  k.has_z = p->z != nullptr;
+  k.softplus = p->delta_softplus != 0;
+  k.u = p->u; k.delta = p->delta; k.z = p->z; k.B = p->B; k.C = p->C;
+  k.A = p->A; k.D = p->D; k.bias = p->delta_bias; k.init = p->initial_state;
+  k.out = p->out; k.last = p->last_state;
+  for (int i = 0; i < 2; ++i) {
+    k.su[i] = p->u_stride[i]; k.sd[i] = p->delta_stride[i]; k.so[i] = p->out_stride[i];
+    k.sz[i] = p->z ? p->z_stride[i] : 0;
+    k.si[i] = p->initial_state ? p->initial_state_stride[i] : 0;
+    k.sl[i] = p->last_state ? p->last_state_stride[i] : 0;
+  }
+  for (int i = 0; i < 3; ++i) { k.sB[i] = p->B_stride[i]; k.sC[i] = p->C_stride[i]; }
+  k.sA = p->A_stride[0];
+  const bool bc_f32 = fixed || p->bc_dtype == SS_F32;
+  const void *fn = ssk::cx_kernel(p->in_dtype, bc_f32, fixed, k.dstate);
+  const int64_t gx = static_cast<int64_t>(k.ngroups) * k.tiles;
+  const int64_t gy = std::min<int64_t>(p->batch, 65535), gz = (p->batch + gy - 1) / gy;
+  if (gx > 0x7fffffff || gz > 65535) return SS_ERR_UNSUPPORTED;
+  void *args[1] = {&k};
+  return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(gz)),
+                          dim3(ssk::cx_threads()), args, 0, stream) == cudaSuccess
+             ? SS_OK
+             : SS_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1163,6 +1302,14 @@ int ss_bwd(const ss_bwd_params *p, void *stream) {
   const int st = validate_bwd(p);
   if (st != SS_OK) return st;
   return launch_bwd(p, static_cast<cudaStream_t>(stream));
+}
+
+int ss_fwd_complex_validate(const ss_fwd_complex_params *p) { return validate_cx(p); }
+
+int ss_fwd_complex(const ss_fwd_complex_params *p, void *stream) {
+  const int st = validate_cx(p);
+  if (st != SS_OK) return st;
+  return launch_cx(p, static_cast<cudaStream_t>(stream));
 }
 
 int ss_device_error(int32_t *out_word, int clear) {

@@ -33,7 +33,8 @@ def test_exports_every_declared_symbol(lib):
                           "ss_fwd_host", "ss_device_error", "ss_fwd_workspace_size", "ss_fwd_noalloc",
                           "ss_state_update_validate", "ss_state_update", "ss_causal_conv1d_validate",
                           "ss_causal_conv1d", "ss_causal_conv1d_update_validate", "ss_causal_conv1d_update",
-                          "ss_bwd_validate", "ss_bwd_workspace_size", "ss_bwd"}
+                          "ss_bwd_validate", "ss_bwd_workspace_size", "ss_bwd",
+                          "ss_fwd_complex_validate", "ss_fwd_complex"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -155,11 +156,11 @@ def test_python_wrapper_refuses_cpu_tensors():
         api.selective_scan_fn(u, u, torch.zeros(4, 4), torch.zeros(1, 4, 8), torch.zeros(1, 4, 8))
 
 
-def test_complex_A_not_implemented():
+def test_complex_A_normalised_to_complex64():
     import torch
     u = torch.zeros(1, 4, 8)
-    with pytest.raises(NotImplementedError):
-        api.normalise(u, u, torch.zeros(4, 4, dtype=torch.complex64), torch.zeros(1, 4, 8), torch.zeros(1, 4, 8))
+    A = api.normalise(u, u, torch.zeros(4, 4, dtype=torch.complex128), torch.zeros(1, 4, 8), torch.zeros(1, 4, 8))[2]
+    assert A.dtype == torch.complex64
 
 
 def test_initial_state_rules(lib):
@@ -402,3 +403,43 @@ def test_bwd_optional_outputs_and_empty(lib):
     q = _good_bwd(with_ws=False)
     q.batch = 0
     assert lib.ss_bwd_validate(ctypes.byref(q)) == 0
+
+
+# ---------------------------------------------------------------------------
+# complex-A forward (ss_fwd_complex): validation only
+# ---------------------------------------------------------------------------
+def _good_cx():
+    f = _good()
+    p = api.SSFwdComplexParams()
+    for k in ("abi_version", "in_dtype", "bc_dtype", "bc_mode", "delta_softplus", "batch", "dim", "seqlen",
+              "dstate", "ngroups", "u", "delta", "z", "B", "C", "D", "delta_bias", "out"):
+        setattr(p, k, getattr(f, k))
+    for k in ("u_stride", "delta_stride", "z_stride", "out_stride", "B_stride", "C_stride", "A_stride"):
+        getattr(p, k)[:] = list(getattr(f, k))
+    cur = 1 << 44  # complex A and states: a region of their own
+    p.A = cur
+    p.last_state = cur + 64 * 16 * 8
+    p.last_state_stride[:] = [64 * 16, 16, 1]
+    p.initial_state_stride[:] = [0, 0, 1]
+    return p
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda p: None, 0),
+    (lambda p: setattr(p, "abi_version", 2), 10),
+    (lambda p: setattr(p, "A", None), 1),
+    (lambda p: setattr(p, "A", p.A + 4), 5),                  # complex64 needs 8-byte alignment
+    (lambda p: setattr(p, "last_state", p.last_state + 4), 5),
+    (lambda p: p.A_stride.__setitem__(1, 2), 4),
+    (lambda p: setattr(p, "dstate", 65), 7),
+    (lambda p: setattr(p, "out", p.u), 6),
+    (lambda p: setattr(p, "last_state", p.A + 8), 6),         # overlaps A (16-byte elements span)
+    (lambda p: (setattr(p, "initial_state", p.last_state), p.initial_state_stride.__setitem__(0, 64 * 16),
+                p.initial_state_stride.__setitem__(1, 16)), 0),  # in place: allowed
+])
+def test_complex_validation(lib, mutate, status):
+    p = _good_cx()
+    mutate(p)
+    assert lib.ss_fwd_complex_validate(ctypes.byref(p)) == status
+    if status:
+        assert lib.ss_fwd_complex(ctypes.byref(p), None) == status
