@@ -90,6 +90,7 @@ struct CxParams {
   int batch, dim, dstate, ngroups, dpg, tiles;  // tiles: CTAs per group along the channels
   int seqlen, nseg;                             // steps; segments of cx_segment_steps() steps
   int has_z, softplus;
+  int bcvec;                         // 16-byte B/C row accesses allowed (variable B/C)
   const void *u, *delta, *z, *B, *C;
   const float *A, *D, *bias, *init;  // A, init: complex64 interleaved
   void *out;

@@ -9,8 +9,10 @@
 // more than 16 states a lane loops over n = j, j + 16, ...). The row is walked
 // in segments of kT steps: lane j prepares step t0 + j of the channel (dt,
 // dt u, the gate) into shared memory, every lane walks the segment for its
-// state(s) accumulating its part of y per step, and a reduce-scatter over the
-// 16 lanes leaves lane j with step t0 + j's sum, which it gates and stores.
+// state(s) accumulating its part of y per step, and the 16 lanes' terms pass
+// through shared memory so that lane j sums step t0 + j's, gates and stores it.
+// The lane's global inputs of the next segment are fetched before the current
+// one is walked.
 // There is no cross-warp communication, so warps run independently.
 #include "ss_dispatch.h"
 #include "ss_fwd_kernel.cuh"
@@ -22,32 +24,77 @@ namespace {
 constexpr int kW = 8;         // warps per CTA
 constexpr int kT = 16;        // steps per segment
 constexpr int kCPC = 2 * kW;  // channels per CTA
-constexpr unsigned kFull = 0xffffffffu;
 
-// afterwards v[0] of lane j holds the sum over the half-warp's 16 lanes of their v[j]
-__device__ __forceinline__ void reduce_scatter16(float (&v)[kT], int lane) {
+constexpr int kYRow = kT + 4;  // padded row of the per-state y terms (conflict-free 16-byte stores)
+
+// sin and cos of th: th = k pi/2 + r (Cody-Waite reduction with fused
+// multiply-adds against a three-part split of pi/2), |r| <= pi/4, then the
+// Taylor series of sin r to r^9 and of cos r to r^8 (truncation below 4e-8)
+// and the quadrant k mod 4. Accurate to a few fp32 ulps for |th| up to ~1e5.
+__device__ __forceinline__ void sincos_rr(float th, float &sn, float &cs) {
+  const float k = rintf(th * 0.636619772367581343f);  // 2 / pi
+  float r = fmaf(-k, 1.5707963705062866f, th);
+  r = fmaf(-k, -4.371138828673793e-08f, r);
+  r = fmaf(-k, -1.7763568394002505e-15f, r);
+  const float r2 = r * r;
+  const float s = r * fmaf(r2, fmaf(r2, fmaf(r2, fmaf(r2, 2.7557319223985893e-06f, -1.984126984126984e-04f),
+                                             8.333333333333333e-03f), -1.6666666666666666e-01f), 1.f);
+  const float c = fmaf(r2, fmaf(r2, fmaf(r2, fmaf(r2, 2.48015873015873e-05f, -1.388888888888889e-03f),
+                                         4.1666666666666664e-02f), -0.5f), 1.f);
+  const int q = static_cast<int>(k) & 3;  // two's complement: k = -1 gives quadrant 3
+  const float s1 = (q & 1) ? c : s, c1 = (q & 1) ? s : c;
+  sn = (q & 2) ? -s1 : s1;
+  cs = ((q + 1) & 2) ? -c1 : c1;
+}
+
+// kT values of one B/C row starting at step t: 16-byte loads when vec (the
+// row is aligned and the segment complete), else element by element with
+// zeros past the end.
+template <typename BCT>
+struct Row {
+  static constexpr int kWords = kT * (int)sizeof(BCT) / 16;  // 16-byte words per segment
+  uint4 w[kWords];
+};
+template <typename BCT>
+__device__ __forceinline__ void fetch_row(const BCT *src, int t, int L, bool vec, Row<BCT> &r) {
+  if (vec && t + kT <= L) {
 #pragma unroll
-  for (int o = 8; o > 0; o >>= 1) {
-    const bool upper = (lane & o) != 0;
+    for (int q = 0; q < Row<BCT>::kWords; ++q) r.w[q] = reinterpret_cast<const uint4 *>(src + t)[q];
+  } else {
+    BCT tmp[kT];
 #pragma unroll
-    for (int k = 0; k < o; ++k) {
-      const float send = upper ? v[k] : v[k + o];
-      const float keep = upper ? v[k + o] : v[k];
-      v[k] = keep + __shfl_xor_sync(kFull, send, o);
+    for (int i = 0; i < kT; ++i) tmp[i] = t + i < L ? src[t + i] : from_f<BCT>(0.f);
+    memcpy(&r.w[0], tmp, sizeof(tmp));
+  }
+}
+template <typename BCT>
+__device__ __forceinline__ void unpack_row(const Row<BCT> &r, float (&v)[kT]) {
+  if constexpr (sizeof(BCT) == 4) {
+#pragma unroll
+    for (int q = 0; q < Row<BCT>::kWords; ++q) {
+      v[4 * q] = __uint_as_float(r.w[q].x);
+      v[4 * q + 1] = __uint_as_float(r.w[q].y);
+      v[4 * q + 2] = __uint_as_float(r.w[q].z);
+      v[4 * q + 3] = __uint_as_float(r.w[q].w);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < Row<BCT>::kWords; ++q) {
+      const uint32_t wd[4] = {r.w[q].x, r.w[q].y, r.w[q].z, r.w[q].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = unpack2<BCT>(wd[k]);
+        v[8 * q + 2 * k] = f.x;
+        v[8 * q + 2 * k + 1] = f.y;
+      }
     }
   }
 }
 
-// kT values of one B/C row starting at step t (zeros past the end)
-template <typename BCT>
-__device__ __forceinline__ void load_row(const BCT *src, int t, int L, float (&v)[kT]) {
-#pragma unroll
-  for (int i = 0; i < kT; ++i) v[i] = t + i < L ? to_f<BCT>(src[t + i]) : 0.f;
-}
-
 template <typename T, typename BCT, bool FIXED, int SPL>
-__global__ void __launch_bounds__(kW * 32) ss_fwd_complex_kernel(const __grid_constant__ CxParams p) {
-  __shared__ __align__(16) float s_ch[kCPC][2][kT];  // dt, dt*u per channel and step
+__global__ void __launch_bounds__(kW * 32, 2) ss_fwd_complex_kernel(const __grid_constant__ CxParams p) {
+  __shared__ __align__(16) float s_ch[kCPC][2][kT];        // dt, dt*u per channel and step
+  __shared__ __align__(16) float s_y[kCPC][16][kYRow];     // per-state y terms of the segment
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, j = lane & 15;
@@ -85,16 +132,36 @@ __global__ void __launch_bounds__(kW * 32) ss_fwd_complex_kernel(const __grid_co
     Cf[s] = (FIXED && ok) ? to_f<BCT>(C_base[n]) : 0.f;
   }
   float *const ch = &s_ch[chl][0][0];
+  float *const sy = &s_y[chl][0][0];
+
+  // the lane's inputs of a segment, fetched one segment ahead (one state group:
+  // B/C rows too)
+  const T zero_t = from_f<T>(0.f);
+  T raw[3], nraw[3];
+  Row<BCT> rb, rc, nrb, nrc;
+  auto fetch = [&](int t0, T (&r)[3], Row<BCT> &fb, Row<BCT> &fc) {
+    const bool vj = active && t0 + j < L;
+    r[0] = vj ? u_row[t0 + j] : zero_t;
+    r[1] = vj ? dl_row[t0 + j] : zero_t;
+    r[2] = (vj && p.has_z) ? z_row[t0 + j] : zero_t;
+    if constexpr (!FIXED && SPL == 1) {
+      const bool ok = active && j < N;
+      fetch_row<BCT>(B_base + j * p.sB[2], t0, ok ? L : 0, p.bcvec != 0, fb);
+      fetch_row<BCT>(C_base + j * p.sC[2], t0, ok ? L : 0, p.bcvec != 0, fc);
+    }
+  };
+  fetch(0, raw, rb, rc);
 
   for (int t0 = 0; t0 < L; t0 += kT) {
+    if (t0 + kT < L) fetch(t0 + kT, nraw, nrb, nrc);
     // lane j prepares step t0 + j
     const bool vj = active && t0 + j < L;
     float uj = 0.f, dtj = 0.f, gate = 1.f;
     if (vj) {
-      uj = to_f<T>(u_row[t0 + j]);
-      const float v = to_f<T>(dl_row[t0 + j]) + bias;
+      uj = to_f<T>(raw[0]);
+      const float v = to_f<T>(raw[1]) + bias;
       dtj = p.softplus ? softplus_f(v) : v;
-      if (p.has_z) gate = silu_f(to_f<T>(z_row[t0 + j]));
+      if (p.has_z) gate = silu_f(to_f<T>(raw[2]));
     }
     ch[j] = dtj;
     ch[kT + j] = dtj * uj;
@@ -113,10 +180,16 @@ __global__ void __launch_bounds__(kW * 32) ss_fwd_complex_kernel(const __grid_co
           Bv[i] = Bf[s];
           Cv[i] = Cf[s];
         }
+      } else if constexpr (SPL == 1) {
+        unpack_row<BCT>(rb, Bv);
+        unpack_row<BCT>(rc, Cv);
       } else {
         const bool ok = active && n < N;
-        load_row<BCT>(B_base + n * p.sB[2], t0, ok ? L : 0, Bv);
-        load_row<BCT>(C_base + n * p.sC[2], t0, ok ? L : 0, Cv);
+        Row<BCT> tb, tc;
+        fetch_row<BCT>(B_base + n * p.sB[2], t0, ok ? L : 0, p.bcvec != 0, tb);
+        fetch_row<BCT>(C_base + n * p.sC[2], t0, ok ? L : 0, p.bcvec != 0, tc);
+        unpack_row<BCT>(tb, Bv);
+        unpack_row<BCT>(tc, Cv);
       }
       float r = xr[s], im = xi[s];
 #pragma unroll
@@ -128,7 +201,7 @@ __global__ void __launch_bounds__(kW * 32) ss_fwd_complex_kernel(const __grid_co
         for (int q = 0; q < 4; ++q) {
           const float e = ex2(dtv[q] * Ar2[s]);
           float sn, cs;
-          sincosf(dtv[q] * Ai[s], &sn, &cs);
+          sincos_rr(dtv[q] * Ai[s], sn, cs);
           const float ar = e * cs, ai = e * sn;
           const float nr = fmaf(ar, r, fmaf(-ai, im, duv[q] * Bv[i + q]));
           im = fmaf(ar, im, ai * r);
@@ -139,10 +212,20 @@ __global__ void __launch_bounds__(kW * 32) ss_fwd_complex_kernel(const __grid_co
       xr[s] = r;
       xi[s] = im;
     }
-    // y of step t0 + j in lane j
-    reduce_scatter16(yv, lane);
-    if (vj) o_row[t0 + j] = from_f<T>(fmaf(Dd, uj, yv[0]) * gate);
-    __syncwarp();  // the channel's step values are read before the next segment overwrites them
+    // y of step t0 + j = sum over the channel's 16 lanes of their term j
+#pragma unroll
+    for (int i = 0; i < kT; i += 4)
+      *reinterpret_cast<float4 *>(sy + j * kYRow + i) = make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
+    __syncwarp();
+    float y = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) y += sy[k * kYRow + j];
+    if (vj) o_row[t0 + j] = from_f<T>(fmaf(Dd, uj, y) * gate);
+    __syncwarp();  // the channel's step values and terms are read before the next segment overwrites them
+#pragma unroll
+    for (int q = 0; q < 3; ++q) raw[q] = nraw[q];
+    rb = nrb;
+    rc = nrc;
   }
 
   if (!active || !p.last) return;

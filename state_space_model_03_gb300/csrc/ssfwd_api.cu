@@ -1149,6 +1149,11 @@ int launch_cx(const ss_fwd_complex_params *p, cudaStream_t stream) {
   }
   for (int i = 0; i < 3; ++i) { k.sB[i] = p->B_stride[i]; k.sC[i] = p->C_stride[i]; }
   k.sA = p->A_stride[0];
+  {
+    const int bs = elem_size(p->bc_dtype);
+    k.bcvec = !fixed && aligned(p->B, 16) && aligned(p->C, 16);
+    for (int i = 0; i < 3 && k.bcvec; ++i) k.bcvec = (p->B_stride[i] * bs) % 16 == 0 && (p->C_stride[i] * bs) % 16 == 0;
+  }
   const bool bc_f32 = fixed || p->bc_dtype == SS_F32;
   const void *fn = ssk::cx_kernel(p->in_dtype, bc_f32, fixed, k.dstate);
   const int64_t gx = static_cast<int64_t>(k.ngroups) * k.tiles;

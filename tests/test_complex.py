@@ -48,6 +48,8 @@ CASES = [
     (W("cx_fp32_plain", 1, 8, 50, 4, dtype="fp32", has_z=False, D_mode="none", has_bias=False,
        delta_softplus=False, delta_std=0.1, seed=105), False),
 ]
+# large imaginary parts: rotation angles dt Im A of tens of radians per step
+FAST_ROTATION = W("cx_fp32_fast_rotation", 2, 16, 200, 16, dtype="fp32", seed=109)
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c[0].name)
@@ -71,6 +73,27 @@ def test_complex_matches_oracle(case):
                                                              return_last_state=True, initial_state=x0)
     assert _rel(_np(out), ref_out) <= TOL[w.dtype]
     assert _rel(_np(last), ref_last) <= (1e-5 if w.dtype == "fp32" else 1e-3)
+
+
+def test_fast_rotations():
+    """|Im A| up to 300: per-step angles dt Im A of tens of radians. The angle
+    is formed in fp32, so its rounding (relative 2^-24) is a phase error that
+    grows with |angle|; the bound is the fp32 one scaled by 1 + max|angle| / 4
+    (equal to 1e-5 up to the angles of ordinary initialisations)."""
+    w = FAST_ROTATION
+    x = _inputs(w, w.seed, im=300.0)
+    dev = {k: (None if x[k] is None else x[k].cuda()) for k in NAMES}
+    out, last = api.selective_scan_fn(**dev, delta_softplus=True, return_last_state=True)
+    torch.cuda.synchronize()
+    ref_out, ref_last = complex_a.selective_scan_complex_ref(**{k: x[k] for k in NAMES}, delta_softplus=True,
+                                                             return_last_state=True)
+    v = x["delta"].double() + x["delta_bias"].double()[None, :, None]
+    dt_max = float(torch.nn.functional.softplus(v).max())
+    angle = dt_max * float(x["A"].imag.abs().max())
+    tol = 1e-5 * (1.0 + angle / 4.0)
+    assert angle > 20.0  # the case does exercise the range reduction
+    assert _rel(_np(out), ref_out) <= tol
+    assert _rel(_np(last), ref_last) <= tol
 
 
 def test_real_valued_A_equals_the_real_forward():
