@@ -48,6 +48,9 @@
 #ifndef SSK_PPACK
 #define SSK_PPACK 1
 #endif
+#ifndef SSK_EXPA
+#define SSK_EXPA -1  // decay factors one step ahead: 1 always, 0 never, -1 for 16-step sub-chunks
+#endif
 #ifndef SSK_NSLOT
 #define SSK_NSLOT 2
 #endif
@@ -943,6 +946,25 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       float yv[CPL][YB];
 #pragma unroll
       for (int tl = 0; tl < PF; ++tl) load(tl, tl);
+      // Decay factors exp(dt A) of the next step, computed one step ahead (the
+      // prefetch ring already holds its dt) so the exponentials' latency is
+      // off the state update's path. Measured: 2.5% faster with 16-step
+      // sub-chunks, 1% slower with 8-step ones.
+      constexpr bool EXPA = SSK_EXPA < 0 ? S >= 16 : SSK_EXPA != 0;
+      f2 an[CPL][K / 2];
+      auto decay = [&](int rr) {
+        const float dts[2] = {rp[rr].x, rp[rr].z};
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const f2 d2 = pk(dts[i], dts[i]);
+#pragma unroll
+          for (int k = 0; k < K / 2; ++k) {
+            const float2 e = upk(mul2(d2, a2p[i][k]));
+            an[i][k] = pk(ex2(e.x), ex2(e.y));
+          }
+        }
+      };
+      if constexpr (EXPA) decay(0);
 #pragma unroll
       for (int tl = 0; tl < S; ++tl) {
         if (tl + PF < S) load(tl + PF, (tl + PF) % (PF + 1));
@@ -951,6 +973,14 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         f2 dt2[CPL], w2[CPL];
         dt2[0] = pk(rp[r].x, rp[r].x); w2[0] = pk(rp[r].y, rp[r].y);
         if constexpr (CPL == 2) { dt2[1] = pk(rp[r].z, rp[r].z); w2[1] = pk(rp[r].w, rp[r].w); }
+        f2 acur[CPL][K / 2];
+        if constexpr (EXPA) {
+#pragma unroll
+          for (int i = 0; i < CPL; ++i)
+#pragma unroll
+            for (int k = 0; k < K / 2; ++k) acur[i][k] = an[i][k];
+          if (tl + 1 < S) decay((tl + 1) % (PF + 1));
+        }
         // B and C of my K states at this step, as fp32 state pairs
         f2 bp[K / 2], cp[K / 2];
         if constexpr (!FIXED && CF::BCPACK) {
@@ -977,8 +1007,13 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
           f2 y2 = pk(0.f, 0.f);
 #pragma unroll
           for (int k = 0; k < K / 2; ++k) {
-            const float2 e = upk(mul2(dt2[i], a2p[i][k]));
-            const f2 a = pk(ex2(e.x), ex2(e.y));
+            f2 a;
+            if constexpr (EXPA) {
+              a = acur[i][k];
+            } else {
+              const float2 e = upk(mul2(dt2[i], a2p[i][k]));
+              a = pk(ex2(e.x), ex2(e.y));
+            }
             if constexpr (FIXED && GEN) {
               x2[i][k] = fma2(a, x2[i][k], mul2(w2[i], bf2[i][k]));
               y2 = fma2(cf2[i][k], x2[i][k], y2);
