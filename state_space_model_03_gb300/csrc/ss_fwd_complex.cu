@@ -31,16 +31,36 @@ constexpr int kYRow = kT + 4;  // padded row of the per-state y terms (conflict-
 // multiply-adds against a three-part split of pi/2), |r| <= pi/4, then the
 // Taylor series of sin r to r^9 and of cos r to r^8 (truncation below 4e-8)
 // and the quadrant k mod 4. Accurate to a few fp32 ulps for |th| up to ~1e5.
+// FAST (16-bit inputs, whose outputs are rounded to 8 or 11 bits): the reduced
+// sin and cos come from the MUFU approximations instead of the series
+// (absolute error ~1e-6 on |r| <= pi/4).
+__device__ __forceinline__ float sin_approx(float x) {
+  float y;
+  asm("sin.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float cos_approx(float x) {
+  float y;
+  asm("cos.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+template <bool FAST>
 __device__ __forceinline__ void sincos_rr(float th, float &sn, float &cs) {
   const float k = rintf(th * 0.636619772367581343f);  // 2 / pi
   float r = fmaf(-k, 1.5707963705062866f, th);
   r = fmaf(-k, -4.371138828673793e-08f, r);
   r = fmaf(-k, -1.7763568394002505e-15f, r);
-  const float r2 = r * r;
-  const float s = r * fmaf(r2, fmaf(r2, fmaf(r2, fmaf(r2, 2.7557319223985893e-06f, -1.984126984126984e-04f),
-                                             8.333333333333333e-03f), -1.6666666666666666e-01f), 1.f);
-  const float c = fmaf(r2, fmaf(r2, fmaf(r2, fmaf(r2, 2.48015873015873e-05f, -1.388888888888889e-03f),
-                                         4.1666666666666664e-02f), -0.5f), 1.f);
+  float s, c;
+  if constexpr (FAST) {
+    s = sin_approx(r);
+    c = cos_approx(r);
+  } else {
+    const float r2 = r * r;
+    s = r * fmaf(r2, fmaf(r2, fmaf(r2, fmaf(r2, 2.7557319223985893e-06f, -1.984126984126984e-04f),
+                                   8.333333333333333e-03f), -1.6666666666666666e-01f), 1.f);
+    c = fmaf(r2, fmaf(r2, fmaf(r2, fmaf(r2, 2.48015873015873e-05f, -1.388888888888889e-03f),
+                               4.1666666666666664e-02f), -0.5f), 1.f);
+  }
   const int q = static_cast<int>(k) & 3;  // two's complement: k = -1 gives quadrant 3
   const float s1 = (q & 1) ? c : s, c1 = (q & 1) ? s : c;
   sn = (q & 2) ? -s1 : s1;
@@ -201,7 +221,7 @@ __global__ void __launch_bounds__(kW * 32, 2) ss_fwd_complex_kernel(const __grid
         for (int q = 0; q < 4; ++q) {
           const float e = ex2(dtv[q] * Ar2[s]);
           float sn, cs;
-          sincos_rr(dtv[q] * Ai[s], sn, cs);
+          sincos_rr<(sizeof(T) < 4)>(dtv[q] * Ai[s], sn, cs);
           const float ar = e * cs, ai = e * sn;
           const float nr = fmaf(ar, r, fmaf(-ai, im, duv[q] * Bv[i + q]));
           im = fmaf(ar, im, ai * r);
