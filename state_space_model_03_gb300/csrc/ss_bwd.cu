@@ -37,6 +37,8 @@ constexpr int kE = 8;          // steps per lane
 constexpr int kCH = 32 * kE;   // steps per chunk
 static_assert(kE == 8, "the dB/dC reduction splits a lane's run into two quads");
 constexpr int kMaxN = 64;
+constexpr int kLaneRow = kE + 4;   // a lane's padded run of dB/dC terms (conflict-free 16-byte accesses)
+constexpr int kRedRow = 32 * kLaneRow;  // one row's dB (or dC) terms of a chunk
 constexpr unsigned kFull = 0xffffffffu;
 
 template <typename T>
@@ -115,7 +117,7 @@ constexpr int kNB = 16;  // states of variable B/C staged in shared memory at a 
 template <typename BCT, bool FIXED>
 struct BwdSmem {
   static constexpr int kRows = kBwdWarps * kMaxN;                     // per-row, per-state floats
-  static constexpr int kRed = FIXED ? 0 : 2 * 2 * kBwdWarps * kCH;    // dB/dC terms, double-buffered
+  static constexpr int kRed = FIXED ? 0 : 2 * 2 * kBwdWarps * kRedRow;  // dB/dC terms, double-buffered
   static constexpr int kStage = FIXED ? 0 : 2 * kNB * kCH * (int)sizeof(BCT);  // B, C of kNB states
   static constexpr int kSmall = (FIXED ? 7 : 3) * kRows;             // carry, dA, A (+ dB, dC sums, B, C values)
   static constexpr int kBytes = kRed * 4 + kStage + kSmall * 4;
@@ -125,7 +127,7 @@ template <typename T, typename BCT, bool FIXED>
 __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_constant__ BwdParams p) {
   using SM = BwdSmem<BCT, FIXED>;
   extern __shared__ __align__(16) unsigned char smem[];
-  float *sred = reinterpret_cast<float *>(smem);                                  // [2][2][K][kCH]
+  float *sred = reinterpret_cast<float *>(smem);                                  // [2][2][K][32][kLaneRow]
   BCT *sbc = reinterpret_cast<BCT *>(smem + SM::kRed * 4);                          // [2][kNB][kCH]
   float *small = reinterpret_cast<float *>(smem + SM::kRed * 4 + SM::kStage);
   float *scar = small;                      // [K][kMaxN] state / adjoint carry
@@ -334,9 +336,10 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_
         float mu = __shfl_down_sync(kFull, fmaf(Pr, mc, Qr), 1);  // adjoint entering the lane's last step
         if (lane == 31) mu = mc;
         float dA_acc = 0.f, dBs = 0.f, dCs = 0.f;
-        // dB/dC terms, step-major within the row: [i][lane] (conflict-free stores)
-        float *rb = sred + (((it & 1) * 2 + 0) * kBwdWarps + warp) * kCH + lane;
-        float *rc = sred + (((it & 1) * 2 + 1) * kBwdWarps + warp) * kCH + lane;
+        // dB/dC terms: each lane's run of kE steps, padded rows (16-byte stores)
+        float *rb = sred + (((it & 1) * 2 + 0) * kBwdWarps + warp) * kRedRow + lane * kLaneRow;
+        float *rc = sred + (((it & 1) * 2 + 1) * kBwdWarps + warp) * kRedRow + lane * kLaneRow;
+        float tb[4], tc[4];
 #pragma unroll
         for (int i = kE - 1; i >= 0; --i) {
           const float lam = fmaf(dy[i], Cv[i], mu);
@@ -349,8 +352,12 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_
             dBs = fmaf(ld, uu[i], dBs);
             dCs = fmaf(dy[i], h[i], dCs);
           } else {
-            rb[i * 32] = ld * uu[i];
-            rc[i * 32] = dy[i] * h[i];
+            tb[i & 3] = ld * uu[i];
+            tc[i & 3] = dy[i] * h[i];
+            if ((i & 3) == 0) {
+              *reinterpret_cast<float4 *>(rb + i) = make_float4(tb[0], tb[1], tb[2], tb[3]);
+              *reinterpret_cast<float4 *>(rc + i) = make_float4(tc[0], tc[1], tc[2], tc[3]);
+            }
           }
           mu = a[i] * lam;
         }
@@ -373,14 +380,15 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_
             const int which = threadIdx.x / (kCH / 4);
             const int r = threadIdx.x % (kCH / 4);
             const int l = r & 31, i0 = (r >> 5) * 4;
-            const float *src = sred + ((it & 1) * 2 + which) * kBwdWarps * kCH + i0 * 32 + l;
+            const float *src = sred + ((it & 1) * 2 + which) * kBwdWarps * kRedRow + l * kLaneRow + i0;
             float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < kBwdWarps; ++k) {
-              s.x += src[k * kCH];
-              s.y += src[k * kCH + 32];
-              s.z += src[k * kCH + 64];
-              s.w += src[k * kCH + 96];
+              const float4 q = *reinterpret_cast<const float4 *>(src + k * kRedRow);
+              s.x += q.x;
+              s.y += q.y;
+              s.z += q.z;
+              s.w += q.w;
             }
             const int t = c * kCH + l * kE + i0;
             float *dst = (which ? p.dC : p.dB) + (((long long)b * p.ngroups + g) * N + n) * L + t;
