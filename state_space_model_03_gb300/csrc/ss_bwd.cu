@@ -242,12 +242,17 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 2) ss_bwd_kernel(const __grid_
           Q = fmaf(a, Q, dt[i] * uu[i] * Bv[i]);
           P *= a;
         }
-        scan_up(P, Q, lane);
-        const float Pc = __shfl_sync(kFull, P, 31), Qc = __shfl_sync(kFull, Q, 31);
+        // the chunk's map: the lanes' maps composed in order by a tree that ends in lane 0
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float Pn = __shfl_down_sync(kFull, P, o), Qn = __shfl_down_sync(kFull, Q, o);
+          Q = fmaf(Pn, Q, Qn);  // this lane's steps first, then lane + o's
+          P *= Pn;
+        }
         if (lane == 0) {
           const float h = my_car[n];
           if (active) ws_row[(long long)c * N + n] = h;
-          my_car[n] = fmaf(Pc, h, Qc);
+          my_car[n] = fmaf(P, h, Q);
         }
       }
     }
