@@ -64,7 +64,7 @@ namespace ssk {
 // needs a conversion per value in every scan lane, so fp32 hand-off wins.
 // SSK_PF / SSK_YB / SSK_BCPACK override these for experiments.
 template <typename T> struct Tune { static constexpr int PF = 2, YB = 4; static constexpr bool BCPACK = false; };
-template <> struct Tune<__nv_bfloat16> { static constexpr int PF = 1, YB = 16; static constexpr bool BCPACK = true; };
+template <> struct Tune<__nv_bfloat16> { static constexpr int PF = 1, YB = 4; static constexpr bool BCPACK = true; };
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
