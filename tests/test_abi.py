@@ -156,6 +156,47 @@ def test_python_wrapper_refuses_cpu_tensors():
         api.selective_scan_fn(u, u, torch.zeros(4, 4), torch.zeros(1, 4, 8), torch.zeros(1, 4, 8))
 
 
+def test_python_entry_points_refuse_cpu_tensors():
+    """The backward and the complex-A forward have no CPU path either."""
+    import torch
+    u = torch.zeros(1, 4, 8)
+    bc = torch.zeros(1, 4, 8)
+    with pytest.raises(RuntimeError):
+        api.selective_scan_bwd(u, u, u, torch.zeros(4, 4), bc, bc)
+    with pytest.raises(RuntimeError):
+        api.selective_scan_fn(u, u, torch.zeros(4, 4, dtype=torch.complex64), bc, bc)
+
+
+def test_bwd_and_complex_param_fillers_check_operands():
+    """make_bwd_params / make_complex_params read shapes, dtypes and strides
+    only (no device access), and reject mismatched operands."""
+    import torch
+    b, d, l, n = 2, 8, 16, 4
+    u = torch.zeros(b, d, l)
+    A = torch.zeros(d, n)
+    B = torch.zeros(b, 1, n, l)
+    f32 = lambda *s: torch.zeros(*s)
+    args = dict(dout=u, u=u, delta=u, A=A, B=B, C=B, D=None, z=None, delta_bias=None, delta_softplus=True,
+                initial_state=None, du=torch.zeros_like(u), ddelta=torch.zeros_like(u), dz=None, dA=f32(d, n),
+                dB=f32(b, 1, n, l), dC=f32(b, 1, n, l), dD=None, ddelta_bias=None, dinitial_state=None)
+    p = api.make_bwd_params(**args)
+    assert (p.batch, p.dim, p.seqlen, p.dstate, p.ngroups) == (b, d, l, n, 1)
+    assert list(p.dout_stride) == [d * l, l, 1] and p.in_dtype == api.SS_F32
+    with pytest.raises(TypeError):
+        api.make_bwd_params(**dict(args, dout=u.half()))
+    with pytest.raises(TypeError):
+        api.make_bwd_params(**dict(args, du=torch.zeros(b, d, l + 1)))
+    Ac = torch.zeros(d, n, dtype=torch.complex64)
+    out = torch.zeros_like(u)
+    last = torch.zeros(b, d, n, dtype=torch.complex64)
+    q = api.make_complex_params(u, u, Ac, B, B, None, None, None, True, out, last)
+    assert list(q.A_stride) == [n, 1] and list(q.last_state_stride) == [d * n, n, 1]
+    with pytest.raises(TypeError):
+        api.make_complex_params(u, u, A, B, B, None, None, None, True, out, None)          # real A
+    with pytest.raises(TypeError):
+        api.make_complex_params(u, u, Ac, B, B, None, None, None, True, out, last.real)    # real state
+
+
 def test_complex_A_normalised_to_complex64():
     import torch
     u = torch.zeros(1, 4, 8)
