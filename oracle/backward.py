@@ -58,6 +58,12 @@ def _softplus(v):
     return np.maximum(v, 0.0) + np.log1p(np.exp(-np.abs(v)))
 
 
+def _dsilu(z):
+    """d silu(z) / dz = s (1 + z (1 - s)), s = sigmoid(z)."""
+    s = _sigmoid(z)
+    return s * (1.0 + z * (1.0 - s))
+
+
 def _dsoftplus(v):
     """d softplus(v) / dv = sigmoid(v)."""
     return _sigmoid(v)
@@ -133,9 +139,8 @@ def selective_scan_bwd_ref(dout, u, delta, A, B, C, D=None, z=None, delta_bias=N
 
     # output gate
     if z is not None:
-        s = _sigmoid(z)
-        dy = dout * z * s
-        dz = dout * y * (s * (1.0 + z * (1.0 - s)))
+        dy = dout * z * _sigmoid(z)
+        dz = dout * y * _dsilu(z)
     else:
         dy, dz = dout, None
 

@@ -163,12 +163,14 @@ def test_empty_sequence_gives_zero_gradients():
         assert not np.any(got[key]), key
 
 
-@pytest.mark.parametrize("slip", ["adjoint_decays_by_own_step", "no_softplus_derivative", "one_group_sum"])
+@pytest.mark.parametrize("slip", ["adjoint_decays_by_own_step", "no_softplus_derivative", "one_group_sum",
+                                  "silu_derivative_as_sigmoid"])
 def test_planted_slips_fail_finite_differences(slip, monkeypatch):
     """Plausible slips planted in the oracle (the adjoint decaying by its own
     step's factor a_t instead of a_{t+1}, softplus' derivative dropped, the B/C
-    gradient summed over all channels instead of each group's) are caught by
-    the finite-difference pin."""
+    gradient summed over all channels instead of each group's, silu's
+    derivative taken as the sigmoid alone) are caught by the finite-difference
+    pin."""
     p, dout = _problem(41, 2, 4, 6, 3, g=2)
     fd = _finite_differences(p, dout, True)
     got = bwd.selective_scan_bwd_ref(dout, **p, delta_softplus=True)
@@ -177,6 +179,8 @@ def test_planted_slips_fail_finite_differences(slip, monkeypatch):
         monkeypatch.setattr(bwd, "_DECAY_OFFSET", 0)
     elif slip == "no_softplus_derivative":
         monkeypatch.setattr(bwd, "_dsoftplus", lambda v: np.ones_like(v))
+    elif slip == "silu_derivative_as_sigmoid":
+        monkeypatch.setattr(bwd, "_dsilu", bwd._sigmoid)
     else:
         monkeypatch.setattr(bwd, "_group_sum",
                             lambda x, ng: np.repeat(x.sum(axis=1, keepdims=True), ng, axis=1)[:, :ng])
