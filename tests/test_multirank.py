@@ -65,3 +65,21 @@ def test_reference_arm_rank0_line():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+@pytest.mark.parametrize("op,workload", [("bwd", "tiny_fp32"), ("complex", "tiny_fp32"),
+                                         ("state_update", None), ("conv1d", None)])
+def test_reference_arm_of_every_op(op, workload):
+    """Each op's reference arm (the fp64 oracle on the host) prints one
+    well-formed line in its own metric, on the CPU."""
+    import json
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--op", op, "--steps", "1",
+           "--warmup", "3", "--cpu-budget", "1"]
+    if workload:
+        cmd += ["--workload", workload]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "GB/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["higher_is_better"] is True
