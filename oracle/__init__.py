@@ -15,7 +15,13 @@ the thread count).
 Parity pins: every function here is pinned by ``tests/test_oracle.py``
 (brute-force unrolling, closed-form geometric sum, LTI convolution against
 numpy.convolve, B = 0, linearity, causality, last_state, B/C-mode
-equivalences, softplus/silu against torch).
+equivalences, softplus/silu against torch) and, for the start state and the
+one-step update, by ``tests/test_oracle_state.py``.
+
+The other operators have oracles of their own, each pinned by its test file:
+``oracle.backward`` (the gradients; ``tests/test_oracle_bwd.py``),
+``oracle.complex_a`` (complex A; ``tests/test_oracle_complex.py``) and
+``oracle.conv1d`` (the causal conv1d; ``tests/test_oracle_conv.py``).
 """
 from __future__ import annotations
 
