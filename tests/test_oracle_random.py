@@ -6,7 +6,9 @@ combination still fails. Each example is small enough for finite differences.
 - backward: central finite differences of the C forward oracle;
 - forward: a run split in two at a random step, the second part started from
   the first part's last_state, equals the whole run (composition law);
-- complex A: the same composition law, and conj(A) invariance of the output.
+- complex A: the same composition law, and conj(A) invariance of the output;
+- conv1d: numpy.convolve of each row with the reversed taps;
+- decode step: k one-step updates (numpy) equal the C forward over k steps.
 """
 import numpy as np
 import pytest
@@ -140,3 +142,48 @@ def test_complex_split_run_composes_and_is_conjugation_invariant(case, data):
         conj["initial_state"] = np.conj(p["initial_state"])
     out_c = complex_a.selective_scan_complex_ref(**conj, delta_softplus=softplus)
     assert _rel(out_c, full) < 1e-12
+
+
+@settings(max_examples=25, deadline=None)
+@given(st.integers(1, 2), st.integers(1, 4), st.integers(1, 24), st.sampled_from([2, 3, 4]),
+       st.booleans(), st.booleans(), st.integers(0, 2 ** 31 - 1))
+def test_conv1d_against_numpy_convolve(b, d, l, width, with_init, silu, seed):
+    """The conv1d oracle equals numpy.convolve of each row (prefixed by its
+    initial states) with the reversed taps, plus bias, then silu."""
+    from oracle import conv1d
+    rng = np.random.default_rng(seed)
+    x, w, bias = rng.standard_normal((b, d, l)), rng.standard_normal((d, width)), rng.standard_normal(d)
+    init = rng.standard_normal((b, d, width - 1)) if with_init else None
+    out = conv1d.causal_conv1d_ref(x, w, bias, initial_states=init, activation="silu" if silu else None)
+    for bi in range(b):
+        for di in range(d):
+            pre = init[bi, di] if with_init else np.zeros(width - 1)
+            row = np.concatenate([pre, x[bi, di]])
+            ref = np.convolve(row, w[di][::-1])[width - 1:width - 1 + l] + bias[di]
+            if silu:
+                ref = ref / (1.0 + np.exp(-ref))
+            assert _rel(out[bi, di], ref) < 1e-12
+
+
+@settings(max_examples=25, deadline=None)
+@given(problems(max_l=8))
+def test_decode_steps_equal_the_forward(case):
+    """k one-step updates from a start state reproduce the forward oracle's
+    k-step run from it (variable B/C: per-step slices; fixed: the same B/C)."""
+    p, softplus, _ = case
+    b, d, l = p["u"].shape
+    n = p["A"].shape[1]
+    x0 = p["initial_state"] if p["initial_state"] is not None else np.zeros((b, d, n))
+    out, last = oracle.selective_scan_ref(**dict(p, initial_state=x0), delta_softplus=softplus,
+                                          return_last_state=True)
+    fixed = p["B"].ndim == 2
+    st_ = x0
+    for t in range(l):
+        Bt = p["B"] if fixed else p["B"][..., t]
+        Ct = p["C"] if fixed else p["C"][..., t]
+        o, st_ = oracle.selective_state_update_ref(st_, p["u"][:, :, t], p["delta"][:, :, t], p["A"], Bt, Ct,
+                                                   D=p["D"], z=None if p["z"] is None else p["z"][:, :, t],
+                                                   delta_bias=p["delta_bias"], delta_softplus=softplus,
+                                                   bc_fixed=fixed)
+        assert _rel(o, out[:, :, t]) < 1e-12
+    assert _rel(st_, last) < 1e-12
