@@ -186,3 +186,25 @@ def test_planted_slips_fail_finite_differences(slip, monkeypatch):
                             lambda x, ng: np.repeat(x.sum(axis=1, keepdims=True), ng, axis=1)[:, :ng])
     got = bwd.selective_scan_bwd_ref(dout, **p, delta_softplus=True)
     assert max(_rel(got[k], fd[k]) for k in fd) > 1e-3
+
+
+def test_golden_tiny_backward():
+    """The backward oracle on the tiny workload equals the committed fixture
+    (written by tests/golden/make_golden.py, which calls only the oracles); a
+    guard against later changes to the oracle, the generator or dout's draw.
+    libm may differ by an ulp between hosts, hence 1e-12 and not equality."""
+    import json
+    import os
+    from state_space_model_03_gb300 import workloads
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "tiny_fp32_bwd_oracle.json")
+    with open(path) as f:
+        doc = json.load(f)
+    w = workloads.WORKLOADS["tiny_fp32"]
+    x = workloads.make_inputs(w)
+    dout = workloads.make_dout(w)
+    assert dout.reshape(-1)[:6].tolist() == doc["dout_head"]
+    got = bwd.selective_scan_bwd_ref(dout, x["u"], x["delta"], x["A"], x["B"], x["C"], D=x["D"], z=x["z"],
+                                     delta_bias=x["delta_bias"], delta_softplus=True)
+    for k, vals in doc["grads"].items():
+        ref = np.array([float(v) for v in vals])
+        assert np.max(np.abs(got[k].reshape(-1) - ref)) <= 1e-12 * np.max(np.abs(ref)), k
