@@ -27,10 +27,12 @@ constexpr int kCPC = 2 * kW;  // channels per CTA
 
 constexpr int kYRow = kT + 4;  // padded row of the per-state y terms (conflict-free 16-byte stores)
 
-// sin and cos of th: th = k pi/2 + r (Cody-Waite reduction with fused
-// multiply-adds against a three-part split of pi/2), |r| <= pi/4, then the
-// Taylor series of sin r to r^9 and of cos r to r^8 (truncation below 4e-8)
-// and the quadrant k mod 4. Accurate to a few fp32 ulps for |th| up to ~1e5.
+// sin and cos of th + lo: th = k pi/2 + r (Cody-Waite reduction with fused
+// multiply-adds against a three-part split of pi/2), r += lo, |r| <= pi/4 + |lo|,
+// then the Taylor series of sin r to r^9 and of cos r to r^8 (truncation below
+// 4e-8) and the quadrant k mod 4. lo is the rounding error of the angle's
+// product (th + lo = dt Im A exactly), so the phase keeps fp32 accuracy at
+// large angles; accurate to a few fp32 ulps for |th| up to ~1e5.
 // FAST (16-bit inputs, whose outputs are rounded to 8 or 11 bits): the reduced
 // sin and cos come from the MUFU approximations instead of the series
 // (absolute error ~1e-6 on |r| <= pi/4).
@@ -45,11 +47,12 @@ __device__ __forceinline__ float cos_approx(float x) {
   return y;
 }
 template <bool FAST>
-__device__ __forceinline__ void sincos_rr(float th, float &sn, float &cs) {
+__device__ __forceinline__ void sincos_rr(float th, float lo, float &sn, float &cs) {
   const float k = rintf(th * 0.636619772367581343f);  // 2 / pi
   float r = fmaf(-k, 1.5707963705062866f, th);
   r = fmaf(-k, -4.371138828673793e-08f, r);
   r = fmaf(-k, -1.7763568394002505e-15f, r);
+  r += lo;
   float s, c;
   if constexpr (FAST) {
     s = sin_approx(r);
@@ -65,6 +68,17 @@ __device__ __forceinline__ void sincos_rr(float th, float &sn, float &cs) {
   const float s1 = (q & 1) ? c : s, c1 = (q & 1) ? s : c;
   sn = (q & 2) ? -s1 : s1;
   cs = ((q + 1) & 2) ? -c1 : c1;
+}
+
+// The step of the complex path. A rotation of dt Im A radians per step turns
+// a relative error of dt into a phase error that grows with |Im A|, so fp32
+// inputs take softplus from the library exponential and log1p (each within a
+// few ulps, against ~3e-6 for the MUFU form the real forward uses). 16-bit
+// inputs, whose outputs are rounded to 8 or 11 bits, keep the MUFU form.
+template <typename T>
+__device__ __forceinline__ float softplus_cx(float v) {
+  if constexpr (sizeof(T) == 4) return fmaxf(v, 0.f) + log1pf(expf(-fabsf(v)));
+  else return softplus_f(v);
 }
 
 // kT values of one B/C row starting at step t: 16-byte loads when vec (the
@@ -180,7 +194,7 @@ __global__ void __launch_bounds__(kW * 32, 2) ss_fwd_complex_kernel(const __grid
     if (vj) {
       uj = to_f<T>(raw[0]);
       const float v = to_f<T>(raw[1]) + bias;
-      dtj = p.softplus ? softplus_f(v) : v;
+      dtj = p.softplus ? softplus_cx<T>(v) : v;
       if (p.has_z) gate = silu_f(to_f<T>(raw[2]));
     }
     ch[j] = dtj;
@@ -221,7 +235,10 @@ __global__ void __launch_bounds__(kW * 32, 2) ss_fwd_complex_kernel(const __grid
         for (int q = 0; q < 4; ++q) {
           const float e = ex2(dtv[q] * Ar2[s]);
           float sn, cs;
-          sincos_rr<(sizeof(T) < 4)>(dtv[q] * Ai[s], sn, cs);
+          const float th = dtv[q] * Ai[s];
+          // fp32 inputs: the product's rounding error joins the reduced angle
+          const float lo = (sizeof(T) < 4) ? 0.f : fmaf(dtv[q], Ai[s], -th);
+          sincos_rr<(sizeof(T) < 4)>(th, lo, sn, cs);
           const float ar = e * cs, ai = e * sn;
           const float nr = fmaf(ar, r, fmaf(-ai, im, duv[q] * Bv[i + q]));
           im = fmaf(ar, im, ai * r);
