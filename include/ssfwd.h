@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define SS_ABI_VERSION 4
+#define SS_ABI_VERSION 5
 
 /* Element types. u, delta, z and out share `in_dtype`. */
 typedef enum ss_dtype { SS_F32 = 0, SS_F16 = 1, SS_BF16 = 2 } ss_dtype;
@@ -119,6 +119,15 @@ typedef struct ss_fwd_params {
    * written); any other overlap with an output is SS_ERR_ALIAS. */
   const float *initial_state;
   int64_t initial_state_stride[3];
+  /* Optional caller-owned device int32 (4-byte aligned, not overlapping any
+   * tensor or the workspace) that receives this call's device-side error
+   * code; NULL = the library's per-device word read by ss_device_error. The
+   * kernels only ever write a nonzero code into it, and only if it still
+   * holds 0 (the first error wins), so the caller zeroes it before the call
+   * and reads it after the stream completes. With a word of its own, each
+   * caller (stream, thread) can tell whether its own launch gave up on a
+   * bounded wait, which the shared word cannot show. */
+  int32_t *error_word;
 } ss_fwd_params;
 
 /* SS_ABI_VERSION of the loaded library. */
@@ -169,15 +178,18 @@ int ss_fwd_host(const ss_fwd_params *p,
  * SS_NOALLOC_MAX_SCRATCH bytes that the library carries on every device
  * (held until the process exits) instead of a caller workspace.
  *
- *  - p->workspace / p->workspace_bytes are ignored; inputs and outputs are
- *    the caller's device buffers as for ss_fwd. Nothing is allocated: no
- *    cudaMalloc, cudaFree or allocating library call.
+ *  - p->workspace / p->workspace_bytes are ignored: they are neither used
+ *    nor validated (a stale pointer left there is harmless). Inputs and
+ *    outputs are the caller's device buffers as for ss_fwd. Nothing is
+ *    allocated: no cudaMalloc, cudaFree or allocating library call.
  *  - A problem whose schedule needs more scratch than the buffer holds is
  *    rejected with SS_ERR_SCRATCH before anything is enqueued (ss_fwd with a
  *    workspace handles it).
- *  - The first call on a device looks up the buffer's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture on the device.
+ *  - The first call on a device that passes validation, whatever its size
+ *    (an empty problem will do), looks up the buffer's device address
+ *    (cudaGetSymbolAddress) with that device current and caches it; later
+ *    calls on that device make no such query. Make that first call before
+ *    any stream capture on the device.
  *  - All calls share the one buffer and it keeps the previous call's
  *    contents. Each call writes every summary it later reads, so nothing needs
  *    clearing, but calls whose work overlaps on the GPU (e.g. concurrent
@@ -433,6 +445,15 @@ int ss_fwd_complex(const ss_fwd_complex_params *p, void *stream);
  * a kernel gave up on a bounded wait or tripped a self-check; 0 otherwise).
  * Reading it synchronises with the device. `clear` nonzero resets it to 0.
  * Returns SS_OK and writes the word into *out_word, or SS_ERR_CUDA.
+ *
+ * The word is shared by every call on the device that passes no error_word of
+ * its own (ss_fwd_params.error_word), across streams and host threads, and is
+ * sticky: it keeps the first code written until it is cleared here. A
+ * nonzero value therefore says that SOME such call failed since the last
+ * clear, not which one; give each call its own error_word to tell them apart.
+ * An ss_fwd call that gave up on a wait still returned SS_OK when it was
+ * enqueued (the failure happens later, on the device), so the word is the
+ * only report of it.
  */
 int ss_device_error(int32_t *out_word, int clear);
 

@@ -31,7 +31,7 @@ _lib = None
 
 SS_F32, SS_F16, SS_BF16 = 0, 1, 2
 SS_BC_FIXED, SS_BC_VARIABLE = 0, 1
-SS_ABI_VERSION = 4
+SS_ABI_VERSION = 5
 _DT = {torch.float32: SS_F32, torch.float16: SS_F16, torch.bfloat16: SS_BF16}
 
 _i64x2, _i64x3, _i64x4 = ctypes.c_int64 * 2, ctypes.c_int64 * 3, ctypes.c_int64 * 4
@@ -52,6 +52,7 @@ class SSFwdParams(ctypes.Structure):
         ("B_stride", _i64x4), ("C_stride", _i64x4), ("A_stride", _i64x2), ("last_state_stride", _i64x3),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64),
         ("initial_state", ctypes.c_void_p), ("initial_state_stride", _i64x3),
+        ("error_word", ctypes.c_void_p),
     ]
 
 

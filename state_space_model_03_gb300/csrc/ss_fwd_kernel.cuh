@@ -73,9 +73,12 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int32_t kErrWaitFull = 1;
 constexpr int32_t kErrWaitEmpty = 2;
 constexpr int32_t kErrWaitReady = 3;
-// Bounded mbarrier wait: try_wait suspends up to a hardware time limit per
-// call; 1<<22 calls is far beyond any legitimate wait (microseconds).
-constexpr uint32_t kMaxWaitIters = 1u << 22;
+// Bounded mbarrier wait: each try_wait suspends at most kSuspendNs (an
+// explicit time hint, so the bound does not rest on a hardware default), and
+// a wait gives up after kMaxWaitIters calls: about a second, far beyond any
+// legitimate wait (microseconds).
+constexpr uint32_t kSuspendNs = 1000;
+constexpr uint32_t kMaxWaitIters = 1u << 20;
 
 struct KParams {
   int batch, dim, seqlen, dstate, ngroups, dpg, tiles_per_group;
@@ -95,6 +98,8 @@ struct KParams {
   float *last;
   long long su[3], sd[3], sz[3], so[3], sB[4], sC[4], sA[2], sl[3];
   int32_t *err;
+  uint32_t wait_limit;  // try_wait calls before a wait gives up (kMaxWaitIters in production)
+  int stall_chunk;      // test hook: chunk the producer never issues (-1: none)
 };
 
 // ----------------------------------------------------------------------------
@@ -117,9 +122,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs) : "memory");
   return ok != 0;
 }
 // Non-blocking: has the phase with this parity completed?
@@ -132,9 +137,11 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
-// Bounded wait; returns false (and records `code`) if the phase never completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err, int32_t code) {
-  for (uint32_t i = 0; i < kMaxWaitIters; ++i)
+// Bounded wait; returns false (and records `code`) if the phase never completed
+// within `limit` try_wait calls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err, int32_t code,
+                                          uint32_t limit = kMaxWaitIters) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   atomicCAS(err, 0, code);
   return false;
@@ -575,6 +582,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     constexpr bool bc_swz = (bc_row == 128);
     const int nrow_bc = p.dstate;
     auto issue = [&](int ci) -> void {
+      if (ci == p.stall_chunk) return;  // test hook: this chunk never lands
       const int s = ci % STAGES;
       const int t0 = tseg0 + ci * L;
       unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
@@ -633,7 +641,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     // issue the next chunk once its stage is free (blocking)
     auto issue_next = [&]() -> bool {
       const int prev = issued - STAGES;  // chunk that last used this stage
-      if (prev >= 0 && !mbar_wait(&bar_empty[prev % STAGES], (prev / STAGES) & 1, p.err, kErrWaitEmpty))
+      if (prev >= 0 && !mbar_wait(&bar_empty[prev % STAGES], (prev / STAGES) & 1, p.err, kErrWaitEmpty, p.wait_limit))
         return false;
       issue(issued++);
       return true;
@@ -648,8 +656,8 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
                (issued < STAGES || mbar_test(&bar_empty[(issued - STAGES) % STAGES], ((issued - STAGES) / STAGES) & 1)))
           issue(issued++);
         if (!ok) break;
-        if (!mbar_wait(&bar_full[ci % STAGES], (ci / STAGES) & 1, p.err, kErrWaitFull) ||
-            (q >= NSLOT && !mbar_wait(&bar_pempty[slot], ((q / NSLOT) - 1) & 1, p.err, kErrWaitEmpty))) {
+        if (!mbar_wait(&bar_full[ci % STAGES], (ci / STAGES) & 1, p.err, kErrWaitFull, p.wait_limit) ||
+            (q >= NSLOT && !mbar_wait(&bar_pempty[slot], ((q / NSLOT) - 1) & 1, p.err, kErrWaitEmpty, p.wait_limit))) {
           ok = false;
           break;
         }
@@ -667,7 +675,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     if (!ok) {
       // give copies already in flight a bounded chance to land before exiting
       for (int ci = (issued > STAGES ? issued - STAGES : 0); ci < issued; ++ci)
-        (void)mbar_wait(&bar_full[ci % STAGES], (ci / STAGES) & 1, p.err, kErrWaitFull);
+        (void)mbar_wait(&bar_full[ci % STAGES], (ci / STAGES) & 1, p.err, kErrWaitFull, p.wait_limit);
     }
     return;
   }
@@ -701,8 +709,8 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     auto prep = [&](int q) -> bool {
       const int ci = q / SUBS, sub = q - ci * SUBS, s = ci % STAGES;
       const int slot = q % NSLOT;
-      if (!mbar_wait(&bar_full[s], (ci / STAGES) & 1, p.err, kErrWaitFull)) return false;
-      if (q >= NSLOT && !mbar_wait(&bar_pempty[slot], ((q / NSLOT) - 1) & 1, p.err, kErrWaitEmpty)) return false;
+      if (!mbar_wait(&bar_full[s], (ci / STAGES) & 1, p.err, kErrWaitFull, p.wait_limit)) return false;
+      if (q >= NSLOT && !mbar_wait(&bar_pempty[slot], ((q / NSLOT) - 1) & 1, p.err, kErrWaitEmpty, p.wait_limit)) return false;
       const unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
       const unsigned char *sd = smem + CF::OFF_DL + s * CF::TILE;
       float2 *P = reinterpret_cast<float2 *>(smem + CF::OFF_P + slot * CF::P_SLOT);
@@ -734,7 +742,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     auto epilogue = [&](int q) -> bool {
       const int ci = q / SUBS, sub = q - ci * SUBS, s = ci % STAGES;
       const int slot = q % NSLOT;
-      if (!mbar_wait(&bar_yfull[slot], (q / NSLOT) & 1, p.err, kErrWaitReady)) return false;
+      if (!mbar_wait(&bar_yfull[slot], (q / NSLOT) & 1, p.err, kErrWaitReady, p.wait_limit)) return false;
       const float *Y = reinterpret_cast<const float *>(smem + CF::OFF_Y + slot * CF::Y_SLOT);
       float y[EPT];
 #pragma unroll
@@ -892,8 +900,8 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     }
     for (int q = 0; q < nsub; ++q) {
       const int slot = q % NSLOT;
-      if (!mbar_wait(&bar_pfull[slot], (q / NSLOT) & 1, p.err, kErrWaitReady)) break;
-      if (!SUMMARY && q >= NSLOT && !mbar_wait(&bar_yempty[slot], ((q / NSLOT) - 1) & 1, p.err, kErrWaitEmpty)) break;
+      if (!mbar_wait(&bar_pfull[slot], (q / NSLOT) & 1, p.err, kErrWaitReady, p.wait_limit)) break;
+      if (!SUMMARY && q >= NSLOT && !mbar_wait(&bar_yempty[slot], ((q / NSLOT) - 1) & 1, p.err, kErrWaitEmpty, p.wait_limit)) break;
       const float2 *P = reinterpret_cast<const float2 *>(smem + CF::OFF_P + slot * CF::P_SLOT);
       const float *b32 = reinterpret_cast<const float *>(smem + CF::OFF_BC + slot * CF::BC_SLOT);
       const float *c32 = b32 + S * NP;

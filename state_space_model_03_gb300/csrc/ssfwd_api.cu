@@ -82,6 +82,7 @@ int validate(const ss_fwd_params *p) {
   if (p->dstate > 64) return SS_ERR_UNSUPPORTED;
   if (!fixed && (p->ngroups < 1 || (p->dim > 0 && p->dim % p->ngroups != 0))) return SS_ERR_SHAPE;
   if (p->batch > 65535 || p->dim > (1 << 30) || p->seqlen > (int64_t(1) << 31) - 1024) return SS_ERR_UNSUPPORTED;
+  if (p->error_word && !aligned(p->error_word, 4)) return SS_ERR_ALIGN;
   if (p->batch * p->dim == 0) return SS_OK;
   if (p->last_state && p->last_state_stride[2] != 1) return SS_ERR_STRIDE;
   for (int i = 0; i < 3; ++i)
@@ -148,12 +149,19 @@ int validate(const ss_fwd_params *p) {
   if (overlap(out, last) || overlap(out, init)) return SS_ERR_ALIAS;
   if (p->initial_state) ins[ni++] = init;  // the workspace must not overlap it either
   if (p->workspace_bytes < 0) return SS_ERR_SHAPE;
+  Range ws{0, 0};
   if (p->workspace && p->workspace_bytes > 0) {
-    const Range ws{reinterpret_cast<uintptr_t>(p->workspace),
-                   reinterpret_cast<uintptr_t>(p->workspace) + static_cast<uintptr_t>(p->workspace_bytes)};
+    ws = Range{reinterpret_cast<uintptr_t>(p->workspace),
+               reinterpret_cast<uintptr_t>(p->workspace) + static_cast<uintptr_t>(p->workspace_bytes)};
     for (int i = 0; i < ni; ++i)
       if (overlap(ws, ins[i])) return SS_ERR_ALIAS;
     if (overlap(ws, out) || overlap(ws, last)) return SS_ERR_ALIAS;
+  }
+  if (p->error_word) {  // written by the kernels on failure: it must not alias anything they touch
+    const Range ew{reinterpret_cast<uintptr_t>(p->error_word), reinterpret_cast<uintptr_t>(p->error_word) + 4};
+    for (int i = 0; i < ni; ++i)
+      if (overlap(ew, ins[i])) return SS_ERR_ALIAS;
+    if (overlap(ew, out) || overlap(ew, last) || overlap(ew, ws)) return SS_ERR_ALIAS;
   }
   return SS_OK;
 }
@@ -338,7 +346,7 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
                                                      p->initial_state_stride[1]);
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
   }
-  int32_t *err = error_word_ptr(dev);
+  int32_t *err = p->error_word ? p->error_word : error_word_ptr(dev);
   if (!err) return SS_ERR_CUDA;
   std::call_once(g_encode_once, load_encode);
 
@@ -377,6 +385,15 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   kp.init = p->initial_state;
   for (int i = 0; i < 3; ++i) kp.si[i] = p->initial_state ? p->initial_state_stride[i] : 0;
   kp.err = err;
+  kp.wait_limit = ssk::kMaxWaitIters;
+  kp.stall_chunk = -1;
+  if (const char *st = std::getenv("SSFWD_TEST_STALL")) {
+    // Test hook: the producer never issues chunk `st` of each CTA and every
+    // wait gives up after a short limit, so the bounded-wait exits and the
+    // error word can be checked without a hang.
+    kp.stall_chunk = std::atoi(st);
+    kp.wait_limit = 1u << 10;
+  }
 
   const int nsm = num_sms(dev);
   SegPlan sp = plan_segments(p, np, ki.L, ki.ch, nsm);
@@ -1210,22 +1227,28 @@ int ss_fwd(const ss_fwd_params *p, void *stream) {
 }
 
 int ss_fwd_noalloc(const ss_fwd_params *p, void *stream) {
-  int st = validate(p);
+  if (!p) return SS_ERR_NULL;
+  if (p->abi_version != SS_ABI_VERSION) return SS_ERR_VERSION;
+  // The caller's workspace fields play no part here: validate and run a copy
+  // without them, so a stale pointer left there cannot cause an alias error.
+  ss_fwd_params q = *p;
+  q.workspace = nullptr;
+  q.workspace_bytes = 0;
+  int st = validate(&q);
   if (st != SS_OK) return st;
+  // Every call looks the scratch address up (cached after the first on each
+  // device), so any first call, even an empty one, prepares the device.
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+  void *scratch = noalloc_scratch(dev);
+  if (!scratch) return SS_ERR_CUDA;
   int64_t need = 0;
-  st = workspace_bytes(p, &need);
+  st = workspace_bytes(&q, &need);
   if (st != SS_OK) return st;
   if (need > SS_NOALLOC_MAX_SCRATCH) return SS_ERR_SCRATCH;
-  void *ws = nullptr;
-  if (need > 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
-    ws = noalloc_scratch(dev);
-    if (!ws) return SS_ERR_CUDA;
-  }
   // The summaries are fully written by the summary pass before the forward
   // pass reads them, so the buffer needs no clearing between calls.
-  return launch(p, static_cast<cudaStream_t>(stream), ws, need);
+  return launch(&q, static_cast<cudaStream_t>(stream), need > 0 ? scratch : nullptr, need);
 }
 
 int ss_fwd_host(const ss_fwd_params *p, const void *h_u, const void *h_delta, const void *h_z, const void *h_B,

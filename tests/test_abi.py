@@ -110,6 +110,11 @@ def test_valid_params_pass(lib):
     (lambda p: setattr(p, "last_state", p.out + 128), 6),
     (lambda p: setattr(p, "workspace_bytes", -1), 2),
     (lambda p: (setattr(p, "workspace", p.u + 64), setattr(p, "workspace_bytes", 256)), 6),
+    (lambda p: setattr(p, "error_word", p.u + 2), 5),         # the error word needs 4-byte alignment
+    (lambda p: setattr(p, "error_word", p.out + 64), 6),      # ... and must not alias an output
+    (lambda p: setattr(p, "error_word", p.A), 6),             # ... or an input
+    (lambda p: (setattr(p, "workspace", p.last_state + (1 << 20)), setattr(p, "workspace_bytes", 256),
+                setattr(p, "error_word", p.last_state + (1 << 20) + 16)), 6),  # ... or the workspace
 ])
 def test_invalid_params_rejected(lib, mutate, status):
     p = _good()
@@ -117,6 +122,30 @@ def test_invalid_params_rejected(lib, mutate, status):
     assert _val(lib, p) == status
     # ss_fwd validates first and returns the same status with nothing launched
     assert lib.ss_fwd(ctypes.byref(p), None) == status
+
+
+def test_caller_error_word_accepted(lib):
+    p = _good()
+    p.error_word = p.last_state + (1 << 20)  # a word of its own, clear of every tensor
+    assert _val(lib, p) == 0
+
+
+def test_noalloc_ignores_the_workspace_fields(lib, monkeypatch):
+    """ss_fwd_noalloc neither uses nor validates p->workspace: a stale pointer
+    that would alias an input under ss_fwd is no error there. The addresses
+    are fake, so the host fault hook stops the call before any launch (on a
+    machine with or without a GPU); the status is then SS_ERR_CUDA, not the
+    alias or shape error a checked workspace would give."""
+    monkeypatch.setenv("SSFWD_FAULT", "launch")
+    p = _good()
+    p.workspace, p.workspace_bytes = p.u + 64, 256
+    assert _val(lib, p) == 6
+    assert lib.ss_fwd_noalloc(ctypes.byref(p), None) == 8
+    p.workspace_bytes = -1
+    assert lib.ss_fwd_noalloc(ctypes.byref(p), None) == 8
+    p.abi_version = 0
+    assert lib.ss_fwd_noalloc(ctypes.byref(p), None) == 10
+    assert lib.ss_fwd_noalloc(None, None) == 1
 
 
 def test_null_params(lib):
