@@ -15,8 +15,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libssfwd.so")
-SOURCES = ["ssfwd_api.cu", "ss_fwd_f32.cu", "ss_fwd_f16.cu", "ss_fwd_bf16.cu", "ss_state_update.cu", "ss_conv1d.cu", "ss_bwd.cu", "ss_fwd_complex.cu"]
-HEADERS = ["ss_dispatch.h", "ss_fwd_kernel.cuh"]
+SOURCES = ["ssfwd_api.cu", "ss_fwd_f32.cu", "ss_fwd_f16.cu", "ss_fwd_bf16.cu", "ss_fwd_lane.cu", "ss_state_update.cu", "ss_conv1d.cu", "ss_bwd.cu", "ss_fwd_complex.cu"]
+HEADERS = ["ss_dispatch.h", "ss_fwd_kernel.cuh", "ss_fwd_instances.cuh"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
          "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"), "-I", CSRC]

@@ -1,52 +1,8 @@
-// Kernel instances for __half inputs (u, delta, z, out).
-#include "ss_dispatch.h"
-#include "ss_fwd_kernel.cuh"
+// Kernel instances of the selective-scan forward for __half inputs.
+#include "ss_fwd_instances.cuh"
 
 namespace ssk {
-
-template <int NP, int K, bool FIXED, bool BCF32, bool TMA, bool SUMMARY, int SUB, int CHN = 32>
-static KernelInfo info() {
-  using CF = Cfg<__half, NP, K, FIXED, BCF32, SUB, CHN>;
-  return KernelInfo{
-      reinterpret_cast<const void *>(&ss_fwd_kernel<__half, NP, K, FIXED, BCF32, TMA, SUMMARY, SUB, CHN>),
-      CF::SMEM_ALLOC, CF::THREADS, CF::CH, CF::L};
-}
-
-template <int NP, int K, bool FIXED, bool BCF32, bool TMA>
-static KernelInfo pick3(bool summary, bool sub8, bool ch16) {
-  if (summary) return ch16 ? KernelInfo{nullptr, 0, 0, 0, 0} : info<NP, K, FIXED, BCF32, TMA, true, 16>();
-  if constexpr (TMA) {
-    if constexpr (NP == 16) {  // 16-channel CTAs: the common state size only
-      if (ch16 && !sub8) return info<NP, K, FIXED, BCF32, TMA, false, 16, 16>();
-    }
-    if (ch16) return KernelInfo{nullptr, 0, 0, 0, 0};
-    if (sub8) return info<NP, K, FIXED, BCF32, TMA, false, 8>();
-  }
-  if (sub8 || ch16) return KernelInfo{nullptr, 0, 0, 0, 0};
-  return info<NP, K, FIXED, BCF32, TMA, false, 16>();
-}
-
-template <int NP, int K, bool FIXED, bool BCF32>
-static KernelInfo pick2(bool tma, bool summary, bool sub8, bool ch16) {
-  return tma ? pick3<NP, K, FIXED, BCF32, true>(summary, sub8, ch16) : pick3<NP, K, FIXED, BCF32, false>(summary, sub8, ch16);
-}
-
-template <int NP, int K>
-static KernelInfo pick(bool fixed, bool bc_f32, bool tma, bool summary, bool sub8, bool ch16) {
-  // fixed B/C live in registers (fp32); BCF32 only selects the variable tile type
-  if (fixed) return pick2<NP, K, true, false>(tma, summary, sub8, ch16);
-  return bc_f32 ? pick2<NP, K, false, true>(tma, summary, sub8, ch16) : pick2<NP, K, false, false>(tma, summary, sub8, ch16);
-}
-
 KernelInfo lookup_f16(int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8, bool ch16) {
-  switch (np) {
-    case 4: return pick<4, 4>(fixed, bc_f32, tma, summary, sub8, ch16);
-    case 8: return pick<8, 4>(fixed, bc_f32, tma, summary, sub8, ch16);
-    case 16: return pick<16, 4>(fixed, bc_f32, tma, summary, sub8, ch16);
-    case 32: return pick<32, 8>(fixed, bc_f32, tma, summary, sub8, ch16);
-    case 64: return pick<64, 8>(fixed, bc_f32, tma, summary, sub8, ch16);
-    default: return KernelInfo{nullptr, 0, 0, 0, 0};
-  }
+  return reg::lookup<__half>(np, fixed, bc_f32, tma, summary, sub8, ch16);
 }
-
 }  // namespace ssk
