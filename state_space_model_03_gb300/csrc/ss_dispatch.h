@@ -85,6 +85,22 @@ struct BwdKernel {
 };
 BwdKernel bwd_kernel(int in_dtype, bool bc_f32, bool fixed, int dstate);
 
+// Fixed-B/C forward with one lane per channel (ss_fwd_lane.cu): the forward
+// (gen: plain update, for a start state) or the segment-summary pass, for
+// padded state counts 4, 8 or 16. Launch with 32 threads per CTA, grid
+// (batch * ceil(dim / 32), segments), the KParams of the 32-channel kernel and
+// three 3-D tensor maps (u, delta, z) with boxes of L steps x 32 channels.
+// smem is for two streamed tensors; add lane_stages() * lane_tile_bytes()
+// when z is streamed.
+struct LaneKernel {
+  const void *fn;
+  int smem;  // dynamic shared memory bytes
+  int L;     // steps per chunk (the box width)
+};
+LaneKernel lane_kernel(int in_dtype, int ns, bool summary, bool gen);
+int lane_tile_bytes();
+int lane_stages();
+
 // Complex-A forward (ss_fwd_complex).
 struct CxParams {
   int batch, dim, dstate, ngroups, dpg, tiles;  // tiles: CTAs per group along the channels

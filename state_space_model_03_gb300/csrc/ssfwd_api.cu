@@ -300,6 +300,79 @@ SegPlan plan_segments(const ss_fwd_params *p, int np, int L, int ch, int nsm) {
   return sp;
 }
 
+// Fixed-B/C forward with one lane per channel (ss_fwd_lane.cu). It serves
+// fixed B/C with dstate <= 16 whenever u, delta (and z) have legal TMA
+// descriptors with 32-channel boxes; everything else runs the 32-channel
+// kernel. Its warps (one per 32 channels per segment) saturate at about eight
+// per SM, and a segmented schedule costs a summary pass (~0.8x of the
+// forward), so the sequence is split only when the unsplit grid gives fewer
+// than three warps per SM, into as many segments as one wave of resident CTAs
+// holds (at most 12 per SM), each at least kLaneMinSeg steps. `cap` bounds the
+// workspace (the caller's, or the static buffer of ss_fwd_noalloc): the plan
+// drops segments until it fits.
+constexpr int64_t kLaneMinSeg = 512;
+
+struct LanePlan {
+  bool use = false;
+  ssk::LaneKernel fwd{}, sum{};
+  int smem = 0, nseg = 1, seg_len = 0;
+  int64_t ws_bytes = 0;
+  CUtensorMap tm[3];
+};
+
+int g_lane_occ[kMaxDevices][3][3][2] = {};  // CTAs/SM of the lane forward by (dtype, ns, z)
+
+bool lane_setup(const ss_fwd_params *p, int dev, int64_t cap, LanePlan *lp) {
+  lp->use = false;
+  if (p->bc_mode != SS_BC_FIXED || p->dstate > 16 || std::getenv("SSFWD_NO_LANE") || std::getenv("SSFWD_NO_TMA"))
+    return false;
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode || dev < 0 || dev >= kMaxDevices) return false;
+  const int np = padded_states(p->dstate);
+  const int es = elem_size(p->in_dtype);
+  lp->fwd = ssk::lane_kernel(p->in_dtype, np, false, p->initial_state != nullptr);
+  lp->sum = ssk::lane_kernel(p->in_dtype, np, true, false);
+  if (!lp->fwd.fn || !lp->sum.fn) return false;
+  std::memset(lp->tm, 0, sizeof(lp->tm));
+  if (!make_map3(&lp->tm[0], p->u, es, p, p->u_stride, lp->fwd.L, 32) ||
+      !make_map3(&lp->tm[1], p->delta, es, p, p->delta_stride, lp->fwd.L, 32) ||
+      (p->z && !make_map3(&lp->tm[2], p->z, es, p, p->z_stride, lp->fwd.L, 32)))
+    return false;
+  lp->smem = lp->fwd.smem + (p->z ? ssk::lane_stages() * ssk::lane_tile_bytes() : 0);
+  int occ = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int &slot = g_lane_occ[dev][p->in_dtype][np == 4 ? 0 : np == 8 ? 1 : 2][p->z ? 1 : 0];
+    if (!slot && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&slot, lp->fwd.fn, 32, lp->smem) != cudaSuccess)
+      slot = 0;
+    occ = slot;
+  }
+  const int nsm = num_sms(dev);
+  if (occ <= 0 || nsm <= 0) return false;
+  const int64_t warps = p->batch * ((p->dim + 31) / 32);  // warps of one segment
+  lp->nseg = 1;
+  lp->seg_len = static_cast<int>(p->seqlen);
+  if (warps < 3 * int64_t(nsm)) {
+    int64_t want = std::min<int64_t>(occ, 12) * nsm / warps;
+    want = std::min<int64_t>(want, p->seqlen / kLaneMinSeg);
+    want = std::min<int64_t>(want, kMaxSegments);
+    const int64_t per_seg = p->batch * p->dim * (np + 1) * int64_t(sizeof(float));
+    if (per_seg > 0) want = std::min<int64_t>(want, cap / per_seg + 1);  // workspace for want - 1 summaries
+    if (want >= 2) {
+      int64_t len = (p->seqlen + want - 1) / want;
+      len = (len + lp->fwd.L - 1) / lp->fwd.L * lp->fwd.L;
+      const int64_t nseg = (p->seqlen + len - 1) / len;
+      if (nseg >= 2) {
+        lp->nseg = static_cast<int>(nseg);
+        lp->seg_len = static_cast<int>(len);
+        lp->ws_bytes = (nseg - 1) * per_seg;
+      }
+    }
+  }
+  lp->use = true;
+  return true;
+}
+
 bool set_smem_attr(int dev, const ssk::KernelInfo &ki, int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary,
                    bool sub8 = false, bool ch16 = false) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -312,12 +385,20 @@ bool set_smem_attr(int dev, const ssk::KernelInfo &ki, int dt, int np, bool fixe
   return true;
 }
 
-// Bytes of workspace the fastest path wants for p (0 if it needs none).
-int workspace_bytes(const ss_fwd_params *p, int64_t *bytes) {
+// Bytes of workspace the fastest path wants for p (0 if it needs none), with
+// at most `cap` bytes for the one-lane-per-channel schedule.
+int workspace_bytes(const ss_fwd_params *p, int64_t *bytes, int64_t cap = INT64_MAX) {
   *bytes = 0;
   if (p->batch * p->dim == 0 || p->seqlen == 0) return SS_OK;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+  {
+    LanePlan lp;
+    if (lane_setup(p, dev, cap, &lp)) {
+      *bytes = lp.ws_bytes;
+      return SS_OK;
+    }
+  }
   const bool fixed = p->bc_mode == SS_BC_FIXED;
   const int np = padded_states(p->dstate);
   ssk::KernelInfo ki = lookup(p->in_dtype, np, fixed, p->bc_dtype == SS_F32, true, false);
@@ -396,6 +477,32 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   }
 
   const int nsm = num_sms(dev);
+  {
+    // fixed B/C, dstate <= 16: one lane per channel when the descriptors allow
+    LanePlan lp;
+    const bool ws_ok = ws && aligned(ws, 16) && !std::getenv("SSFWD_NO_SEGMENTS");
+    if (lane_setup(p, dev, ws_ok ? ws_bytes : 0, &lp)) {
+      kp.nseg = lp.nseg;
+      kp.seg_len = lp.seg_len;
+      kp.ws = lp.nseg > 1 ? static_cast<float *>(ws) : nullptr;
+      const unsigned gx = static_cast<unsigned>(p->batch * ((p->dim + 31) / 32));
+      if (std::getenv("SSFWD_DEBUG"))
+        std::fprintf(stderr, "ssfwd: lane np=%d L=%d grid=%ux%d seg_len=%d smem=%d\n", np, lp.fwd.L, gx,
+                     lp.nseg, lp.seg_len, lp.smem);
+      if (fault_injected("launch")) return SS_ERR_CUDA;
+      void *args[4] = {&kp, &lp.tm[0], &lp.tm[1], &lp.tm[2]};
+      if (lp.nseg > 1) {
+        const int ssm = lp.sum.smem;  // the summary pass streams u and delta only
+        if (cudaLaunchKernel(lp.sum.fn, dim3(gx, lp.nseg - 1), dim3(32), args, static_cast<size_t>(ssm), stream) !=
+            cudaSuccess)
+          return SS_ERR_CUDA;
+      }
+      return cudaLaunchKernel(lp.fwd.fn, dim3(gx, lp.nseg), dim3(32), args, static_cast<size_t>(lp.smem), stream) ==
+                     cudaSuccess
+                 ? SS_OK
+                 : SS_ERR_CUDA;
+    }
+  }
   SegPlan sp = plan_segments(p, np, ki.L, ki.ch, nsm);
   if (sp.nseg > 1 && (!ws || ws_bytes < sp.ws_bytes || !aligned(ws, 16) || std::getenv("SSFWD_NO_SEGMENTS"))) {
     sp.nseg = 1;  // no (or too small a) workspace: single pass over the whole sequence
@@ -1243,7 +1350,7 @@ int ss_fwd_noalloc(const ss_fwd_params *p, void *stream) {
   void *scratch = noalloc_scratch(dev);
   if (!scratch) return SS_ERR_CUDA;
   int64_t need = 0;
-  st = workspace_bytes(&q, &need);
+  st = workspace_bytes(&q, &need, SS_NOALLOC_MAX_SCRATCH);
   if (st != SS_OK) return st;
   if (need > SS_NOALLOC_MAX_SCRATCH) return SS_ERR_SCRATCH;
   // The summaries are fully written by the summary pass before the forward

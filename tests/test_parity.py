@@ -290,6 +290,61 @@ def test_segmented_sequence(case, monkeypatch):
         assert float((lst - l1).abs().max()) <= TOL[dt] * float(l1.abs().max())
 
 
+LANE = [
+    # fixed B/C, dstate <= 16, TMA-legal rows: the one-lane-per-channel kernel.
+    # (batch, dim, seqlen, dstate, dtype, z, D, bias, softplus, last, init, segmented)
+    (2, 37, 264, 16, "bf16", True, True, True, True, True, False, False),
+    (1, 40, 1000, 13, "fp16", True, False, True, True, True, False, False),
+    (3, 32, 96, 4, "fp32", False, True, False, False, True, False, False),
+    (1, 64, 8, 8, "bf16", True, True, True, True, True, False, False),
+    (2, 33, 4000, 1, "fp32", True, True, True, True, True, False, True),
+    (2, 37, 512, 16, "fp32", False, True, True, True, True, True, False),
+    (1, 48, 16384, 16, "bf16", True, True, True, True, True, False, True),
+    (1, 40, 8000, 13, "bf16", True, True, True, True, True, True, True),
+    (1, 32, 10000, 16, "fp16", True, True, True, True, False, False, True),
+    (1, 64, 9000, 8, "fp32", False, True, True, True, True, True, True),
+]
+
+
+@pytest.mark.parametrize("case", LANE, ids=[f"{c[4]}-b{c[0]}d{c[1]}l{c[2]}n{c[3]}{'-init' if c[10] else ''}"
+                                            f"{'-seg' if c[11] else ''}" for c in LANE])
+def test_fixed_bc_one_lane_per_channel(case, capfd, monkeypatch):
+    """Fixed B/C with up to 16 states on TMA-legal rows runs the kernel that
+    gives each lane a whole channel (the launch report says so); with few
+    rows and a long sequence it splits the sequence into segments. Checked
+    element by element against the oracle, start states included."""
+    b, d, l, n, dt, z, D, bias, sp, last, init, seg = case
+    w = workloads.Workload("lane", b, d, l, n, bc="fixed", dtype=dt, has_z=z, D_mode="normal" if D else "none",
+                           has_bias=bias, delta_softplus=sp, return_last_state=last, bc_std=0.25,
+                           dt_range=(0.001, 0.01) if seg else (0.001, 0.1), seed=2000 + l + n)
+    x = workloads.make_inputs(w)
+    if not sp:  # the raw sum is the step: keep delta + delta_bias a positive step size
+        x["delta"] = (x["delta"].float().abs() * 0.05 + 0.01).to(x["delta"].dtype)
+    x0 = None
+    if init:
+        g = torch.Generator().manual_seed(w.seed + 3)
+        x0 = torch.randn(b, d, n, generator=g)
+    monkeypatch.setenv("SSFWD_DEBUG", "1")
+    dev = _to_dev(x)
+    res = api.selective_scan_fn(**dev, delta_softplus=sp, return_last_state=last,
+                                initial_state=None if x0 is None else x0.cuda())
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    report = capfd.readouterr().err
+    assert "ssfwd: lane" in report, report
+    nseg = int(report.split("ssfwd: lane")[1].split("grid=")[1].split()[0].split("x")[1])
+    assert (nseg > 1) == seg, report
+    out, lst = res if last else (res, None)
+    ref = oracle.selective_scan_ref(**{k: x[k] for k in NAMES}, delta_softplus=sp, return_last_state=last,
+                                    initial_state=x0, threads=8)
+    ref_out, ref_last = ref if last else (ref, None)
+    o = out.double().cpu().numpy()
+    assert np.isfinite(o).all()
+    assert _rel(o, ref_out) <= TOL[dt]
+    if last:
+        assert _rel(lst.double().cpu().numpy(), ref_last) <= TOL[dt]
+
+
 VARIANT_OF = {("32", "16"): 0, ("32", "8"): 1, ("16", "16"): 2}  # (ch, sub) of the launch report
 VARIANT_CASES = [
     # 16 states (all three forward variants exist), ragged channel tiles and
