@@ -2,15 +2,21 @@
 """Selective-scan forward bench: HBM GB/s, (b*d*l) elements/s and the fraction
 of the GB300 HBM roofline, on seeded synthetic Mamba-layer workloads.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference] [--shard]
 
 One step = one selective-scan forward over the whole workload (all of the
 path: softplus, exp, recurrence, C contraction, D skip, silu gate, last_state),
 inputs resident in HBM. Each step is preceded (outside its timed interval) by a
 write of 2x the L2 size so that no input is served from L2. Kernel time is
 measured with CUDA events on the launching stream; the reported time is the
-max over ranks. Under torchrun every rank runs the full workload on its own GPU
-(independent problems, no data-path collective: weak scaling).
+max over ranks.
+
+Without --workload the scan bench times the four full-size workloads one after
+the other in the same process and prints one line for the largest
+(long_fixed_fp32) with all four under "per_config". Under torchrun every rank
+runs its own copy of the workload (independent problems, no data-path
+collective: weak scaling); with --shard the ranks split ONE problem over batch
+x dim instead (whole groups where the rows allow; strong scaling).
 
 --impl reference times the fp64 CPU oracle (as it stands) on the host cores on
 bounded samples of the same workload, in the same metric.
@@ -62,7 +68,8 @@ def _peaks():
 # Sources that define each timed kernel (its traffic record stays valid while
 # these files are unchanged).
 KERNEL_SOURCES = {
-    "scan": ("ss_fwd_kernel.cuh", "ss_fwd_f32.cu", "ss_fwd_f16.cu", "ss_fwd_bf16.cu"),
+    "scan": ("ss_fwd_kernel.cuh", "ss_fwd_instances.cuh", "ss_fwd_f32.cu", "ss_fwd_f16.cu", "ss_fwd_bf16.cu",
+             "ss_fwd_lane.cu"),
     "state_update": ("ss_state_update.cu",),
     "conv1d": ("ss_conv1d.cu",),
     "bwd": ("ss_bwd.cu",),
@@ -200,6 +207,22 @@ def cpu_baseline(w, x, budget_s=15.0):
                       f"fp64 C oracle, {threads} host threads"}
 
 
+# The largest single-GPU workload is the headline line; the default run also
+# times the other full-size workloads in the same process (per_config).
+HEADLINE_WORKLOAD = "long_fixed_fp32"
+PER_CONFIG = ("mamba130m_bf16", "grouped_bf16", "mamba2p8b_fp16", "long_fixed_fp32")
+PUBLISHED_NOTE = ("the pages quote no throughput, latency or hardware for this operator (the published "
+                  "figures of the baseline are empty), so there is no context line to compare with")
+
+
+def _config(w, world, shard_mode):
+    """The workload as both arms describe it (identical keys and values)."""
+    return {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": w.dstate,
+            "groups": w.groups, "bc": w.bc, "io_dtype": w.dtype, "z": w.has_z,
+            "return_last_state": w.return_last_state,
+            "parallelism": (f"partitioned x{world} (batch x dim)" if shard_mode else f"independent x{world}")}
+
+
 def run_reference(args, rank, world):
     """--impl reference: the fp64 CPU oracle as it stands, on host cores."""
     if rank != 0:
@@ -222,46 +245,60 @@ def run_reference(args, rank, world):
     times = [_oracle_rows_rate(w, x, step_rows[args.warmup + i], threads) for i in range(args.steps)]
     t = sum(times)
     gbs = args.steps * R * _row_bytes(w) / t / 1e9
+    sample = (f"each step: {R} of {nrows} (batch, channel) rows of {w.name} (a rotating sample), full seqlen, "
+              f"fp64 C oracle on {threads} host threads; the rate is the sampled rows' bytes over their time")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded, Mamba-layer shapes)",
-            "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen,
-                       "dstate": w.dstate, "groups": w.groups, "bc": w.bc, "io_dtype": w.dtype},
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "kind": "oracle", "cores": threads,
-                             "sample": f"each step: {R} of {nrows} (batch, channel) rows of {w.name}, "
-                                       f"full seqlen, fp64 C oracle on {threads} host threads"},
-            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "higher_is_better": True, "scaling": "strong" if args.shard else "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded, Mamba-layer shapes)",
+            "config": _config(w, world, args.shard),
+            "method": {"sample": sample},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "kind": "oracle", "cores": threads, "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "published": None, "published_note": PUBLISHED_NOTE}
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, local_rank):
+def _measure(w, x, args, world, rank, dev, shard_mode):
+    """Time args.steps forward steps of workload w on this rank (the whole
+    problem, or this rank's blocks of the partition when shard_mode), L2
+    flushed before each step outside the timed interval. Returns the per-step
+    kernel time (max over ranks) and the launch facts."""
     import torch
-    from state_space_model_03_gb300 import api
-
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    w = workloads.WORKLOADS[args.workload]
-    x = workloads.make_inputs(w)
+    from state_space_model_03_gb300 import api, shard
     lib = api.load_library()
-    d = {k: (None if x[k] is None else x[k].to(dev)) for k in NAMES}
-    nu = api.normalise(*(d[k] for k in NAMES))
-    out = torch.empty(w.batch, w.dim, w.seqlen, dtype=d["u"].dtype, device=dev)
-    last = (torch.empty(w.batch, w.dim, w.dstate, dtype=torch.float32, device=dev)
-            if w.return_last_state else None)
-    params = api.make_params(*nu, w.delta_softplus, out, last)
-    workspace = api.attach_workspace(params, dev)  # segment summaries when the sequence is split
-    launches_per_step = 2 if workspace is not None else 1
-    pref = ctypes.byref(params)
+    B4 = x["B"].unsqueeze(1) if x["B"].dim() == 3 else x["B"]
+    groups = 1 if w.bc == "fixed" else B4.shape[1]
+    if shard_mode:
+        blocks = shard.plan(w.batch, w.dim, groups, world)[rank]
+    else:
+        blocks = [shard.Block(0, w.batch, 0, w.dim)]
+    xx = dict(x)
+    if x["B"].dim() == 3:
+        xx["B"], xx["C"] = x["B"].unsqueeze(1), x["C"].unsqueeze(1)
+    jobs = []
+    for blk in blocks:
+        o = shard.block_operands(xx, blk, groups)
+        d = {k: (None if o[k] is None else o[k].contiguous().to(dev)) for k in NAMES}
+        nu = api.normalise(*(d[k] for k in NAMES))
+        out = torch.empty(nu[0].shape, dtype=nu[0].dtype, device=dev)
+        last = (torch.empty(nu[0].shape[0], nu[0].shape[1], w.dstate, dtype=torch.float32, device=dev)
+                if w.return_last_state else None)
+        params = api.make_params(*nu, w.delta_softplus, out, last)
+        ws = api.attach_workspace(params, dev)
+        jobs.append((params, ws, d, nu, out, last))
+    launches_per_step = sum(2 if j[1] is not None else 1 for j in jobs)
+    prefs = [ctypes.byref(j[0]) for j in jobs]
     stream = torch.cuda.Stream(device=dev)
     sptr = stream.cuda_stream
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
 
     def step():
-        st = lib.ss_fwd(pref, sptr)
-        if st != 0:
-            raise RuntimeError(api.status_string(st))
+        for pr in prefs:
+            st = lib.ss_fwd(pr, sptr)
+            if st != 0:
+                raise RuntimeError(api.status_string(st))
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -275,7 +312,7 @@ def run_ours(args, rank, world, local_rank):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     region0 = torch.cuda.Event(enable_timing=True)
     region1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk, torch.cuda.stream(stream):
+    with ClockSampler(local_rank_of(dev)) as clk, torch.cuda.stream(stream):
         region0.record(stream)
         for i in range(args.steps):
             flush_buf.fill_(i & 0xFF)
@@ -289,65 +326,130 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     if api.device_error() != 0:
         raise RuntimeError("device error word set during the bench")
-    kms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
     ms = sum(kms) / len(kms)
     region_ms = region0.elapsed_time(region1) / args.steps
     ms, region_ms = max_over_ranks([ms, region_ms], world, dev)
-    cb = workloads.compulsory_bytes(w)
-    gbs = job_rate(cb, world, ms) / 1e9
-    elems = job_rate(w.elems, world, ms)
-    peak, peak_src = _peaks()
-    clocks = clk.summary()
+    del jobs, prefs, flush_buf
+    torch.cuda.empty_cache()
+    return {"ms": ms, "region_ms": region_ms, "launches_per_step": launches_per_step,
+            "segmented": launches_per_step > len(blocks), "blocks": [list(b) for b in blocks],
+            "clocks": clk.summary(), "l2_flush_mib": 2 * l2 >> 20}
 
-    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    hx = {k: (None if x[k] is None else x[k].pin_memory()) for k in NAMES}
-    runner = api.HostRunner(**hx, delta_softplus=w.delta_softplus, return_last_state=w.return_last_state,
-                            device=dev)
-    e2e_steps = max(3, min(args.steps, 50))
+
+def local_rank_of(dev):
+    return dev.index if dev.index is not None else 0
+
+
+def _rates(w, ms, world, shard_mode, peak):
+    """Whole-job rates of a step of ms milliseconds (slowest rank): N copies of
+    the problem (weak scaling) or one problem split over N ranks (strong).
+    frac is per GPU: the bytes one rank moved over its time, over its peak."""
+    cb = workloads.compulsory_bytes(w)
+    units = 1 if shard_mode else world
+    gbs = units * cb / (ms * 1e-3) / 1e9
+    return {"ms_per_step": ms, "gbs": gbs, "elems_per_s": units * w.elems / (ms * 1e-3),
+            "frac": gbs / world / peak}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from state_space_model_03_gb300 import api
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peak, peak_src = _peaks()
+    names = [args.workload] if args.workload else list(PER_CONFIG)
+    head = args.workload or HEADLINE_WORKLOAD
+    per_config, measured = {}, {}
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        x = workloads.make_inputs(w)
+        m = _measure(w, x, args, world, rank, dev, args.shard)
+        measured[name] = (w, x, m)
+        r = _rates(w, m["ms"], world, args.shard, peak)
+        per_config[name] = {"ms_per_step": r["ms_per_step"], "gbs": r["gbs"], "elems_per_s": r["elems_per_s"],
+                            "frac": r["frac"],
+                            "launches_per_step": m["launches_per_step"],
+                            "sequence_segmented": m["segmented"], "traffic": _traffic(name)}
+    w, x, m = measured[head]
+    ms = m["ms"]
+    cb = workloads.compulsory_bytes(w)
+    r = _rates(w, ms, world, args.shard, peak)
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the
+    # timed region: this rank's whole problem, or its blocks of the partition
+    from state_space_model_03_gb300 import shard
+    xx = dict(x)
+    if x["B"].dim() == 3:
+        xx["B"], xx["C"] = x["B"].unsqueeze(1), x["C"].unsqueeze(1)
+    groups = 1 if w.bc == "fixed" else xx["B"].shape[1]
+    hosts = []
+    for blk in [shard.Block(*b) for b in m["blocks"]]:
+        o = shard.block_operands(xx, blk, groups)
+        hx = {k: (None if o[k] is None else o[k].contiguous().pin_memory()) for k in NAMES}
+        hosts.append((api.HostRunner(**hx, delta_softplus=w.delta_softplus,
+                                     return_last_state=w.return_last_state, device=dev), hx))
+    e2e_steps = max(3, min(args.steps, 20))
+    stream0 = hosts[0][0].stream
     for _ in range(2):
-        runner.run(**hx)
+        for runner, hx in hosts:
+            runner.run(**hx)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(runner.stream)
+    e0.record(stream0)
     for _ in range(e2e_steps):
-        runner.enqueue(**hx)
-    e1.record(runner.stream)
-    runner.stream.synchronize()
+        for runner, hx in hosts:
+            if runner.stream is not stream0:
+                runner.stream.wait_stream(stream0)
+            runner.enqueue(**hx)
+            if runner.stream is not stream0:
+                stream0.wait_stream(runner.stream)
+    e1.record(stream0)
+    stream0.synchronize()
     e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], world, dev)[0]
+    h2d = sum(rn.h2d_bytes for rn, _ in hosts)
+    d2h = sum(rn.d2h_bytes for rn, _ in hosts)
 
     if rank != 0:
         return
+    clocks = m["clocks"]
     sm_mhz = clocks.get("sm_mhz") or 1900.0
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     pair_ops = PAIR_FP32_OPS[w.bc]
     alu_floor_s = w.elems * w.dstate * pair_ops / (128.0 * nsm * sm_mhz * 1e6)
+    cfg = _config(w, world, args.shard)
     line = {
-        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": {"fp32": "f32", "fp16": "f16", "bf16": "bf16"}[w.dtype],
+        "metric": METRIC, "value": r["gbs"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "strong" if args.shard else "weak",
+        "vs_baseline": None, "published": None, "published_note": PUBLISHED_NOTE,
+        "dtype": {"fp32": "f32", "fp16": "f16", "bf16": "bf16"}[w.dtype],
         "data": "synthetic (seeded, Mamba-layer shapes)",
-        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": w.dstate,
-                   "groups": w.groups, "bc": w.bc, "io_dtype": w.dtype, "z": w.has_z,
-                   "return_last_state": w.return_last_state, "parallelism": f"independent x{world}",
-                   "sequence_segmented": workspace is not None,
-                   "l2": f"flushed before every step ({2 * l2 >> 20} MiB write, outside the kernel interval)"},
-        "elems_per_s": elems,
+        "config": cfg,
+        "method": {"l2": f"flushed before every step ({m['l2_flush_mib']} MiB write, outside the kernel interval)",
+                   "sequence_segmented": m["segmented"], "launches_per_step": m["launches_per_step"],
+                   "rank0_blocks": m["blocks"]},
+        "elems_per_s": r["elems_per_s"],
         "compulsory_bytes_per_step": cb,
-        "region_ms_per_step_incl_flush": region_ms,
-        "roofline": {"bound": "hbm", "achieved": cb / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
-                     "frac": cb / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
-                     "traffic": _traffic(w.name)},
+        "region_ms_per_step_incl_flush": m["region_ms"],
+        "roofline": {"bound": "hbm", "achieved": r["gbs"] / world, "peak": peak, "unit": "GB/s",
+                     "frac": r["frac"], "peak_source": peak_src,
+                     "traffic": _traffic(w.name),
+                     "note": ("achieved = compulsory bytes of the step over the step's kernel time "
+                              f"({m['launches_per_step']} launch(es) per step on the launching stream)")},
         "alu_floor": {"fp32_lane_ops_per_pair": pair_ops, "pairs_per_step": w.elems * w.dstate,
                       "fp32_lanes_per_sm_clk": 128, "sms": nsm, "sm_mhz": sm_mhz,
                       "floor_ms": alu_floor_s * 1e3,
                       "gbs_at_floor": cb / alu_floor_s / 1e9},
-        "e2e": {"value": job_rate(cb, world, e2e_ms) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
+        "per_config": per_config,
+        "e2e": {"value": _rates(w, e2e_ms, world, args.shard, peak)["gbs"], "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
-        "gpu_launches": args.steps * launches_per_step,
+        "gpu_launches": args.steps * sum(v["launches_per_step"] for v in per_config.values()),
         "clocks": clocks,
         "kernel_hash": _kernel_hash(),
     }
@@ -473,8 +575,8 @@ def run_decode(args, rank, world, local_rank):
                    "parallelism": f"independent x{world}",
                    "l2": f"flushed before every step ({2 * l2 >> 20} MiB write, outside the kernel interval)"},
         "compulsory_bytes_per_step": cb,
-        "roofline": {"bound": "hbm", "achieved": cb / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
-                     "frac": cb / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
+        "roofline": {"bound": "hbm", "achieved": r["gbs"] / world, "peak": peak, "unit": "GB/s",
+                     "frac": r["frac"], "peak_source": peak_src,
                      "traffic": _traffic(w.name, "state_update")},
         "e2e": {"value": job_rate(cb, world, e2e_ms) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h_out.numel() * h_out.element_size(),
@@ -605,8 +707,8 @@ def run_conv(args, rank, world, local_rank):
                    "l2": f"flushed before every step ({2 * l2 >> 20} MiB write, outside the kernel interval)"},
         "elems_per_s": job_rate(w.elems, world, ms),
         "compulsory_bytes_per_step": cb,
-        "roofline": {"bound": "hbm", "achieved": cb / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
-                     "frac": cb / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
+        "roofline": {"bound": "hbm", "achieved": r["gbs"] / world, "peak": peak, "unit": "GB/s",
+                     "frac": r["frac"], "peak_source": peak_src,
                      "traffic": _traffic(w.name, "conv1d")},
         "e2e": {"value": job_rate(cb, world, e2e_ms) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": hx.numel() * hx.element_size(),
@@ -969,6 +1071,9 @@ def main():
                     choices=sorted(workloads.WORKLOADS) + sorted(workloads.DECODE_WORKLOADS)
                     + sorted(workloads.CONV_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--shard", action="store_true",
+                    help="scan only: partition ONE problem over the ranks (batch x dim, whole groups where the "
+                         "rows allow; strong scaling) instead of one independent copy per rank")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()
@@ -1003,10 +1108,10 @@ def main():
                 import torch
                 torch.distributed.destroy_process_group()
         return
-    if args.workload is None:
-        args.workload = DEFAULT_WORKLOAD
-    elif args.workload not in workloads.WORKLOADS:
+    if args.workload is not None and args.workload not in workloads.WORKLOADS:
         ap.error(f"--op {args.op} takes a scan workload")
+    if args.workload is None and (args.op != "scan" or args.impl == "reference"):
+        args.workload = DEFAULT_WORKLOAD if args.op != "scan" else HEADLINE_WORKLOAD
     if args.op in ("bwd", "complex"):
         if world > 1 and args.impl == "ours":
             import torch
