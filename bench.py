@@ -210,7 +210,7 @@ def cpu_baseline(w, x, budget_s=15.0):
 # The largest single-GPU workload is the headline line; the default run also
 # times the other full-size workloads in the same process (per_config).
 HEADLINE_WORKLOAD = "long_fixed_fp32"
-PER_CONFIG = ("mamba130m_bf16", "grouped_bf16", "mamba2p8b_fp16", "long_fixed_fp32")
+PER_CONFIG = ("mamba130m_bf16", "mamba130m_bf16_l2047", "grouped_bf16", "mamba2p8b_fp16", "long_fixed_fp32")
 PUBLISHED_NOTE = ("the pages quote no throughput, latency or hardware for this operator (the published "
                   "figures of the baseline are empty), so there is no context line to compare with")
 

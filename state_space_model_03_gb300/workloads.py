@@ -67,6 +67,10 @@ WORKLOADS = {
     "long_fixed_fp32": Workload("long_fixed_fp32", 1, 2048, 65536, 16, bc="fixed", dtype="fp32",
                                 bc_std=1.0 / 16, delta_std=0.5, has_z=False, D_mode="ones",
                                 dt_range=(0.001, 0.01), return_last_state=True, seed=4),
+    # the 130M-shaped layer on a sequence length with no 16-byte row stride (a
+    # typical prompt length): the rows cannot be described to TMA, so the
+    # forward streams them with plain loads
+    "mamba130m_bf16_l2047": Workload("mamba130m_bf16_l2047", 8, 1536, 2047, 16, dtype="bf16", seed=5),
 }
 
 

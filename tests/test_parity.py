@@ -69,7 +69,8 @@ def _sample_rows(w, k=24, seed=0):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["mamba130m_bf16", "grouped_bf16", "mamba2p8b_fp16", "long_fixed_fp32"])
+@pytest.mark.parametrize("name", ["mamba130m_bf16", "mamba130m_bf16_l2047", "grouped_bf16", "mamba2p8b_fp16",
+                                  "long_fixed_fp32"])
 def test_workload_full_size_sampled(name):
     w = workloads.WORKLOADS[name]
     x = workloads.make_inputs(w)
