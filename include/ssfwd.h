@@ -160,6 +160,16 @@ int ss_fwd(const ss_fwd_params *p, void *stream);
  * buffers. Host buffers should be pinned for the copies to be asynchronous.
  * Nothing is synchronised: host outputs are valid once `stream` completes.
  * Copy sizes are the contiguous sizes of each tensor. Returns as ss_fwd.
+ *
+ * The copies overlap the work: the problem is cut into row blocks (whole
+ * batch rows, or channel ranges of one batch row that keep groups whole), and
+ * block i's inputs travel host-to-device while block i-1 runs and block i-2's
+ * outputs travel back. The copies run on two streams internal to the library
+ * (created with a few events on the first call on each device and kept until
+ * the process exits), forked from `stream` by an event and joined back into
+ * it, so the results still complete in `stream`'s order. All blocks share
+ * p->workspace. On an error after the copies began, `stream` still waits for
+ * the copies already issued.
  */
 int ss_fwd_host(const ss_fwd_params *p,
                 const void *h_u, const void *h_delta, const void *h_z,

@@ -535,9 +535,11 @@ class HostRunner:
     """
 
     def __init__(self, u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                 delta_softplus=False, return_last_state=False, device="cuda"):
+                 delta_softplus=False, return_last_state=False, device="cuda", initial_state=None):
         lib = load_library()
         self._lib = lib
+        # an optional start state stays on the device (float32 (batch, dim, dstate))
+        self.initial_state = None if initial_state is None else _unit_last(initial_state)
         host = normalise(u, delta, A, B, C, D, z, delta_bias)
         self._host_shapes = [None if t is None else (tuple(t.shape), t.dtype) for t in host]
         dev = [None if t is None else torch.empty(t.shape, dtype=t.dtype, device=device) for t in host]
@@ -546,7 +548,7 @@ class HostRunner:
         self.out = torch.empty(du.shape, dtype=du.dtype, device=device)
         self.last = (torch.empty((du.shape[0], du.shape[1], dev[2].shape[1]), dtype=torch.float32, device=device)
                      if return_last_state else None)
-        self.params = make_params(*dev, delta_softplus, self.out, self.last)
+        self.params = make_params(*dev, delta_softplus, self.out, self.last, self.initial_state)
         self.workspace = attach_workspace(self.params, self.out.device)
         self.h_out = torch.empty(du.shape, dtype=du.dtype, pin_memory=True)
         self.h_last = (torch.empty(self.last.shape, dtype=torch.float32, pin_memory=True)

@@ -665,6 +665,119 @@ bool host_layout_ok(const ss_fwd_params *p) {
 }
 
 // ---------------------------------------------------------------------------
+// Host-staged forward (ss_fwd_host): the copies overlap the kernels
+// ---------------------------------------------------------------------------
+// The problem is cut into row blocks, each whole batch rows or a range of
+// channels inside one batch row (group-aligned for grouped B/C), so that each
+// block's u, delta, z, out and last_state are contiguous in memory. Block i's
+// inputs go host-to-device on one internal stream, its kernel runs on the
+// caller's stream, and its outputs go device-to-host on a second internal
+// stream, so the two copy directions and the kernels of neighbouring blocks
+// run at the same time. Events fork the internal streams from the caller's
+// stream and join them back, so the call keeps the caller's stream ordering.
+// The streams and events are created once per device and kept until exit.
+constexpr int kHostBlocksMax = 8;
+constexpr int64_t kHostBlockBytes = int64_t(32) << 20;  // input bytes per block, at least
+
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, in_done[kHostBlocksMax] = {}, k_done[kHostBlocksMax] = {};
+  std::mutex mu;  // one enqueue sequence at a time per device (the events are reused)
+};
+HostPipe g_pipe[kMaxDevices];
+
+HostPipe *host_pipe(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  HostPipe &hp = g_pipe[dev];
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!hp.ready) {
+    const unsigned ev = cudaEventDisableTiming;
+    bool ok = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.fork, ev) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.join, ev) == cudaSuccess;
+    for (int i = 0; ok && i < kHostBlocksMax; ++i)
+      ok = cudaEventCreateWithFlags(&hp.in_done[i], ev) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.k_done[i], ev) == cudaSuccess;
+    if (!ok) return nullptr;
+    hp.ready = true;
+  }
+  return &hp;
+}
+
+struct HostBlock {
+  int64_t b0, b1, d0, d1;
+};
+
+// Row blocks of about kHostBlockBytes of inputs each (at most kHostBlocksMax).
+int host_blocks(const ss_fwd_params *p, HostBlock *blk) {
+  const int64_t es = elem_size(p->in_dtype);
+  const int64_t in_bytes = p->batch * p->dim * p->seqlen * es * (p->z ? 3 : 2);
+  int want = static_cast<int>(std::min<int64_t>(kHostBlocksMax, std::max<int64_t>(1, in_bytes / kHostBlockBytes)));
+  if (std::getenv("SSFWD_HOST_SERIAL")) want = 1;
+  if (const char *nb = std::getenv("SSFWD_HOST_BLOCKS"))  // diagnostics: a fixed block count
+    want = std::max(1, std::min(kHostBlocksMax, std::atoi(nb)));
+  if (want <= 1 || p->batch * p->dim <= 1) {
+    blk[0] = {0, p->batch, 0, p->dim};
+    return 1;
+  }
+  int n = 0;
+  if (p->batch >= want) {  // whole batch rows
+    for (int i = 0; i < want; ++i) {
+      const int64_t a = p->batch * i / want, c = p->batch * (i + 1) / want;
+      if (c > a) blk[n++] = {a, c, 0, p->dim};
+    }
+    return n;
+  }
+  // channel ranges inside each batch row, on a unit that keeps groups whole
+  const int per_b = (want + static_cast<int>(p->batch) - 1) / static_cast<int>(p->batch);
+  const int64_t unit = (p->bc_mode == SS_BC_VARIABLE && p->ngroups > 1) ? p->dim / p->ngroups : 32;
+  const int64_t units = (p->dim + unit - 1) / unit;
+  const int parts = static_cast<int>(std::min<int64_t>(per_b, units));
+  for (int64_t b = 0; b < p->batch; ++b)
+    for (int i = 0; i < parts && n < kHostBlocksMax; ++i) {
+      const int64_t a = std::min(p->dim, units * i / parts * unit), c = std::min(p->dim, units * (i + 1) / parts * unit);
+      if (c > a) blk[n++] = {b, b + 1, a, c};
+    }
+  return n;
+}
+
+// The sub-problem of one block (device pointers offset into the full buffers).
+ss_fwd_params host_block_params(const ss_fwd_params *p, const HostBlock &k) {
+  ss_fwd_params q = *p;
+  const int64_t es = elem_size(p->in_dtype), bs = elem_size(p->bc_dtype);
+  const int64_t row0 = k.b0 * p->dim + k.d0;  // first (batch, channel) row of the block
+  auto off = [&](const void *ptr, int64_t elems, int64_t size) -> const void * {
+    return ptr ? static_cast<const char *>(ptr) + elems * size : nullptr;
+  };
+  q.batch = k.b1 - k.b0;
+  q.dim = k.d1 - k.d0;
+  q.u = off(p->u, row0 * p->seqlen, es);
+  q.delta = off(p->delta, row0 * p->seqlen, es);
+  q.z = off(p->z, row0 * p->seqlen, es);
+  q.out = const_cast<void *>(off(p->out, row0 * p->seqlen, es));
+  q.last_state = static_cast<float *>(const_cast<void *>(off(p->last_state, row0 * p->dstate, 4)));
+  q.A = static_cast<const float *>(off(p->A, k.d0 * p->A_stride[0], 4));
+  q.D = static_cast<const float *>(off(p->D, k.d0, 4));
+  q.delta_bias = static_cast<const float *>(off(p->delta_bias, k.d0, 4));
+  if (p->initial_state)
+    q.initial_state = static_cast<const float *>(
+        off(p->initial_state, k.b0 * p->initial_state_stride[0] + k.d0 * p->initial_state_stride[1], 4));
+  if (p->bc_mode == SS_BC_FIXED) {
+    q.B = off(p->B, k.d0 * p->B_stride[0], 4);
+    q.C = off(p->C, k.d0 * p->C_stride[0], 4);
+  } else {
+    const int64_t dpg = p->dim / p->ngroups;
+    const int64_t g0 = k.d0 / dpg, g1 = (k.d1 - 1) / dpg + 1;
+    q.ngroups = g1 - g0;
+    q.B = off(p->B, k.b0 * p->B_stride[0] + g0 * p->B_stride[1], bs);
+    q.C = off(p->C, k.b0 * p->C_stride[0] + g0 * p->C_stride[1], bs);
+  }
+  return q;
+}
+
+// ---------------------------------------------------------------------------
 // Decode step (ss_state_update)
 // ---------------------------------------------------------------------------
 int validate_su(const ss_state_update_params *p) {
@@ -1366,36 +1479,80 @@ int ss_fwd_host(const ss_fwd_params *p, const void *h_u, const void *h_delta, co
   if (!host_layout_ok(p)) return SS_ERR_STRIDE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t es = elem_size(p->in_dtype), bs = elem_size(p->bc_dtype);
-  const size_t n3 = static_cast<size_t>(p->batch * p->dim * p->seqlen);
   const size_t nbc = p->bc_mode == SS_BC_FIXED ? static_cast<size_t>(p->dim * p->dstate)
                                                : static_cast<size_t>(p->batch * p->ngroups * p->dstate * p->seqlen);
   struct Copy {
     void *dst;
     const void *src;
     size_t bytes;
-  } in[8] = {{const_cast<void *>(p->u), h_u, n3 * es},
-             {const_cast<void *>(p->delta), h_delta, n3 * es},
-             {const_cast<void *>(p->z), h_z, n3 * es},
-             {const_cast<void *>(p->B), h_B, nbc * bs},
-             {const_cast<void *>(p->C), h_C, nbc * bs},
-             {const_cast<float *>(p->A), h_A, static_cast<size_t>(p->dim * p->dstate) * 4},
-             {const_cast<float *>(p->D), h_D, static_cast<size_t>(p->dim) * 4},
-             {const_cast<float *>(p->delta_bias), h_delta_bias, static_cast<size_t>(p->dim) * 4}};
+  };
+  // inputs that every block reads whole: B, C, A, D, delta_bias
+  const Copy shared_in[5] = {{const_cast<void *>(p->B), h_B, nbc * bs},
+                             {const_cast<void *>(p->C), h_C, nbc * bs},
+                             {const_cast<float *>(p->A), h_A, static_cast<size_t>(p->dim * p->dstate) * 4},
+                             {const_cast<float *>(p->D), h_D, static_cast<size_t>(p->dim) * 4},
+                             {const_cast<float *>(p->delta_bias), h_delta_bias, static_cast<size_t>(p->dim) * 4}};
+  for (const Copy &c : shared_in)
+    if (c.src && c.bytes && !c.dst) return SS_ERR_NULL;
+  if (h_z && !p->z) return SS_ERR_NULL;
   if (fault_injected("h2d")) return SS_ERR_CUDA;
-  for (auto &c : in) {
-    if (!c.src || c.bytes == 0) continue;
-    if (!c.dst) return SS_ERR_NULL;
-    if (cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return SS_ERR_CUDA;
-  }
-  st = launch(p, s, p->workspace, p->workspace_bytes);
-  if (st != SS_OK) return st;
-  if (h_out && n3 && cudaMemcpyAsync(h_out, p->out, n3 * es, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  if (p->batch * p->dim == 0) return SS_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+  HostPipe *hp = host_pipe(dev);
+  if (!hp) return SS_ERR_CUDA;
+  HostBlock blk[kHostBlocksMax];
+  const int nblk = host_blocks(p, blk);
+  std::lock_guard<std::mutex> lk(hp->mu);
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // on a failure after the fork, the caller's stream still waits for whatever
+  // the copy streams already hold, so no copy outlives the call's ordering
+  auto fail = [&](int code) -> int {
+    if (ok(cudaEventRecord(hp->join, hp->in))) (void)cudaStreamWaitEvent(s, hp->join, 0);
+    if (ok(cudaEventRecord(hp->join, hp->out))) (void)cudaStreamWaitEvent(s, hp->join, 0);
+    return code;
+  };
+  // fork: the copy streams start after the work already on the caller's stream
+  if (!ok(cudaEventRecord(hp->fork, s)) || !ok(cudaStreamWaitEvent(hp->in, hp->fork, 0)) ||
+      !ok(cudaStreamWaitEvent(hp->out, hp->fork, 0)))
     return SS_ERR_CUDA;
-  if (h_last_state && p->last_state) {
-    const size_t nl = static_cast<size_t>(p->batch * p->dim * p->dstate) * 4;
-    if (nl && cudaMemcpyAsync(h_last_state, p->last_state, nl, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-      return SS_ERR_CUDA;
+  for (const Copy &c : shared_in)
+    if (c.src && c.bytes && !ok(cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, hp->in)))
+      return fail(SS_ERR_CUDA);
+  const char *hin[3] = {static_cast<const char *>(h_u), static_cast<const char *>(h_delta),
+                        static_cast<const char *>(h_z)};
+  const void *din[3] = {p->u, p->delta, p->z};
+  for (int i = 0; i < nblk; ++i) {
+    const HostBlock &k = blk[i];
+    const size_t row0 = static_cast<size_t>(k.b0 * p->dim + k.d0);
+    const size_t rows = static_cast<size_t>((k.b1 - k.b0) * (k.d1 - k.d0));
+    const size_t o = row0 * p->seqlen * es, n = rows * p->seqlen * es;
+    for (int t = 0; t < 3; ++t) {
+      if (!hin[t] || n == 0) continue;
+      if (!ok(cudaMemcpyAsync(static_cast<char *>(const_cast<void *>(din[t])) + o, hin[t] + o, n,
+                              cudaMemcpyHostToDevice, hp->in)))
+        return fail(SS_ERR_CUDA);
+    }
+    if (!ok(cudaEventRecord(hp->in_done[i], hp->in)) || !ok(cudaStreamWaitEvent(s, hp->in_done[i], 0)))
+      return fail(SS_ERR_CUDA);
+    const ss_fwd_params q = host_block_params(p, k);
+    st = launch(&q, s, p->workspace, p->workspace_bytes);
+    if (st != SS_OK) return fail(st);
+    if (!ok(cudaEventRecord(hp->k_done[i], s)) || !ok(cudaStreamWaitEvent(hp->out, hp->k_done[i], 0)))
+      return fail(SS_ERR_CUDA);
+    if (h_out && n && !ok(cudaMemcpyAsync(static_cast<char *>(h_out) + o, static_cast<const char *>(p->out) + o, n,
+                                          cudaMemcpyDeviceToHost, hp->out)))
+      return fail(SS_ERR_CUDA);
+    if (h_last_state && p->last_state) {
+      const size_t lo = row0 * p->dstate * 4, ln = rows * p->dstate * 4;
+      if (ln && !ok(cudaMemcpyAsync(reinterpret_cast<char *>(h_last_state) + lo,
+                                    reinterpret_cast<const char *>(p->last_state) + lo, ln, cudaMemcpyDeviceToHost,
+                                    hp->out)))
+        return fail(SS_ERR_CUDA);
+    }
   }
+  // join: the caller's stream completes after the last copy back
+  if (!ok(cudaEventRecord(hp->join, hp->out)) || !ok(cudaStreamWaitEvent(s, hp->join, 0))) return SS_ERR_CUDA;
   return SS_OK;
 }
 

@@ -190,6 +190,40 @@ def test_host_entry_point_matches_device():
         assert torch.equal(ho, out.cpu()) and torch.equal(hl, last.cpu())
 
 
+@pytest.mark.parametrize("w", [
+    # about 100 MB of inputs: three blocks of whole batch rows
+    workloads.Workload("host_batches", 4, 1024, 4096, 16, dtype="bf16", return_last_state=True, seed=22),
+    # one batch row: four blocks of 512 channels (fixed B/C, one lane per channel, segments per block)
+    workloads.Workload("host_channels", 1, 2048, 8192, 16, bc="fixed", dtype="fp32", has_z=False,
+                       bc_std=1.0 / 16, dt_range=(0.001, 0.01), return_last_state=True, seed=23),
+    # two batch rows of four groups: channel blocks that keep groups whole
+    workloads.Workload("host_groups", 2, 1024, 8192, 16, groups=4, bc_4d=True, dtype="bf16",
+                       return_last_state=True, seed=24),
+], ids=lambda w: w.name)
+def test_host_entry_point_overlapped_blocks(w, monkeypatch):
+    """ss_fwd_host cuts large problems into row blocks whose copies overlap the
+    kernels of their neighbours; the result matches the device path (and the
+    serial single-block schedule) within the tolerance, start state included."""
+    x = workloads.make_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 9)
+    x0 = torch.randn(w.batch, w.dim, w.dstate, generator=g)
+    dev = _to_dev(x)
+    ref_out, ref_last = api.selective_scan_fn(**dev, delta_softplus=True, return_last_state=True,
+                                              initial_state=x0.cuda())
+    torch.cuda.synchronize()
+    hx = {k: (None if x[k] is None else x[k].pin_memory()) for k in NAMES}
+    tol = TOL[w.dtype]
+    for serial in (False, True):
+        if serial:
+            monkeypatch.setenv("SSFWD_HOST_SERIAL", "1")
+        r = api.HostRunner(**hx, delta_softplus=True, return_last_state=True, initial_state=x0.cuda())
+        for _ in range(2):
+            ho, hl = r.run(**hx)
+            assert api.device_error() == 0
+            assert float((ho.float() - ref_out.cpu().float()).abs().max()) <= tol * float(ref_out.float().abs().max())
+            assert float((hl - ref_last.cpu()).abs().max()) <= tol * float(ref_last.abs().max())
+
+
 def test_seqlen_zero_and_empty():
     w = workloads.Workload("e", 2, 8, 5, 4, dtype="fp32", return_last_state=True, seed=2)
     x = workloads.make_inputs(w)
