@@ -73,7 +73,7 @@ __device__ __forceinline__ void sincos_rr(float th, float lo, float &sn, float &
 // The step of the complex path. A rotation of dt Im A radians per step turns
 // a relative error of dt into a phase error that grows with |Im A|, so fp32
 // inputs take softplus from the library exponential and log1p (each within a
-// few ulps, against ~3e-6 for the MUFU form the real forward uses). 16-bit
+// few ulps, against ~5e-7 for the one-MUFU form the real forward uses). 16-bit
 // inputs, whose outputs are rounded to 8 or 11 bits, keep the MUFU form.
 template <typename T>
 __device__ __forceinline__ float softplus_cx(float v) {

@@ -45,7 +45,7 @@ struct LaneCfg {
 };
 
 template <typename T, int NS, bool SUMMARY, bool GEN>
-__global__ void __launch_bounds__(32, 16)
+__global__ void __launch_bounds__(32, 12)
 ss_fwd_lane_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tm_u,
                    const __grid_constant__ CUtensorMap tm_dl, const __grid_constant__ CUtensorMap tm_z) {
   using CF = LaneCfg<T>;
