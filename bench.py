@@ -70,10 +70,10 @@ def _peaks():
 KERNEL_SOURCES = {
     "scan": ("ss_fwd_kernel.cuh", "ss_fwd_instances.cuh", "ss_fwd_f32.cu", "ss_fwd_f16.cu", "ss_fwd_bf16.cu",
              "ss_fwd_lane.cu"),
-    "state_update": ("ss_state_update.cu",),
-    "conv1d": ("ss_conv1d.cu",),
-    "bwd": ("ss_bwd.cu",),
-    "complex": ("ss_fwd_complex.cu",),
+    "state_update": ("ss_state_update.cu", "ss_fwd_kernel.cuh"),
+    "conv1d": ("ss_conv1d.cu", "ss_fwd_kernel.cuh"),
+    "bwd": ("ss_bwd.cu", "ss_fwd_kernel.cuh"),
+    "complex": ("ss_fwd_complex.cu", "ss_fwd_kernel.cuh"),
 }
 
 
@@ -575,8 +575,8 @@ def run_decode(args, rank, world, local_rank):
                    "parallelism": f"independent x{world}",
                    "l2": f"flushed before every step ({2 * l2 >> 20} MiB write, outside the kernel interval)"},
         "compulsory_bytes_per_step": cb,
-        "roofline": {"bound": "hbm", "achieved": r["gbs"] / world, "peak": peak, "unit": "GB/s",
-                     "frac": r["frac"], "peak_source": peak_src,
+        "roofline": {"bound": "hbm", "achieved": cb / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": cb / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
                      "traffic": _traffic(w.name, "state_update")},
         "e2e": {"value": job_rate(cb, world, e2e_ms) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h_out.numel() * h_out.element_size(),
@@ -707,8 +707,8 @@ def run_conv(args, rank, world, local_rank):
                    "l2": f"flushed before every step ({2 * l2 >> 20} MiB write, outside the kernel interval)"},
         "elems_per_s": job_rate(w.elems, world, ms),
         "compulsory_bytes_per_step": cb,
-        "roofline": {"bound": "hbm", "achieved": r["gbs"] / world, "peak": peak, "unit": "GB/s",
-                     "frac": r["frac"], "peak_source": peak_src,
+        "roofline": {"bound": "hbm", "achieved": cb / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": cb / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
                      "traffic": _traffic(w.name, "conv1d")},
         "e2e": {"value": job_rate(cb, world, e2e_ms) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": hx.numel() * hx.element_size(),
