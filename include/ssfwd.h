@@ -86,6 +86,11 @@ typedef enum ss_status {
  *
  * Sizes: batch, dim, seqlen >= 0; 1 <= dstate <= 64. batch*dim*seqlen == 0 is
  * a no-op (except the zero fill of last_state when seqlen == 0).
+ *
+ * Memory touched: the call may read any byte between the first and the last
+ * element of u, delta, z, B and C (the gaps of a strided layout included:
+ * rows whose start is not 16-byte aligned are read as the aligned 16-byte
+ * blocks that cover them); it writes only the elements of out and last_state.
  */
 typedef struct ss_fwd_params {
   int32_t abi_version;      /* must be SS_ABI_VERSION */

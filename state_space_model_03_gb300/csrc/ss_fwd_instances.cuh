@@ -13,7 +13,7 @@ namespace reg {
 
 template <typename T, int NP, int K, bool FIXED, bool BCF32, bool TMA, bool SUMMARY, int SUB, int CHN = 32>
 KernelInfo info() {
-  using CF = Cfg<T, NP, K, FIXED, BCF32, SUB, CHN>;
+  using CF = Cfg<T, NP, K, FIXED, BCF32, SUB, CHN, !TMA>;
   return KernelInfo{reinterpret_cast<const void *>(&ss_fwd_kernel<T, NP, K, FIXED, BCF32, TMA, SUMMARY, SUB, CHN>),
                     CF::SMEM_ALLOC, CF::THREADS, CF::CH, CF::L};
 }

@@ -100,6 +100,7 @@ struct KParams {
   int32_t *err;
   uint32_t wait_limit;  // try_wait calls before a wait gives up (kMaxWaitIters in production)
   int stall_chunk;      // test hook: chunk the producer never issues (-1: none)
+  int rows_bulk;        // producer without TMA: stage rows by bulk copies (else plain loads)
 };
 
 // ----------------------------------------------------------------------------
@@ -287,6 +288,33 @@ __device__ __forceinline__ int swz(int row, int byte) {
   return row * 128 + ((((byte >> 4) ^ row) & 7) << 4) + (byte & 15);
 }
 
+// The 16 bytes at byte offset o (0..15) of the 32 bytes a:b (little-endian
+// words), without indexing registers at run time: whole words by two
+// selects, then the byte shift by funnel shifts.
+__device__ __forceinline__ uint4 bytes_at(uint4 a, uint4 b, int o) {
+  const uint32_t x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const int k = o >> 2;
+  uint32_t c[6], d[5];
+#pragma unroll
+  for (int i = 0; i < 6; ++i) c[i] = (k & 2) ? x[i + 2] : x[i];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) d[i] = (k & 1) ? c[i + 1] : c[i];
+  const uint32_t sh = static_cast<uint32_t>(o & 3) * 8u;
+  return make_uint4(__funnelshift_r(d[0], d[1], sh), __funnelshift_r(d[1], d[2], sh),
+                    __funnelshift_r(d[2], d[3], sh), __funnelshift_r(d[3], d[4], sh));
+}
+
+// v (bytes p0 .. p0+15 of a row) with the bytes at positions >= nb cleared.
+__device__ __forceinline__ uint4 keep_below(uint4 v, int p0, int nb) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = nb - (p0 + 4 * i);  // valid bytes of word i
+    w[i] = q >= 4 ? w[i] : (q <= 0 ? 0u : (w[i] & ((1u << (8 * q)) - 1u)));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // N consecutive elements (row, col .. col+N-1) of a 128B-swizzled tile of T,
 // widened to fp32. Pieces of up to 16 bytes each lie inside one 16-byte chunk
 // (col * sizeof(T) is a multiple of the piece size), so each is one vector LDS.
@@ -353,10 +381,43 @@ __device__ __forceinline__ void stg_row(T *dst, const float (&v)[N], bool vec, i
   }
 }
 
+// N consecutive elements (col .. col+N-1) of a row held as its covering
+// 16-byte blocks, the row's byte k at row + o + k (o < 16), widened to fp32.
+// col * sizeof(T) and N * sizeof(T) are multiples of 16.
+template <typename T, int N>
+__device__ __forceinline__ void lds_row_off(const unsigned char *row, int col, int o, float (&v)[N]) {
+  constexpr int BYTES = N * (int)sizeof(T);
+  constexpr int PE = 16 / (int)sizeof(T);
+  static_assert(BYTES % 16 == 0, "whole 16-byte pieces");
+  const unsigned char *ptr = row + col * (int)sizeof(T);
+  uint4 prev = *reinterpret_cast<const uint4 *>(ptr);
+#pragma unroll
+  for (int q = 0; q < BYTES / 16; ++q) {
+    const uint4 next = *reinterpret_cast<const uint4 *>(ptr + 16 * (q + 1));
+    const uint4 r = bytes_at(prev, next, o);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (sizeof(T) == 4) {
+        v[q * PE + i] = __uint_as_float(w[i]);
+      } else {
+        const float2 f = unpack2<T>(w[i]);
+        v[q * PE + 2 * i] = f.x;
+        v[q * PE + 2 * i + 1] = f.y;
+      }
+    }
+    prev = next;
+  }
+}
+
 // ----------------------------------------------------------------------------
 // Configuration
 // ----------------------------------------------------------------------------
-template <typename T, int NP, int K, bool FIXED, bool BCF32, int SUB = 16, int CHN = 32>
+// GEN: the producer without TMA (rows TMA cannot describe), whose u / delta /
+// z tiles hold each row as the 16-byte blocks that cover it (144 bytes a row,
+// row byte k at offset (row address & 15) + k), plus a staging buffer for
+// B/C rows.
+template <typename T, int NP, int K, bool FIXED, bool BCF32, int SUB = 16, int CHN = 32, bool GEN = false>
 struct Cfg {
   using BCT = typename std::conditional<BCF32, float, T>::type;  // stored B/C type (variable B/C)
   static constexpr int TN = NP / K;              // scan lanes per channel
@@ -386,7 +447,8 @@ struct Cfg {
   static_assert(CPL == 1 || CPL == 2, "one or two channels per scan lane");
   static_assert(CPW <= CH && CH % CPW == 0, "scan warps tile the CTA's channels");
   // shared memory map (bytes); TMA tiles are 1024-aligned for the 128B swizzle
-  static constexpr int TILE = CH * 128;                          // u / delta / z tile
+  static constexpr int ROWB = GEN ? 144 : 128;                    // bytes of a u / delta / z tile row
+  static constexpr int TILE = CH * ROWB;                         // u / delta / z tile
   static constexpr int BC_ROW = L * (int)sizeof(BCT);             // bytes of one raw B/C row
   static constexpr int BCMAX = (NP * BC_ROW + 1023) / 1024 * 1024;  // raw B or C tile
   static constexpr int OFF_U = 0;
@@ -415,7 +477,18 @@ struct Cfg {
   static constexpr int Y_SLOT = S * CH * TN * 4;                  // partial y [S][CH*TN]
   static constexpr int OFF_BAR = OFF_Y + NSLOT * Y_SLOT;
   static constexpr int NBAR = 2 * STAGES + 4 * NSLOT;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8;
+  // GEN: staging for 32 B/C row pieces of 128 bytes (144 with their covering
+  // blocks; variable B/C) and, when the producer does not convert B/C, for the
+  // chunk's outputs when out rows are not 16-byte aligned (row r's byte k at
+  // (out row address & 15) + k), with its full / empty barriers. (A second
+  // output buffer does not fit beside three CTAs per SM; two half-chunk
+  // buffers measured slower: twice the ragged row ends to write.)
+  static constexpr int STG_SLOT = 144;
+  static constexpr bool OSTAGE = GEN && !PPACK && !FIXED;  // (fixed B/C keep four CTAs per SM)
+  static constexpr int OFF_STG = (OFF_BAR + NBAR * 8 + 127) / 128 * 128;
+  static constexpr int OFF_OUT = OFF_STG + (FIXED ? 0 : 32 * STG_SLOT);
+  static constexpr int OFF_OBAR = OFF_OUT + (OSTAGE ? CH * STG_SLOT : 0);
+  static constexpr int SMEM = GEN ? OFF_OBAR + (OSTAGE ? 16 : 0) : OFF_BAR + NBAR * 8;
   static constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024
   // CTAs per SM the shared memory allows (228 KB per SM, 1 KB reserved per CTA);
   // passed to __launch_bounds__ so the register budget matches that occupancy.
@@ -433,13 +506,13 @@ struct Cfg {
 // twice the hand-offs; the host picks it only when that occupancy is needed.
 // CHN: channels per CTA; 16 gives twice the CTAs for a finer spread over SMs.
 template <typename T, int NP, int K, bool FIXED, bool BCF32, bool USE_TMA, bool SUMMARY, int SUB = 16, int CHN = 32>
-__global__ void __launch_bounds__(Cfg<T, NP, K, FIXED, BCF32, SUB, CHN>::THREADS,
-                                  Cfg<T, NP, K, FIXED, BCF32, SUB, CHN>::MINB)
+__global__ void __launch_bounds__(Cfg<T, NP, K, FIXED, BCF32, SUB, CHN, !USE_TMA>::THREADS,
+                                  Cfg<T, NP, K, FIXED, BCF32, SUB, CHN, !USE_TMA>::MINB)
 ss_fwd_kernel(const __grid_constant__ KParams p,
               const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
               const __grid_constant__ CUtensorMap tm_C) {
-  using CF = Cfg<T, NP, K, FIXED, BCF32, SUB, CHN>;
+  using CF = Cfg<T, NP, K, FIXED, BCF32, SUB, CHN, !USE_TMA>;
   using BCT = typename CF::BCT;
   constexpr int TN = CF::TN, CPW = CF::CPW, CPL = CF::CPL, CH = CF::CH, L = CF::L, S = CF::S, SUBS = CF::SUBS;
   constexpr int STAGES = CF::STAGES, WS = CF::WS, WE = CF::WE, EPT = CF::EPT;
@@ -486,6 +559,10 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       // a stage is released by the element warps and, when it converts the
       // B/C tiles, by the producer (so it cannot refill a stage it still reads)
       mbar_init(&bar_empty[s], WE + (CF::PPACK ? 1 : 0));
+    }
+    if constexpr (CF::OSTAGE) {
+      mbar_init(reinterpret_cast<uint64_t *>(smem + CF::OFF_OBAR), WE);     // outputs of a chunk staged
+      mbar_init(reinterpret_cast<uint64_t *>(smem + CF::OFF_OBAR) + 1, 1);  // staging free again
     }
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&bar_pfull[s], WE + (CF::PPACK ? 1 : 0));
@@ -589,8 +666,147 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
 
     constexpr bool bc_swz = (bc_row == 128);
     const int nrow_bc = p.dstate;
-    auto issue = [&](int ci) -> void {
-      if (ci == p.stall_chunk) return;  // test hook: this chunk never lands
+
+    // Producer without TMA (rows TMA cannot describe). Lane l's u, delta (and
+    // z) rows of the chunk (channel d0 + l) land in tile row l as the 16-byte
+    // blocks that cover them, by 16-byte asynchronous copies: row byte k at
+    // (row address & 15) + k, which the element warps read with that offset.
+    // B/C rows, read by the B/C conversion, are staged the same way, 32 row
+    // pieces of 128 bytes at a time, and shifted into their tiles with the
+    // bytes past the sequence's end cleared. Blocks are read only between a
+    // tensor's first and last byte: a row at either end of a tensor loads the
+    // bytes of a block left out itself.
+    unsigned char *stg = smem + CF::OFF_STG + lane * CF::STG_SLOT;  // this lane's B/C staging slot
+    const int nuz = (p.has_z && !SUMMARY) ? 3 : 2;
+    constexpr int PPR = bc_row / 128 > 0 ? bc_row / 128 : 1;  // 128-byte pieces per B/C row
+    constexpr int EPP = 128 / bcs;                          // B/C elements per piece
+    const int npc = FIXED ? 0 : nrow_bc * PPR;              // pieces per B/C tensor
+    const int dl = d0 + lane, dcl = min(dl, p.dim - 1);
+    const bool row_ok = dl < p.dim;
+    auto tspan = [&](const void *base, long long ext) -> uintptr_t {
+      return reinterpret_cast<uintptr_t>(base) + static_cast<uintptr_t>(ext);
+    };
+    const unsigned char *rp_u = static_cast<const unsigned char *>(p.u) + (b * p.su[0] + dcl * p.su[1]) * (long long)sizeof(T);
+    const unsigned char *rp_d =
+        static_cast<const unsigned char *>(p.delta) + (b * p.sd[0] + dcl * p.sd[1]) * (long long)sizeof(T);
+    const unsigned char *rp_z =
+        nuz == 3 ? static_cast<const unsigned char *>(p.z) + (b * p.sz[0] + dcl * p.sz[1]) * (long long)sizeof(T) : rp_u;
+    const uintptr_t hi_u = tspan(p.u, ((p.batch - 1) * p.su[0] + (p.dim - 1) * p.su[1] + seqlen) * (long long)sizeof(T));
+    const uintptr_t hi_d =
+        tspan(p.delta, ((p.batch - 1) * p.sd[0] + (p.dim - 1) * p.sd[1] + seqlen) * (long long)sizeof(T));
+    const uintptr_t hi_z =
+        nuz == 3 ? tspan(p.z, ((p.batch - 1) * p.sz[0] + (p.dim - 1) * p.sz[1] + seqlen) * (long long)sizeof(T)) : hi_u;
+    const uintptr_t hi_B =
+        FIXED ? 0 : tspan(p.B, ((p.batch - 1) * p.sB[0] + (p.ngroups - 1) * p.sB[1] + (nrow_bc - 1) * p.sB[2] + seqlen) * (long long)bcs);
+    const uintptr_t hi_C =
+        FIXED ? 0 : tspan(p.C, ((p.batch - 1) * p.sC[0] + (p.ngroups - 1) * p.sC[1] + (nrow_bc - 1) * p.sC[2] + seqlen) * (long long)bcs);
+    // the covering blocks of the nb bytes at src that lie inside [lo, hi), to dst
+    auto copy_piece = [&](const unsigned char *src, int nb, uintptr_t lo, uintptr_t hi, unsigned char *dst) {
+      if (nb <= 0) return;
+      const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+      const uintptr_t c0 = a & ~uintptr_t(15), c1 = (a + nb + 15) & ~uintptr_t(15);
+      const int nblk = static_cast<int>((c1 - c0) >> 4);
+      const int first = c0 < lo ? 1 : 0, last = c1 > hi ? nblk - 1 : nblk;
+      for (int m = first; m < last; ++m)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + 16 * m)),
+                     "l"(reinterpret_cast<const void *>(c0 + 16 * m)) : "memory");
+    };
+    // once the copies have landed: the piece's bytes in blocks left out
+    auto patch_piece = [&](const unsigned char *src, int nb, uintptr_t lo, uintptr_t hi, unsigned char *dst) {
+      if (nb <= 0) return;
+      const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+      const uintptr_t c0 = a & ~uintptr_t(15), c1 = (a + nb + 15) & ~uintptr_t(15);
+      if (c0 >= lo && c1 <= hi) return;
+      const int o = static_cast<int>(a & 15), nblk = static_cast<int>((c1 - c0) >> 4);
+      const int first = c0 < lo ? 1 : 0, last = c1 > hi ? nblk - 1 : nblk;
+      for (int e = 0; e < nb; e += 2) {  // two bytes at a time: elements are at least 2-byte aligned
+        const int m = (o + e) >> 4;
+        if (m < first || m >= last) *reinterpret_cast<uint16_t *>(dst + o + e) = *reinterpret_cast<const uint16_t *>(src + e);
+      }
+    };
+    // the copies of chunk ci (u, delta, z rows and the first B/C batch) ...
+    auto stage_begin = [&](int ci) {
+      const int t0 = tseg0 + ci * L, s = ci % STAGES;
+      const int nbr = row_ok ? min(L, seqlen - t0) * (int)sizeof(T) : 0;
+      const long long tb = (long long)t0 * (long long)sizeof(T);
+      copy_piece(rp_u + tb, nbr, reinterpret_cast<uintptr_t>(p.u), hi_u, smem + CF::OFF_U + s * CF::TILE + lane * CF::ROWB);
+      copy_piece(rp_d + tb, nbr, reinterpret_cast<uintptr_t>(p.delta), hi_d,
+                 smem + CF::OFF_DL + s * CF::TILE + lane * CF::ROWB);
+      if (nuz == 3)
+        copy_piece(rp_z + tb, nbr, reinterpret_cast<uintptr_t>(p.z), hi_z, smem + CF::OFF_Z + s * CF::TILE + lane * CF::ROWB);
+    };
+    // B/C piece pb + lane of chunk ci: pieces 0 .. npc-1 of B, then of C
+    auto bc_piece = [&](int ci, int i, const unsigned char *&src, int &nb, uintptr_t &lo, uintptr_t &hi, int &tensor, int &n,
+                        int &h) -> bool {
+      const int t0 = tseg0 + ci * L;
+      tensor = i >= npc ? 1 : 0;
+      const int ii = i - tensor * npc;
+      n = ii / PPR;
+      h = ii - n * PPR;
+      if (i >= 2 * npc) return false;
+      const long long s0 = tensor ? p.sC[0] : p.sB[0], s1 = tensor ? p.sC[1] : p.sB[1];
+      const long long s2 = tensor ? p.sC[2] : p.sB[2];
+      const void *base = tensor ? p.C : p.B;
+      src = static_cast<const unsigned char *>(base) + (b * s0 + g * s1 + n * s2 + t0 + h * EPP) * (long long)bcs;
+      nb = max(0, min(EPP, seqlen - t0 - h * EPP)) * bcs;
+      lo = reinterpret_cast<uintptr_t>(base);
+      hi = tensor ? hi_C : hi_B;
+      return true;
+    };
+    auto bc_copy = [&](int ci, int pb) {
+      const unsigned char *src;
+      int nb, tensor, n, h;
+      uintptr_t lo, hi;
+      if (bc_piece(ci, pb + lane, src, nb, lo, hi, tensor, n, h)) copy_piece(src, nb, lo, hi, stg);
+    };
+    // ... and, once they have landed, the patches and the B/C shifts
+    auto stage_end = [&](int ci) {
+      const int t0 = tseg0 + ci * L, s = ci % STAGES;
+      const int nbr = row_ok ? min(L, seqlen - t0) * (int)sizeof(T) : 0;
+      const long long tb = (long long)t0 * (long long)sizeof(T);
+      for (int pb = 0;; pb += 32) {
+        if (pb > 0) bc_copy(ci, pb);
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (pb == 0) {
+          patch_piece(rp_u + tb, nbr, reinterpret_cast<uintptr_t>(p.u), hi_u, smem + CF::OFF_U + s * CF::TILE + lane * CF::ROWB);
+          patch_piece(rp_d + tb, nbr, reinterpret_cast<uintptr_t>(p.delta), hi_d,
+                      smem + CF::OFF_DL + s * CF::TILE + lane * CF::ROWB);
+          if (nuz == 3)
+            patch_piece(rp_z + tb, nbr, reinterpret_cast<uintptr_t>(p.z), hi_z,
+                        smem + CF::OFF_Z + s * CF::TILE + lane * CF::ROWB);
+        }
+        const unsigned char *src;
+        int nb, tensor, n, h;
+        uintptr_t lo, hi;
+        if (bc_piece(ci, pb + lane, src, nb, lo, hi, tensor, n, h)) {
+          patch_piece(src, nb, lo, hi, stg);
+          // shift the piece into its tile: swizzled 128-byte rows, or the
+          // piece's own 128 bytes of a longer linear row
+          unsigned char *tl = smem + (tensor ? CF::OFF_CR : CF::OFF_BR) + s * CF::BCMAX;
+          const int o = static_cast<int>(reinterpret_cast<uintptr_t>(src) & 15);
+          uint4 prev = *reinterpret_cast<const uint4 *>(stg);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 next = *reinterpret_cast<const uint4 *>(stg + 16 * (j + 1));
+            uint4 v = bytes_at(prev, next, o);
+            if (nb < 128) v = keep_below(v, 16 * j, nb);
+            *reinterpret_cast<uint4 *>(bc_swz ? tl + swz(n, 16 * j) : tl + n * bc_row + h * 128 + 16 * j) = v;
+            prev = next;
+          }
+        }
+        if (pb + 32 >= 2 * npc) break;
+      }
+    };
+    auto stage_rows = [&](int ci) -> bool {
+      stage_begin(ci);
+      bc_copy(ci, 0);
+      stage_end(ci);
+      return true;
+    };
+    (void)stage_rows;
+
+    auto issue = [&](int ci) -> bool {
+      if (ci == p.stall_chunk) return true;  // test hook: this chunk never lands
       const int s = ci % STAGES;
       const int t0 = tseg0 + ci * L;
       unsigned char *su = smem + CF::OFF_U + s * CF::TILE;
@@ -612,15 +828,15 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
             tma_load_4d(scr, &tm_C, &bar_full[s], t0, 0, g, b);
           }
         }
+      } else if (p.rows_bulk) {
+        if (!stage_rows(ci)) return false;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_full[s]);
       } else {
-        // Generic path (rows TMA cannot describe): plain loads into the same
-        // (swizzled) layouts. A warp's 32 lanes read 32 consecutive steps of one
-        // row (coalesced), and each lane issues NB loads per tensor before any
-        // of their shared-memory stores, so their latencies overlap. Measured on
-        // the 130M-shaped layer with 2047 steps: 850 us one element at a time,
-        // 494 us with NB = 8, 473 us with NB = 16; whole-row copies across the
-        // warp (aligned words realigned in registers, or two half-word loads
-        // per lane) measured 1600-2150 us and are not used.
+        // Plain loads (the comparison path, SSFWD_NO_BULK) into the same
+        // layouts: a warp's 32 lanes read 32 consecutive steps of one row
+        // (coalesced), each lane issuing NB loads per tensor before any of
+        // their shared-memory stores, so their latencies overlap.
         constexpr int NB = 16;
         const T *gu = static_cast<const T *>(p.u);
         const T *gd = static_cast<const T *>(p.delta);
@@ -644,10 +860,17 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
             const int i = base + k * 32 + lane;
             if (i >= CH * L) break;
             const int r = i / L, t = i - r * L;
-            const int off = swz(r, t * (int)sizeof(T));
-            *reinterpret_cast<T *>(su + off) = vu[k];
-            *reinterpret_cast<T *>(sd + off) = vd[k];
-            if (ldz) *reinterpret_cast<T *>(sz + off) = vz[k];
+            // row r's byte k at (chunk start address & 15) + k
+            const long long dr = min(d0 + r, p.dim - 1);
+            const int ou = static_cast<int>(reinterpret_cast<uintptr_t>(gu + b * p.su[0] + dr * p.su[1] + t0) & 15);
+            const int od = static_cast<int>(reinterpret_cast<uintptr_t>(gd + b * p.sd[0] + dr * p.sd[1] + t0) & 15);
+            const int row = r * CF::ROWB + t * (int)sizeof(T);
+            *reinterpret_cast<T *>(su + row + ou) = vu[k];
+            *reinterpret_cast<T *>(sd + row + od) = vd[k];
+            if (ldz) {
+              const int oz = static_cast<int>(reinterpret_cast<uintptr_t>(gz + b * p.sz[0] + dr * p.sz[1] + t0) & 15);
+              *reinterpret_cast<T *>(sz + row + oz) = vz[k];
+            }
           }
         }
         if (!FIXED) {
@@ -679,6 +902,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_full[s]);
       }
+      return true;
     };
     int issued = 0;
     bool ok = true;
@@ -687,8 +911,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       const int prev = issued - STAGES;  // chunk that last used this stage
       if (prev >= 0 && !mbar_wait(&bar_empty[prev % STAGES], (prev / STAGES) & 1, p.err, kErrWaitEmpty, p.wait_limit))
         return false;
-      issue(issued++);
-      return true;
+      return issue(issued++);
     };
     if constexpr (CF::PPACK) {
       // per sub-chunk: make sure its chunk is issued, issue further chunks
@@ -698,7 +921,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         while (ok && issued <= ci) ok = issue_next();
         while (ok && issued < nchunks &&
                (issued < STAGES || mbar_test(&bar_empty[(issued - STAGES) % STAGES], ((issued - STAGES) / STAGES) & 1)))
-          issue(issued++);
+          ok = issue(issued++);
         if (!ok) break;
         if (!mbar_wait(&bar_full[ci % STAGES], (ci / STAGES) & 1, p.err, kErrWaitFull, p.wait_limit) ||
             (q >= NSLOT && !mbar_wait(&bar_pempty[slot], ((q / NSLOT) - 1) & 1, p.err, kErrWaitEmpty, p.wait_limit))) {
@@ -713,11 +936,74 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         }
       }
       while (ok && issued < nchunks) ok = issue_next();
+    } else if (CF::OSTAGE && !SUMMARY && !p.out_vec) {
+      // outputs staged in shared memory: once the element warps have staged
+      // chunk c, lane r writes out row r's steps of it: the 16-byte-aligned
+      // interior by a bulk copy, the ragged ends (under 16 bytes each) by
+      // two-byte stores; only rows of this CTA's group and steps of this
+      // segment are written. Then the stage of chunk c is refilled.
+      uint64_t *bar_ofull = reinterpret_cast<uint64_t *>(smem + CF::OFF_OBAR), *bar_oempty = bar_ofull + 1;
+      const int rr = d0 + lane;
+      const bool out_ok = tile * CH + lane < p.dpg && rr < p.dim;
+      unsigned char *ost = smem + CF::OFF_OUT + lane * CF::STG_SLOT;
+      const unsigned char *orow =
+          reinterpret_cast<const unsigned char *>(static_cast<T *>(p.out) + b * p.so[0] + (long long)min(rr, p.dim - 1) * p.so[1]);
+      auto store_out = [&](int c) -> bool {
+        if (!mbar_wait(bar_ofull, c & 1, p.err, kErrWaitReady, p.wait_limit)) return false;
+        const int t0 = tseg0 + c * L;
+        const int nb = out_ok ? min(L, tseg1 - t0) * (int)sizeof(T) : 0;
+        unsigned char *dst = const_cast<unsigned char *>(orow) + (long long)t0 * (long long)sizeof(T);
+        const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+        const int o = static_cast<int>(a & 15);
+        const uintptr_t a0 = (a + 15) & ~uintptr_t(15), a1 = (a + nb) & ~uintptr_t(15);
+        const int inner = (nb > 0 && a1 > a0) ? static_cast<int>(a1 - a0) : 0;
+        if (inner) {
+          asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(a0),
+                       "r"(smem_u32(ost + o + (a0 - a))), "r"(inner) : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        const int head = inner ? static_cast<int>(a0 - a) : nb, tail0 = inner ? static_cast<int>(a1 - a) : nb;
+        for (int e = 0; e < head; e += 2)  // elements are at least 2-byte aligned
+          *reinterpret_cast<uint16_t *>(dst + e) = *reinterpret_cast<const uint16_t *>(ost + o + e);
+        for (int e = tail0; e < nb; e += 2)
+          *reinterpret_cast<uint16_t *>(dst + e) = *reinterpret_cast<const uint16_t *>(ost + o + e);
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the staging has been read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_oempty);
+        return true;
+      };
+      while (ok && issued < nchunks && issued < STAGES) ok = issue_next();
+      for (int c = 0; ok && c < nchunks; ++c) {
+        // chunk c's stage and staged outputs are released together: start
+        // the copies of the chunk that refills the stage, write the outputs
+        // back while they are in flight, then finish the stage
+        const int nx = issued;
+        const bool more = nx < nchunks;
+        if (more && !mbar_wait(&bar_empty[c % STAGES], (c / STAGES) & 1, p.err, kErrWaitEmpty, p.wait_limit)) {
+          ok = false;
+          break;
+        }
+        const bool copy = more && nx != p.stall_chunk;  // test hook: that chunk never lands
+        if (copy) {
+          stage_begin(nx);
+          bc_copy(nx, 0);
+        }
+        ok = store_out(c);
+        if (copy) {
+          stage_end(nx);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_full[nx % STAGES]);
+        }
+        if (more) ++issued;
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");            // no copy still in flight
+      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // every bulk store has completed
     } else {
       while (ok && issued < nchunks) ok = issue_next();
     }
-    if (!ok) {
+    if (USE_TMA && !ok) {
       // give copies already in flight a bounded chance to land before exiting
+      // (the generic producer has none left: stage_rows waits for its own)
       for (int ci = (issued > STAGES ? issued - STAGES : 0); ci < issued; ++ci)
         (void)mbar_wait(&bar_full[ci % STAGES], (ci / STAGES) & 1, p.err, kErrWaitFull, p.wait_limit);
     }
@@ -741,6 +1027,23 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     const float Dd = p.has_D ? p.D[d] : 0.f;
     const float bias = p.has_bias ? p.bias[d] : 0.f;
     const int softplus = p.softplus, has_z = p.has_z;
+    // rows without TMA: this channel's row byte offset in the u / delta / z
+    // tiles (the same for every chunk: chunks are 128 bytes apart)
+    auto row_off = [&](const void *base, const long long *st) -> int {
+      if constexpr (USE_TMA) return 0;
+      return static_cast<int>(
+          reinterpret_cast<uintptr_t>(static_cast<const T *>(base) + b * st[0] + (long long)d * st[1] + tseg0) & 15);
+    };
+    const int o_u = row_off(p.u, p.su), o_d = row_off(p.delta, p.sd);
+    const int o_z = has_z ? row_off(p.z, p.sz) : 0;
+    // outputs staged for the producer (out rows not 16-byte aligned)
+    const bool ostage = CF::OSTAGE && !SUMMARY && !p.out_vec;
+    uint64_t *bar_ofull = reinterpret_cast<uint64_t *>(smem + CF::OFF_OBAR);
+    const int o_out = ostage ? row_off(p.out, p.so) : 0;
+    auto tile_row = [&](const unsigned char *tile, int col, int o, auto &v) {
+      if constexpr (USE_TMA) lds_row<T, EPT>(tile, c, col, v);
+      else lds_row_off<T, EPT>(tile + c * CF::ROWB, col, o, v);
+    };
     T *gout = static_cast<T *>(p.out);
     const long long orow = (long long)b * p.so[0] + (long long)d * p.so[1];
     const bool out_vec = p.out_vec != 0;
@@ -761,8 +1064,8 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       const int col0 = sub * S + h * EPT;
       const int t0 = tseg0 + ci * L + col0;
       float uv[EPT], dv[EPT];
-      lds_row<T, EPT>(su, c, col0, uv);
-      lds_row<T, EPT>(sd, c, col0, dv);
+      tile_row(su, col0, o_u, uv);
+      tile_row(sd, col0, o_d, dv);
 #pragma unroll
       for (int k = 0; k < EPT; ++k) {
         const float v = dv[k] + bias;
@@ -811,17 +1114,31 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       const unsigned char *sz = smem + CF::OFF_Z + s * CF::TILE;
       const int col0 = sub * S + h * EPT;
       float uv[EPT];
-      lds_row<T, EPT>(su, c, col0, uv);
+      tile_row(su, col0, o_u, uv);
 #pragma unroll
       for (int k = 0; k < EPT; ++k) y[k] = fmaf(Dd, uv[k], y[k]);
       if (has_z) {
         float zv[EPT];
-        lds_row<T, EPT>(sz, c, col0, zv);
+        tile_row(sz, col0, o_z, zv);
 #pragma unroll
         for (int k = 0; k < EPT; ++k) y[k] *= silu_t<T>(zv[k]);
       }
       const int t0 = tseg0 + ci * L + col0;
-      if (ch_ok && t0 < tseg1) stg_row<T, EPT>(gout + orow + t0, y, out_vec, tseg1 - t0);
+      if (ostage) {
+        // outputs staged for the producer's row stores (it writes only the
+        // rows and steps that belong to this CTA)
+        if (sub == 0 && ci > 0 && !mbar_wait(bar_ofull + 1, (ci - 1) & 1, p.err, kErrWaitEmpty, p.wait_limit))
+          return false;
+        unsigned char *orow_s = smem + CF::OFF_OUT + c * CF::STG_SLOT + o_out + col0 * (int)sizeof(T);
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) reinterpret_cast<T *>(orow_s)[k] = from_f<T>(y[k]);
+        if (sub == SUBS - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_ofull);
+        }
+      } else if (ch_ok && t0 < tseg1) {
+        stg_row<T, EPT>(gout + orow + t0, y, out_vec, tseg1 - t0);
+      }
       if (sub == SUBS - 1) {  // last use of this stage
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_empty[s]);

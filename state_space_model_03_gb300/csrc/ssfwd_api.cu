@@ -584,6 +584,9 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
     std::memset(tm_sum, 0, sizeof(tm_sum));
   }
   kp.tiles_per_group = (kp.dpg + ki.ch - 1) / ki.ch;
+  // rows TMA cannot describe: bulk-copied aligned interiors (SSFWD_NO_BULK:
+  // the plain-load producer, for comparison)
+  kp.rows_bulk = !tma && !std::getenv("SSFWD_NO_BULK");
   ssk::KParams kps = kp;  // summary pass: 32-channel CTAs
   ssk::KernelInfo ks{};
   if (sp.nseg > 1) {
@@ -597,7 +600,7 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   if (std::getenv("SSFWD_DEBUG"))  // opt-in launch report on stderr
     std::fprintf(stderr,
                  "ssfwd: %s np=%d fixed=%d bc_f32=%d ch=%d L=%d grid=%ux%ux%d seg_len=%d sub=%d threads=%d smem=%d\n",
-                 tma ? "tma" : "generic", np, (int)fixed, (int)bc_f32, ki.ch, ki.L, gx, gy, sp.nseg, sp.seg_len,
+                 tma ? "tma" : (kp.rows_bulk ? "generic-bulk" : "generic"), np, (int)fixed, (int)bc_f32, ki.ch, ki.L, gx, gy, sp.nseg, sp.seg_len,
                  sub8 ? 8 : 16, ki.threads, ki.smem);
   if (sp.nseg > 1) {
     void *sargs[6] = {&kps, &tm_sum[0], &tm_sum[1], &tm_sum[2], &tm_sum[3], &tm_sum[4]};
