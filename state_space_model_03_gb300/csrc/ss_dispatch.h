@@ -21,7 +21,8 @@ KernelInfo lookup_f16(int np, bool fixed, bool bc_f32, bool tma, bool summary, b
 KernelInfo lookup_bf16(int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8, bool ch16);
 
 // Decode step (ss_state_update): launch parameters and kernel lookup.
-// lpc: lanes per channel (1, 2, 4, 8, 16), 4 states per lane, 256 threads.
+// lpc: lanes per channel, 4 * q states per lane (q 1: lpc 1..16; q 2: lpc
+// 1..8; q 4: lpc 1..4), 256 threads.
 struct SUParams {
   int batch, dim, dstate, dpg;
   int fixed, has_z, has_D, has_bias, softplus;
@@ -32,7 +33,7 @@ struct SUParams {
   void *out;
   long long sst[3], su[2], sd[2], sz[2], so[2], sB[3], sC[3], sA[2];
 };
-const void *state_update_kernel(int in_dtype, bool bc_f32, int lpc);
+const void *state_update_kernel(int in_dtype, bool bc_f32, int lpc, int q);
 
 // Causal depthwise conv1d (ss_causal_conv1d / ss_causal_conv1d_update).
 struct ConvParams {

@@ -7,9 +7,9 @@
 //
 // The step is bound by HBM traffic: the fp32 state is read and written once
 // (8 bytes per (batch, channel, state)); everything else is a few bytes per
-// (batch, channel) or per (batch, group). LPC = ceil(dstate/4) adjacent lanes
-// own one channel, 4 states each (16-byte state and A accesses, so a warp
-// streams 32/LPC contiguous state rows), and reduce y with shuffles. The grid
+// (batch, channel) or per (batch, group). LPC adjacent lanes own one channel,
+// 4 * Q states each (16-byte state and A accesses, so a warp streams 32/LPC
+// contiguous state rows), and reduce y with shuffles. The grid
 // is (channel tiles, batch rows): no integer division in the index math, which
 // measured as the limit of a flat-index version.
 #include "ss_dispatch.h"
@@ -119,7 +119,22 @@ __global__ void __launch_bounds__(256) ss_state_update_kernel(const __grid_const
 }
 
 template <typename T, typename BCT>
-const void *pick(int lpc) {
+const void *pick(int lpc, int q) {
+  if (q == 4) {
+    switch (lpc) {
+      case 1: return (const void *)&ss_state_update_kernel<T, BCT, 1, 4>;
+      case 2: return (const void *)&ss_state_update_kernel<T, BCT, 2, 4>;
+      default: return (const void *)&ss_state_update_kernel<T, BCT, 4, 4>;
+    }
+  }
+  if (q == 2) {
+    switch (lpc) {
+      case 1: return (const void *)&ss_state_update_kernel<T, BCT, 1, 2>;
+      case 2: return (const void *)&ss_state_update_kernel<T, BCT, 2, 2>;
+      case 4: return (const void *)&ss_state_update_kernel<T, BCT, 4, 2>;
+      default: return (const void *)&ss_state_update_kernel<T, BCT, 8, 2>;
+    }
+  }
   switch (lpc) {
     case 1: return (const void *)&ss_state_update_kernel<T, BCT, 1, 1>;
     case 2: return (const void *)&ss_state_update_kernel<T, BCT, 2, 1>;
@@ -131,11 +146,11 @@ const void *pick(int lpc) {
 
 }  // namespace
 
-const void *state_update_kernel(int in_dtype, bool bc_f32, int lpc) {
+const void *state_update_kernel(int in_dtype, bool bc_f32, int lpc, int q) {
   switch (in_dtype) {
-    case 0: return pick<float, float>(lpc);
-    case 1: return bc_f32 ? pick<__half, float>(lpc) : pick<__half, __half>(lpc);
-    default: return bc_f32 ? pick<__nv_bfloat16, float>(lpc) : pick<__nv_bfloat16, __nv_bfloat16>(lpc);
+    case 0: return pick<float, float>(lpc, q);
+    case 1: return bc_f32 ? pick<__half, float>(lpc, q) : pick<__half, __half>(lpc, q);
+    default: return bc_f32 ? pick<__nv_bfloat16, float>(lpc, q) : pick<__nv_bfloat16, __nv_bfloat16>(lpc, q);
   }
 }
 

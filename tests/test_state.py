@@ -165,6 +165,26 @@ def test_state_update_matches_oracle(case, softplus):
     assert _rel(_np(s), ref_state) <= (1e-5 if dtype == "fp32" else 1e-3)
 
 
+@pytest.mark.parametrize("q", [1, 2, 4])
+@pytest.mark.parametrize("case", [c for c in STEP_CASES if c[2] in (13, 16, 32, 64)],
+                         ids=lambda c: f"{c[4]}_{c[5]}_n{c[2]}")
+def test_state_update_every_lane_split(case, q, monkeypatch):
+    """Every split of a channel's states over lanes (4, 8 or 16 states a lane;
+    the default is 8) gives the oracle's result."""
+    monkeypatch.setenv("SSFWD_SU_Q", str(q))
+    batch, dim, n, g, dtype, form, bc_f32 = case
+    st, u, delta, A, B, C, D, z, bias = _step_inputs(batch, dim, n, g, dtype, form, 90 + n, bc_f32)
+    ref_out, ref_state = oracle.selective_state_update_ref(st, u, delta, A, B, C, D=D, z=z, delta_bias=bias,
+                                                           delta_softplus=True, bc_fixed=form == "fixed")
+    s = st.cuda()
+    out = api.selective_state_update(s, u.cuda(), delta.cuda(), A.cuda(), B.cuda(), C.cuda(), D=D.cuda(),
+                                     z=z.cuda(), delta_bias=bias.cuda(), delta_softplus=True,
+                                     bc_fixed=form == "fixed")
+    torch.cuda.synchronize()
+    assert _rel(_np(out), ref_out) <= TOL[dtype]
+    assert _rel(_np(s), ref_state) <= (1e-5 if dtype == "fp32" else 1e-3)
+
+
 def test_state_update_optional_operands_and_views():
     """No z, D or bias; state as a strided view (odd row stride: the scalar path)."""
     batch, dim, n = 3, 80, 16
