@@ -14,11 +14,12 @@ struct KernelInfo {
 // np in {4, 8, 16, 32, 64}; bc_f32: variable B/C stored as fp32 (else in the
 // input dtype); summary: the segment-summary pass instead of the forward;
 // sub8: 8-step hand-offs (instantiated for the TMA forward only); ch16:
-// 16-channel CTAs (TMA forward, np == 16 only).
+// 16-channel CTAs (TMA forward, np == 16 only); ys: y summed by the scan
+// warps (TMA forward, np == 16, 16-step hand-offs, 32-channel CTAs only).
 // Returns fn == nullptr if not instantiated.
-KernelInfo lookup_f32(int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8, bool ch16);
-KernelInfo lookup_f16(int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8, bool ch16);
-KernelInfo lookup_bf16(int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8, bool ch16);
+KernelInfo lookup_f32(int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8, bool ch16, bool ys);
+KernelInfo lookup_f16(int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8, bool ch16, bool ys);
+KernelInfo lookup_bf16(int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8, bool ch16, bool ys);
 
 // Decode step (ss_state_update): launch parameters and kernel lookup.
 // lpc: lanes per channel, 4 * q states per lane (q 1: lpc 1..16; q 2: lpc

@@ -2,7 +2,7 @@
 #include "ss_fwd_instances.cuh"
 
 namespace ssk {
-KernelInfo lookup_bf16(int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8, bool ch16) {
-  return reg::lookup<__nv_bfloat16>(np, fixed, bc_f32, tma, summary, sub8, ch16);
+KernelInfo lookup_bf16(int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8, bool ch16, bool ys) {
+  return reg::lookup<__nv_bfloat16>(np, fixed, bc_f32, tma, summary, sub8, ch16, ys);
 }
 }  // namespace ssk

@@ -417,7 +417,10 @@ __device__ __forceinline__ void lds_row_off(const unsigned char *row, int col, i
 // z tiles hold each row as the 16-byte blocks that cover it (144 bytes a row,
 // row byte k at offset (row address & 15) + k), plus a staging buffer for
 // B/C rows.
-template <typename T, int NP, int K, bool FIXED, bool BCF32, int SUB = 16, int CHN = 32, bool GEN = false>
+// YS: the scan warps sum y over their TN lanes before the hand-off (a
+// smaller y slot: a fourth CTA per SM fits with 16-step hand-offs).
+template <typename T, int NP, int K, bool FIXED, bool BCF32, int SUB = 16, int CHN = 32, bool GEN = false,
+          bool YS = false>
 struct Cfg {
   using BCT = typename std::conditional<BCF32, float, T>::type;  // stored B/C type (variable B/C)
   static constexpr int TN = NP / K;              // scan lanes per channel
@@ -474,7 +477,12 @@ struct Cfg {
   // producer alone was 5% slower there)
   static constexpr bool PPACK = !FIXED && !BCPACK && SSK_PPACK != 0;
   static constexpr int OFF_Y = OFF_BC + NSLOT * BC_SLOT;
-  static constexpr int Y_SLOT = S * CH * TN * 4;                  // partial y [S][CH*TN]
+  // YS: y summed over the TN lanes, [CH][YP] (a channel's steps contiguous,
+  // rows padded to S + 4 floats so that 8 lanes reading 16 bytes of 8
+  // channels at one step offset hit distinct banks); else the TN partial y's
+  // [S][CH * TN]
+  static constexpr int YP = S + 4;
+  static constexpr int Y_SLOT = YS ? CH * YP * 4 : S * CH * TN * 4;
   static constexpr int OFF_BAR = OFF_Y + NSLOT * Y_SLOT;
   static constexpr int NBAR = 2 * STAGES + 4 * NSLOT;
   // GEN: staging for 32 B/C row pieces of 128 bytes (144 with their covering
@@ -505,14 +513,15 @@ struct Cfg {
 // hand-off buffers (a fourth CTA fits per SM on 16-bit inputs) at the cost of
 // twice the hand-offs; the host picks it only when that occupancy is needed.
 // CHN: channels per CTA; 16 gives twice the CTAs for a finer spread over SMs.
-template <typename T, int NP, int K, bool FIXED, bool BCF32, bool USE_TMA, bool SUMMARY, int SUB = 16, int CHN = 32>
-__global__ void __launch_bounds__(Cfg<T, NP, K, FIXED, BCF32, SUB, CHN, !USE_TMA>::THREADS,
-                                  Cfg<T, NP, K, FIXED, BCF32, SUB, CHN, !USE_TMA>::MINB)
+template <typename T, int NP, int K, bool FIXED, bool BCF32, bool USE_TMA, bool SUMMARY, int SUB = 16, int CHN = 32,
+          bool YS = false>
+__global__ void __launch_bounds__(Cfg<T, NP, K, FIXED, BCF32, SUB, CHN, !USE_TMA, YS>::THREADS,
+                                  Cfg<T, NP, K, FIXED, BCF32, SUB, CHN, !USE_TMA, YS>::MINB)
 ss_fwd_kernel(const __grid_constant__ KParams p,
               const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
               const __grid_constant__ CUtensorMap tm_C) {
-  using CF = Cfg<T, NP, K, FIXED, BCF32, SUB, CHN, !USE_TMA>;
+  using CF = Cfg<T, NP, K, FIXED, BCF32, SUB, CHN, !USE_TMA, YS>;
   using BCT = typename CF::BCT;
   constexpr int TN = CF::TN, CPW = CF::CPW, CPL = CF::CPL, CH = CF::CH, L = CF::L, S = CF::S, SUBS = CF::SUBS;
   constexpr int STAGES = CF::STAGES, WS = CF::WS, WE = CF::WE, EPT = CF::EPT;
@@ -1092,21 +1101,30 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       if (!mbar_wait(&bar_yfull[slot], (q / NSLOT) & 1, p.err, kErrWaitReady, p.wait_limit)) return false;
       const float *Y = reinterpret_cast<const float *>(smem + CF::OFF_Y + slot * CF::Y_SLOT);
       float y[EPT];
+      if constexpr (YS) {
+        static_assert(EPT % 4 == 0, "16-byte y reads");
 #pragma unroll
-      for (int k = 0; k < EPT; ++k) {
-        const float *row = Y + (h * EPT + k) * (CH * TN) + c * TN;
-        float acc = 0.f;
-        if constexpr (TN % 4 == 0) {
-#pragma unroll
-          for (int jj = 0; jj < TN; jj += 4) {
-            const float4 v4 = *reinterpret_cast<const float4 *>(row + jj);
-            acc += (v4.x + v4.y) + (v4.z + v4.w);
-          }
-        } else {
-#pragma unroll
-          for (int jj = 0; jj < TN; ++jj) acc += row[jj];
+        for (int k = 0; k < EPT; k += 4) {
+          const float4 v4 = *reinterpret_cast<const float4 *>(Y + c * CF::YP + h * EPT + k);
+          y[k] = v4.x; y[k + 1] = v4.y; y[k + 2] = v4.z; y[k + 3] = v4.w;
         }
-        y[k] = acc;
+      } else {
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+          const float *row = Y + (h * EPT + k) * (CH * TN) + c * TN;
+          float acc = 0.f;
+          if constexpr (TN % 4 == 0) {
+#pragma unroll
+            for (int jj = 0; jj < TN; jj += 4) {
+              const float4 v4 = *reinterpret_cast<const float4 *>(row + jj);
+              acc += (v4.x + v4.y) + (v4.z + v4.w);
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < TN; ++jj) acc += row[jj];
+          }
+          y[k] = acc;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_yempty[slot]);
@@ -1400,12 +1418,39 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
           }
         }
         if constexpr (!SUMMARY) {
-          if (tl % YB == YB - 1) {
+          if (!YS && tl % YB == YB - 1) {
 #pragma unroll
             for (int u = 0; u < YB; ++u)
 #pragma unroll
               for (int i = 0; i < CPL; ++i)  // step-major rows
                 Y[(tl - YB + 1 + u) * (CH * TN) + (cbase + i) * TN + j] = yv[i][u];
+          }
+          if (YS && tl % YB == YB - 1) {
+            // sum the partial y's of the channel group's TN lanes by a
+            // reduce-scatter: the CPL * YB values (step-major) halve each
+            // round, lane j keeping block j of the sums, which it stores
+            constexpr int NV = CPL * YB, VPL = NV / TN;
+            static_assert(NV % TN == 0, "y values split evenly over the channel's lanes");
+            float v[NV];
+#pragma unroll
+            for (int u = 0; u < YB; ++u)
+#pragma unroll
+              for (int i = 0; i < CPL; ++i) v[u * CPL + i] = yv[i][u];
+#pragma unroll
+            for (int m = TN / 2, len = NV; m > 0; m >>= 1, len >>= 1) {
+              const bool up = (j & m) != 0;
+#pragma unroll
+              for (int k = 0; k < len / 2; ++k) {
+                const float send = up ? v[k] : v[k + len / 2];
+                const float keep = up ? v[k + len / 2] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+              const int idx = j * VPL + k, u = idx / CPL, i = idx - u * CPL;
+              Y[(cbase + i) * CF::YP + tl - YB + 1 + u] = v[k];
+            }
           }
         }
       }

@@ -24,8 +24,8 @@ __device__ int32_t g_error_word;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int32_t *g_err_ptr[kMaxDevices] = {};
-bool g_attr_done[kMaxDevices][3][5][2][2][2][2][2][2] = {};
-int g_occupancy[kMaxDevices][3][5][2][2][3] = {};  // CTAs/SM of the TMA forward variants 0, 1, 2
+bool g_attr_done[kMaxDevices][3][5][2][2][2][2][2][2][2] = {};
+int g_occupancy[kMaxDevices][3][5][2][2][4] = {};  // CTAs/SM of the TMA forward variants 0 .. 3
 bool g_bwd_attr_done[kMaxDevices][3][2][2] = {};     // dynamic shared memory attribute set for ss_bwd
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -177,11 +177,11 @@ int padded_states(int64_t n) {
 int np_index(int np) { return np == 4 ? 0 : np == 8 ? 1 : np == 16 ? 2 : np == 32 ? 3 : 4; }
 
 ssk::KernelInfo lookup(int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary, bool sub8 = false,
-                       bool ch16 = false) {
+                       bool ch16 = false, bool ys = false) {
   switch (dt) {
-    case SS_F32: return ssk::lookup_f32(np, fixed, bc_f32, tma, summary, sub8, ch16);
-    case SS_F16: return ssk::lookup_f16(np, fixed, bc_f32, tma, summary, sub8, ch16);
-    default: return ssk::lookup_bf16(np, fixed, bc_f32, tma, summary, sub8, ch16);
+    case SS_F32: return ssk::lookup_f32(np, fixed, bc_f32, tma, summary, sub8, ch16, ys);
+    case SS_F16: return ssk::lookup_f16(np, fixed, bc_f32, tma, summary, sub8, ch16, ys);
+    default: return ssk::lookup_bf16(np, fixed, bc_f32, tma, summary, sub8, ch16, ys);
   }
 }
 
@@ -374,9 +374,9 @@ bool lane_setup(const ss_fwd_params *p, int dev, int64_t cap, LanePlan *lp) {
 }
 
 bool set_smem_attr(int dev, const ssk::KernelInfo &ki, int dt, int np, bool fixed, bool bc_f32, bool tma, bool summary,
-                   bool sub8 = false, bool ch16 = false) {
+                   bool sub8 = false, bool ch16 = false, bool ys = false) {
   std::lock_guard<std::mutex> lk(g_mu);
-  bool &done = g_attr_done[dev][dt][np_index(np)][fixed][bc_f32 && !fixed][tma][summary][sub8][ch16];
+  bool &done = g_attr_done[dev][dt][np_index(np)][fixed][bc_f32 && !fixed][tma][summary][sub8][ch16][ys];
   if (!done) {
     if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) != cudaSuccess)
       return false;
@@ -528,24 +528,28 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   const int groups = kp.ngroups;
   // Forward variant: 32-channel CTAs with 16-step hand-offs (0), the same
   // with 8-step hand-offs (1: smaller buffers, one more resident CTA per SM,
-  // about 1.36x the time per CTA), or 16-channel CTAs (2). A CTA's time
-  // grows only mildly with the CTAs that share its SM (the recurrence is
-  // latency-bound), so the variant that runs the grid in the fewest waves of
-  // resident CTAs wins. Among equals: 16-channel CTAs when the 32-channel grid
-  // leaves no SM more than two CTAs (about 5% faster there), else variant 0.
-  bool sub8 = false, ch16 = false;
+  // about 1.36x the time per CTA), 16-channel CTAs (2), or the scan warps
+  // summing y over their lanes (3: a smaller y slot, so a fourth 16-step CTA
+  // fits per SM; about 7% slower than variant 0 per CTA, 20% faster than
+  // variant 1). A CTA's time grows only mildly with the CTAs that share its SM
+  // (the recurrence is latency-bound), so the variant that runs the grid in
+  // the fewest waves of resident CTAs wins. Among equals: 16-channel CTAs when
+  // the 32-channel grid leaves no SM more than two CTAs (about 5% faster
+  // there), else variant 0, then 3.
+  bool sub8 = false, ch16 = false, ys = false;
   if (tma) {
-    ssk::KernelInfo kv[3] = {};
-    int64_t waves[3] = {0, 0, 0}, ctas[3] = {0, 0, 0};
+    ssk::KernelInfo kv[4] = {};
+    int64_t waves[4] = {0, 0, 0, 0}, ctas[4] = {0, 0, 0, 0};
     const char *force = std::getenv("SSFWD_VARIANT");  // diagnostics: one variant only
-    for (int v = 0; v < 3; ++v) {
-      const bool v8 = v == 1, v16 = v == 2;
+    for (int v = 0; v < 4; ++v) {
+      const bool v8 = v == 1, v16 = v == 2, vys = v == 3;
       if (v16 && std::getenv("SSFWD_NO_CH16")) continue;
       if (v8 && std::getenv("SSFWD_NO_SUB8")) continue;
+      if (vys && std::getenv("SSFWD_NO_YSUM")) continue;
       if (force && std::atoi(force) != v) continue;
-      ssk::KernelInfo k = lookup(p->in_dtype, np, fixed, bc_f32, true, false, v8, v16);
+      ssk::KernelInfo k = lookup(p->in_dtype, np, fixed, bc_f32, true, false, v8, v16, vys);
       if (!k.fn) continue;
-      if (!set_smem_attr(dev, k, p->in_dtype, np, fixed, bc_f32, true, false, v8, v16)) return SS_ERR_CUDA;
+      if (!set_smem_attr(dev, k, p->in_dtype, np, fixed, bc_f32, true, false, v8, v16, vys)) return SS_ERR_CUDA;
       int occ = 0;
       {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -560,10 +564,10 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
       waves[v] = (ctas[v] + int64_t(occ) * nsm - 1) / (int64_t(occ) * nsm);
     }
     const int64_t ctas32 = int64_t((kp.dpg + 31) / 32) * groups * kp.batch * sp.nseg;
-    const int order_small[3] = {2, 0, 1}, order[3] = {0, 2, 1};
+    const int order_small[4] = {2, 0, 3, 1}, order[4] = {0, 2, 3, 1};
     const int *pref = ctas32 <= 2 * int64_t(nsm) ? order_small : order;
     int best = -1;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 4; ++i) {
       const int v = pref[i];
       if (kv[v].fn && (best < 0 || waves[v] < waves[best])) best = v;
     }
@@ -572,6 +576,7 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
       bestk = kv[best];
       sub8 = best == 1;
       ch16 = best == 2;
+      ys = best == 3;
     }
     ki = bestk;
     if (ch16 && !encode(tm, ki.ch)) return SS_ERR_INTERNAL;
@@ -599,9 +604,9 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   const unsigned gx = static_cast<unsigned>(kp.tiles_per_group * kp.ngroups), gy = static_cast<unsigned>(kp.batch);
   if (std::getenv("SSFWD_DEBUG"))  // opt-in launch report on stderr
     std::fprintf(stderr,
-                 "ssfwd: %s np=%d fixed=%d bc_f32=%d ch=%d L=%d grid=%ux%ux%d seg_len=%d sub=%d threads=%d smem=%d\n",
+                 "ssfwd: %s np=%d fixed=%d bc_f32=%d ch=%d L=%d grid=%ux%ux%d seg_len=%d sub=%d ysum=%d threads=%d smem=%d\n",
                  tma ? "tma" : (kp.rows_bulk ? "generic-bulk" : "generic"), np, (int)fixed, (int)bc_f32, ki.ch, ki.L, gx, gy, sp.nseg, sp.seg_len,
-                 sub8 ? 8 : 16, ki.threads, ki.smem);
+                 sub8 ? 8 : 16, (int)ys, ki.threads, ki.smem);
   if (sp.nseg > 1) {
     void *sargs[6] = {&kps, &tm_sum[0], &tm_sum[1], &tm_sum[2], &tm_sum[3], &tm_sum[4]};
     const unsigned sx = static_cast<unsigned>(kps.tiles_per_group * kps.ngroups);

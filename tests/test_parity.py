@@ -380,9 +380,10 @@ def test_fixed_bc_one_lane_per_channel(case, capfd, monkeypatch):
         assert _rel(lst.double().cpu().numpy(), ref_last) <= TOL[dt]
 
 
-VARIANT_OF = {("32", "16"): 0, ("32", "8"): 1, ("16", "16"): 2}  # (ch, sub) of the launch report
+# (ch, sub, ysum) of the launch report
+VARIANT_OF = {("32", "16", "0"): 0, ("32", "8", "0"): 1, ("16", "16", "0"): 2, ("32", "16", "1"): 3}
 VARIANT_CASES = [
-    # 16 states (all three forward variants exist), ragged channel tiles and
+    # 16 states (all four forward variants exist), ragged channel tiles and
     # steps, two groups; one 16-bit and one fp32 case
     workloads.Workload("variants_bf16", 2, 2 * 80, 296, 16, groups=2, bc_4d=True, dtype="bf16",
                        return_last_state=True, seed=31),
@@ -390,11 +391,12 @@ VARIANT_CASES = [
 ]
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
 @pytest.mark.parametrize("w", VARIANT_CASES, ids=lambda w: w.name)
 def test_each_forward_variant(w, variant, monkeypatch, capfd):
     """Every forward variant (0: 32-channel CTAs, 16-step hand-offs; 1: 8-step
-    hand-offs; 2: 16-channel CTAs), forced one at a time, matches the oracle.
+    hand-offs; 2: 16-channel CTAs; 3: as 0 with y summed over each channel's
+    lanes by the scan warps), forced one at a time, matches the oracle.
     Rows are 16-byte aligned so that the TMA path (which has the variants)
     runs."""
     monkeypatch.setenv("SSFWD_VARIANT", str(variant))
@@ -404,7 +406,7 @@ def test_each_forward_variant(w, variant, monkeypatch, capfd):
     out, last = _run(x)
     line = [ln for ln in capfd.readouterr().err.splitlines() if ln.startswith("ssfwd:")][-1]
     f = dict(kv.split("=") for kv in line.split()[2:] if "=" in kv)
-    assert line.split()[1] == "tma" and VARIANT_OF[(f["ch"], f["sub"])] == variant, line
+    assert line.split()[1] == "tma" and VARIANT_OF[(f["ch"], f["sub"], f["ysum"])] == variant, line
     _check_full(w, x, out, last)
 
 
@@ -417,19 +419,22 @@ def _picked(capfd, w):
     err = capfd.readouterr().err
     line = [ln for ln in err.splitlines() if ln.startswith("ssfwd:")][-1]
     f = dict(kv.split("=") for kv in line.split()[2:] if "=" in kv)
-    return VARIANT_OF[(f["ch"], f["sub"])]
+    return VARIANT_OF[(f["ch"], f["sub"], f["ysum"])]
 
 
 def test_variant_choice_follows_waves(capfd, monkeypatch):
     """With 152 SMs: a grid that fits the resident 32-channel CTAs runs variant
-    0; one that needs a second wave of them but fits with 8-step hand-offs runs
-    variant 1; one that leaves every SM at most two 32-channel CTAs runs
-    16-channel CTAs. Sizes are small in seqlen; the choice depends only on
-    the grid."""
+    0; one that needs a second wave of them but fits with the smaller y
+    hand-off (a fourth CTA per SM) runs variant 3, or variant 1 when variant 3
+    is turned off; one that leaves every SM at most two 32-channel CTAs runs
+    16-channel CTAs. Sizes are small in seqlen; the choice depends only on the
+    grid."""
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("the expected choices are stated for 152 SMs")
     monkeypatch.setenv("SSFWD_DEBUG", "1")
     mk = lambda b, d, g: workloads.Workload("pick", b, d, 96, 16, groups=g, bc_4d=g > 1, dtype="bf16", seed=5)
     assert _picked(capfd, mk(8, 1536, 1)) == 0   # 384 CTAs <= 3 per SM
-    assert _picked(capfd, mk(4, 4096, 4)) == 1   # 512 CTAs: 4 per SM fit only with 8-step hand-offs
+    assert _picked(capfd, mk(4, 4096, 4)) == 3   # 512 CTAs: 4 per SM fit with the smaller y hand-off
     assert _picked(capfd, mk(4, 1536, 1)) == 2   # 192 CTAs: at most 2 per SM
+    monkeypatch.setenv("SSFWD_NO_YSUM", "1")
+    assert _picked(capfd, mk(4, 4096, 4)) == 1   # ... or with 8-step hand-offs
