@@ -200,7 +200,51 @@ ss_fwd_lane_kernel(const __grid_constant__ KParams p, const __grid_constant__ CU
 #pragma unroll
           for (int k = 0; k < G; ++k) yv[k] *= silu_t<T>(zv[k]);
         }
-        if (ok && tg < tseg1) stg_row<T, G>(gout + orow + tg, yv, out_vec, tseg1 - tg);
+        if (out_vec) {
+          // y replaces the u values just read (same lane, same 16 bytes); the
+          // warp stores the chunk's rows whole below
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if constexpr (sizeof(T) == 4) w[i] = __float_as_uint(yv[i]);
+            else w[i] = pack2<T>(yv[2 * i], yv[2 * i + 1]);
+          }
+          *reinterpret_cast<uint4 *>(tile(s, 0) + swz(lane, g * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else if (ok && tg < tseg1) {
+          stg_row<T, G>(gout + orow + tg, yv, false, tseg1 - tg);
+        }
+      }
+    }
+    if constexpr (!SUMMARY) {
+      if (out_vec) {
+        // the chunk's outputs, row by row: 8 lanes store one row's 128
+        // contiguous bytes, 4 rows per warp store (instead of each lane
+        // storing 16 bytes into each of 32 rows); only steps of this segment
+        __syncwarp();
+        const int tv = min(L, tseg1 - tc0);
+        constexpr int EPC = 16 / (int)sizeof(T);  // elements per 16-byte piece
+#pragma unroll 2
+        for (int it = 0; it < 8; ++it) {
+          const int r = it * 4 + (lane >> 3), c16 = lane & 7, e0 = c16 * EPC;
+          const int dr = d0 + r;
+          if (dr < p.dim && e0 < tv) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(tile(s, 0) + swz(r, 16 * c16));
+            T *dst = gout + (long long)b * p.so[0] + (long long)dr * p.so[1] + tc0 + e0;
+            if (e0 + EPC <= tv) {
+              *reinterpret_cast<uint4 *>(dst) = v;
+            } else {  // the sequence's last, partial chunk: element by element
+              const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < EPC; ++e) {
+                if (e >= tv - e0) break;
+                if constexpr (sizeof(T) == 4)
+                  reinterpret_cast<uint32_t *>(dst)[e] = wv[e];
+                else
+                  reinterpret_cast<uint16_t *>(dst)[e] = static_cast<uint16_t>(wv[e / 2] >> (16 * (e & 1)));
+              }
+            }
+          }
+        }
       }
     }
     __syncwarp();  // every lane is done with stage s
