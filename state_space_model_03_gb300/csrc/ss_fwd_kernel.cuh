@@ -100,7 +100,7 @@ struct KParams {
   int32_t *err;
   uint32_t wait_limit;  // try_wait calls before a wait gives up (kMaxWaitIters in production)
   int stall_chunk;      // test hook: chunk the producer never issues (-1: none)
-  int rows_bulk;        // producer without TMA: stage rows by bulk copies (else plain loads)
+  int rows_bulk;        // producer without TMA: rows by 16-byte asynchronous copies (else plain loads)
 };
 
 // ----------------------------------------------------------------------------
@@ -1012,7 +1012,7 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     }
     if (USE_TMA && !ok) {
       // give copies already in flight a bounded chance to land before exiting
-      // (the generic producer has none left: stage_rows waits for its own)
+      // (the producer without TMA has none left: it waits for its own copies)
       for (int ci = (issued > STAGES ? issued - STAGES : 0); ci < issued; ++ci)
         (void)mbar_wait(&bar_full[ci % STAGES], (ci / STAGES) & 1, p.err, kErrWaitFull, p.wait_limit);
     }

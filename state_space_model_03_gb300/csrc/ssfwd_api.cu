@@ -512,8 +512,9 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
   kp.seg_len = sp.seg_len;
   kp.ws = sp.nseg > 1 ? static_cast<float *>(ws) : nullptr;
 
-  // TMA when every streamed tensor has a legal descriptor; else the generic
-  // (plain-load) producer with the same compute path.
+  // TMA when every streamed tensor has a legal descriptor; else the instance
+  // without tensor maps (rows copied as their covering 16-byte blocks), with
+  // the same compute path.
   auto encode = [&](CUtensorMap *tm, int ch) -> bool {
     std::memset(tm, 0, 5 * sizeof(CUtensorMap));
     bool ok = make_map3(&tm[0], p->u, es, p, p->u_stride, ki.L, ch);
@@ -589,8 +590,9 @@ int launch(const ss_fwd_params *p, cudaStream_t stream, void *ws, int64_t ws_byt
     std::memset(tm_sum, 0, sizeof(tm_sum));
   }
   kp.tiles_per_group = (kp.dpg + ki.ch - 1) / ki.ch;
-  // rows TMA cannot describe: bulk-copied aligned interiors (SSFWD_NO_BULK:
-  // the plain-load producer, for comparison)
+  // rows TMA cannot describe: the producer copies the 16-byte blocks that
+  // cover each row (SSFWD_NO_BULK: plain loads into the same layout, for
+  // comparison)
   kp.rows_bulk = !tma && !std::getenv("SSFWD_NO_BULK");
   ssk::KParams kps = kp;  // summary pass: 32-channel CTAs
   ssk::KernelInfo ks{};
