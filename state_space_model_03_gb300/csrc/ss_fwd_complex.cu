@@ -48,6 +48,15 @@ __device__ __forceinline__ float cos_approx(float x) {
 }
 template <bool FAST>
 __device__ __forceinline__ void sincos_rr(float th, float lo, float &sn, float &cs) {
+  if constexpr (FAST) {
+    // sin.approx / cos.approx keep an absolute error near 2^-21 for |x| up to
+    // 100 pi on their own, so angles in that range skip the reduction
+    if (fabsf(th + lo) <= 314.0f) {
+      sn = sin_approx(th + lo);
+      cs = cos_approx(th + lo);
+      return;
+    }
+  }
   const float k = rintf(th * 0.636619772367581343f);  // 2 / pi
   float r = fmaf(-k, 1.5707963705062866f, th);
   r = fmaf(-k, -4.371138828673793e-08f, r);
