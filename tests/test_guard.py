@@ -8,8 +8,10 @@ every byte outside the view must still hold the poison, and the view itself
 must equal the output of the same call on plainly allocated tensors. The
 shapes are ragged on purpose: dim 37 (a partial channel tile), seqlen 1, 7 and
 257 (partial chunks and sub-chunks), dstate 3 and 13 (padded state slots),
-the TMA and the plain-load producers, and the split-sequence schedule with
-its workspace guarded too.
+the TMA producer and the one without tensor maps (odd row lengths, outputs
+staged and written back by row), the one-lane-per-channel kernel (whole-row
+output stores, partial last chunks), and the split-sequence schedule with its
+workspace guarded too.
 """
 import ctypes
 
@@ -82,6 +84,12 @@ FWD_CASES = [
        return_last_state=True, seed=305), 4, 3),
     (W("g_grouped_bf16", 2, 74, 200, 16, groups=2, bc_4d=True, dtype="bf16", return_last_state=True,
        seed=306), 8, 0),
+    # fixed B/C on TMA-legal rows: the one-lane-per-channel kernel, whose outputs leave as whole rows
+    # of a chunk; a partial last chunk (264 = 4 x 64 + 8, 260 = 8 x 32 + 4) and a partial channel tile
+    (W("g_lane_bf16_l264", 2, 37, 264, 13, bc="fixed", dtype="bf16", bc_std=0.25, return_last_state=True,
+       seed=309), 8, 2),
+    (W("g_lane_fp32_l260", 2, 37, 260, 13, bc="fixed", dtype="fp32", has_z=False, bc_std=0.25,
+       return_last_state=True, seed=310), 4, 3),
 ]
 
 
