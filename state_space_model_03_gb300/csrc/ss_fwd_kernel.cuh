@@ -381,6 +381,37 @@ __device__ __forceinline__ void stg_row(T *dst, const float (&v)[N], bool vec, i
   }
 }
 
+// N floats as T packed into N * sizeof(T) / 16 words of 16 bytes.
+template <typename T, int N>
+__device__ __forceinline__ void pack_row(const float (&v)[N], uint4 *w) {
+  constexpr int PE = 16 / (int)sizeof(T);
+  static_assert(N % PE == 0, "whole 16-byte words");
+#pragma unroll
+  for (int q = 0; q < N / PE; ++q) {
+    uint32_t x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (sizeof(T) == 4) x[i] = __float_as_uint(v[q * PE + i]);
+      else x[i] = pack2<T>(v[q * PE + 2 * i], v[q * PE + 2 * i + 1]);
+    }
+    w[q] = make_uint4(x[0], x[1], x[2], x[3]);
+  }
+}
+
+// The elements of a 16-byte block at dst (aligned) whose bytes lie in
+// [from, to) (multiples of sizeof(T)), stored one by one.
+template <typename T>
+__device__ __forceinline__ void stg_block_part(unsigned char *dst, uint4 blk, int from, int to) {
+  const uint32_t w[4] = {blk.x, blk.y, blk.z, blk.w};
+#pragma unroll
+  for (int e = 0; e < 16 / (int)sizeof(T); ++e) {
+    const int off = e * (int)sizeof(T);
+    if (off < from || off >= to) continue;
+    if constexpr (sizeof(T) == 4) *reinterpret_cast<uint32_t *>(dst + off) = w[e];
+    else *reinterpret_cast<uint16_t *>(dst + off) = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+  }
+}
+
 // N consecutive elements (col .. col+N-1) of a row held as its covering
 // 16-byte blocks, the row's byte k at row + o + k (o < 16), widened to fp32.
 // col * sizeof(T) and N * sizeof(T) are multiples of 16.
@@ -486,17 +517,10 @@ struct Cfg {
   static constexpr int OFF_BAR = OFF_Y + NSLOT * Y_SLOT;
   static constexpr int NBAR = 2 * STAGES + 4 * NSLOT;
   // GEN: staging for 32 B/C row pieces of 128 bytes (144 with their covering
-  // blocks; variable B/C) and, when the producer does not convert B/C, for the
-  // chunk's outputs when out rows are not 16-byte aligned (row r's byte k at
-  // (out row address & 15) + k), with its full / empty barriers. (A second
-  // output buffer does not fit beside three CTAs per SM; two half-chunk
-  // buffers measured slower: twice the ragged row ends to write.)
+  // blocks; variable B/C)
   static constexpr int STG_SLOT = 144;
-  static constexpr bool OSTAGE = GEN && !PPACK && !FIXED;  // (fixed B/C keep four CTAs per SM)
   static constexpr int OFF_STG = (OFF_BAR + NBAR * 8 + 127) / 128 * 128;
-  static constexpr int OFF_OUT = OFF_STG + (FIXED ? 0 : 32 * STG_SLOT);
-  static constexpr int OFF_OBAR = OFF_OUT + (OSTAGE ? CH * STG_SLOT : 0);
-  static constexpr int SMEM = GEN ? OFF_OBAR + (OSTAGE ? 16 : 0) : OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = GEN ? OFF_STG + (FIXED ? 0 : 32 * STG_SLOT) : OFF_BAR + NBAR * 8;
   static constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024
   // CTAs per SM the shared memory allows (228 KB per SM, 1 KB reserved per CTA);
   // passed to __launch_bounds__ so the register budget matches that occupancy.
@@ -568,10 +592,6 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       // a stage is released by the element warps and, when it converts the
       // B/C tiles, by the producer (so it cannot refill a stage it still reads)
       mbar_init(&bar_empty[s], WE + (CF::PPACK ? 1 : 0));
-    }
-    if constexpr (CF::OSTAGE) {
-      mbar_init(reinterpret_cast<uint64_t *>(smem + CF::OFF_OBAR), WE);     // outputs of a chunk staged
-      mbar_init(reinterpret_cast<uint64_t *>(smem + CF::OFF_OBAR) + 1, 1);  // staging free again
     }
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&bar_pfull[s], WE + (CF::PPACK ? 1 : 0));
@@ -945,68 +965,6 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         }
       }
       while (ok && issued < nchunks) ok = issue_next();
-    } else if (CF::OSTAGE && !SUMMARY && !p.out_vec) {
-      // outputs staged in shared memory: once the element warps have staged
-      // chunk c, lane r writes out row r's steps of it: the 16-byte-aligned
-      // interior by a bulk copy, the ragged ends (under 16 bytes each) by
-      // two-byte stores; only rows of this CTA's group and steps of this
-      // segment are written. Then the stage of chunk c is refilled.
-      uint64_t *bar_ofull = reinterpret_cast<uint64_t *>(smem + CF::OFF_OBAR), *bar_oempty = bar_ofull + 1;
-      const int rr = d0 + lane;
-      const bool out_ok = tile * CH + lane < p.dpg && rr < p.dim;
-      unsigned char *ost = smem + CF::OFF_OUT + lane * CF::STG_SLOT;
-      const unsigned char *orow =
-          reinterpret_cast<const unsigned char *>(static_cast<T *>(p.out) + b * p.so[0] + (long long)min(rr, p.dim - 1) * p.so[1]);
-      auto store_out = [&](int c) -> bool {
-        if (!mbar_wait(bar_ofull, c & 1, p.err, kErrWaitReady, p.wait_limit)) return false;
-        const int t0 = tseg0 + c * L;
-        const int nb = out_ok ? min(L, tseg1 - t0) * (int)sizeof(T) : 0;
-        unsigned char *dst = const_cast<unsigned char *>(orow) + (long long)t0 * (long long)sizeof(T);
-        const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
-        const int o = static_cast<int>(a & 15);
-        const uintptr_t a0 = (a + 15) & ~uintptr_t(15), a1 = (a + nb) & ~uintptr_t(15);
-        const int inner = (nb > 0 && a1 > a0) ? static_cast<int>(a1 - a0) : 0;
-        if (inner) {
-          asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(a0),
-                       "r"(smem_u32(ost + o + (a0 - a))), "r"(inner) : "memory");
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
-        const int head = inner ? static_cast<int>(a0 - a) : nb, tail0 = inner ? static_cast<int>(a1 - a) : nb;
-        for (int e = 0; e < head; e += 2)  // elements are at least 2-byte aligned
-          *reinterpret_cast<uint16_t *>(dst + e) = *reinterpret_cast<const uint16_t *>(ost + o + e);
-        for (int e = tail0; e < nb; e += 2)
-          *reinterpret_cast<uint16_t *>(dst + e) = *reinterpret_cast<const uint16_t *>(ost + o + e);
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the staging has been read
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_oempty);
-        return true;
-      };
-      while (ok && issued < nchunks && issued < STAGES) ok = issue_next();
-      for (int c = 0; ok && c < nchunks; ++c) {
-        // chunk c's stage and staged outputs are released together: start
-        // the copies of the chunk that refills the stage, write the outputs
-        // back while they are in flight, then finish the stage
-        const int nx = issued;
-        const bool more = nx < nchunks;
-        if (more && !mbar_wait(&bar_empty[c % STAGES], (c / STAGES) & 1, p.err, kErrWaitEmpty, p.wait_limit)) {
-          ok = false;
-          break;
-        }
-        const bool copy = more && nx != p.stall_chunk;  // test hook: that chunk never lands
-        if (copy) {
-          stage_begin(nx);
-          bc_copy(nx, 0);
-        }
-        ok = store_out(c);
-        if (copy) {
-          stage_end(nx);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_full[nx % STAGES]);
-        }
-        if (more) ++issued;
-      }
-      asm volatile("cp.async.wait_all;" ::: "memory");            // no copy still in flight
-      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // every bulk store has completed
     } else {
       while (ok && issued < nchunks) ok = issue_next();
     }
@@ -1045,10 +1003,18 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     };
     const int o_u = row_off(p.u, p.su), o_d = row_off(p.delta, p.sd);
     const int o_z = has_z ? row_off(p.z, p.sz) : 0;
-    // outputs staged for the producer (out rows not 16-byte aligned)
-    const bool ostage = CF::OSTAGE && !SUMMARY && !p.out_vec;
-    uint64_t *bar_ofull = reinterpret_cast<uint64_t *>(smem + CF::OFF_OBAR);
-    const int o_out = ostage ? row_off(p.out, p.so) : 0;
+    // out rows not 16-byte aligned (the instance without tensor maps; with
+    // them out rows are aligned unless out is a view at an odd offset, and are
+    // then stored element by element): each lane stores the 16-byte-aligned
+    // blocks of its row that end inside its piece (EPT steps), taking the 16
+    // bytes before the piece from its half-lane partner (8 lanes away): the
+    // first half's piece for the second half, the previous sub-chunk's second
+    // half (kept in registers) for the first. o_out is the row's byte offset at
+    // the segment's first step, out_end the segment's end in the same
+    // coordinates; blocks reaching past either are written element by element.
+    constexpr bool SHIFT = !USE_TMA && (EPT * (int)sizeof(T)) % 16 == 0;
+    constexpr int NWO = SHIFT ? EPT * (int)sizeof(T) / 16 : 1;  // 16-byte words of a piece
+    const bool shift_out = SHIFT && !SUMMARY && !p.out_vec;
     auto tile_row = [&](const unsigned char *tile, int col, int o, auto &v) {
       if constexpr (USE_TMA) lds_row<T, EPT>(tile, c, col, v);
       else lds_row_off<T, EPT>(tile + c * CF::ROWB, col, o, v);
@@ -1056,6 +1022,10 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
     T *gout = static_cast<T *>(p.out);
     const long long orow = (long long)b * p.so[0] + (long long)d * p.so[1];
     const bool out_vec = p.out_vec != 0;
+    const int o_out = static_cast<int>(reinterpret_cast<uintptr_t>(gout + orow + tseg0) & 15);
+    const int out_end = o_out + (tseg1 - tseg0) * (int)sizeof(T);
+    unsigned char *out_base = reinterpret_cast<unsigned char *>(gout + orow + tseg0) - o_out;  // 16-byte aligned
+    uint4 prev_tail = make_uint4(0u, 0u, 0u, 0u);
     // SUMMARY: sum of dt over my steps of the segment. The forward decays the
     // carried state by exp(A * sum), and a plain fp32 sum over thousands of
     // steps is off by ~1e-4 relative, so it is compensated (Kahan); fp64 adds
@@ -1095,7 +1065,9 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
       return true;
     };
     // epilogue of sub-chunk q: sum partial y, D skip, gate, round, store
-    auto epilogue = [&](int q) -> bool {
+    // shc: std::bool_constant of whether out rows take the shifted stores (the
+    // loop below is compiled once with them and once without)
+    auto epilogue = [&](int q, auto shc) -> bool {
       const int ci = q / SUBS, sub = q - ci * SUBS, s = ci % STAGES;
       const int slot = q % NSLOT;
       if (!mbar_wait(&bar_yfull[slot], (q / NSLOT) & 1, p.err, kErrWaitReady, p.wait_limit)) return false;
@@ -1142,19 +1114,32 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         for (int k = 0; k < EPT; ++k) y[k] *= silu_t<T>(zv[k]);
       }
       const int t0 = tseg0 + ci * L + col0;
-      if (ostage) {
-        // outputs staged for the producer's row stores (it writes only the
-        // rows and steps that belong to this CTA)
-        if (sub == 0 && ci > 0 && !mbar_wait(bar_ofull + 1, (ci - 1) & 1, p.err, kErrWaitEmpty, p.wait_limit))
-          return false;
-        unsigned char *orow_s = smem + CF::OFF_OUT + c * CF::STG_SLOT + o_out + col0 * (int)sizeof(T);
+      bool stored = false;
+      if constexpr (SHIFT && decltype(shc)::value) {
+        {
+          uint4 wv[NWO + 1];  // the 16 bytes before the piece, then the piece
+          pack_row<T, EPT>(y, &wv[1]);
+          const uint4 send = h ? prev_tail : wv[NWO];
+          prev_tail = wv[NWO];
+          wv[0] = make_uint4(__shfl_xor_sync(0xffffffffu, send.x, 8), __shfl_xor_sync(0xffffffffu, send.y, 8),
+                             __shfl_xor_sync(0xffffffffu, send.z, 8), __shfl_xor_sync(0xffffffffu, send.w, 8));
+          if (ch_ok) {
+            const int ps = o_out + (t0 - tseg0) * (int)sizeof(T);  // the piece's first byte
 #pragma unroll
-        for (int k = 0; k < EPT; ++k) reinterpret_cast<T *>(orow_s)[k] = from_f<T>(y[k]);
-        if (sub == SUBS - 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_ofull);
+            for (int j = 0; j <= NWO; ++j) {
+              const int a0 = ps - o_out + 16 * j;  // block start (aligned)
+              const int b0 = max(a0, o_out), b1 = min(a0 + 16, out_end);
+              // the block's last byte of this segment must lie in this piece
+              if (b0 >= b1 || b1 - 1 < ps || b1 - 1 >= ps + 16 * NWO) continue;
+              const uint4 blk = o_out == 0 ? wv[j < NWO ? j + 1 : NWO] : bytes_at(wv[j], wv[j < NWO ? j + 1 : NWO], 16 - o_out);
+              if (b1 - b0 == 16) *reinterpret_cast<uint4 *>(out_base + a0) = blk;
+              else stg_block_part<T>(out_base + a0, blk, b0 - a0, b1 - a0);
+            }
+          }
+          stored = true;
         }
-      } else if (ch_ok && t0 < tseg1) {
+      }
+      if (!stored && ch_ok && t0 < tseg1) {
         stg_row<T, EPT>(gout + orow + t0, y, out_vec, tseg1 - t0);
       }
       if (sub == SUBS - 1) {  // last use of this stage
@@ -1180,11 +1165,19 @@ ss_fwd_kernel(const __grid_constant__ KParams p,
         p.ws[(long long)nsum * NP * p.batch * p.dim + ((long long)b * p.dim + d) * nsum + seg] = lam;
     } else {
       // prep runs NSLOT - 1 sub-chunks ahead of the epilogue
-      bool ok = true;
-      for (int q = 0; q < NSLOT - 1 && q < nsub && ok; ++q) ok = prep(q);
-      for (int q = 0; q < nsub && ok; ++q) {
-        if (q + NSLOT - 1 < nsub && !prep(q + NSLOT - 1)) break;
-        ok = epilogue(q);
+      auto run = [&](auto shc) {
+        bool ok = true;
+        for (int q = 0; q < NSLOT - 1 && q < nsub && ok; ++q) ok = prep(q);
+        for (int q = 0; q < nsub && ok; ++q) {
+          if (q + NSLOT - 1 < nsub && !prep(q + NSLOT - 1)) break;
+          ok = epilogue(q, shc);
+        }
+      };
+      if constexpr (SHIFT) {
+        if (shift_out) run(std::true_type{});
+        else run(std::false_type{});
+      } else {
+        run(std::false_type{});
       }
     }
     return;

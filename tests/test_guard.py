@@ -8,10 +8,11 @@ every byte outside the view must still hold the poison, and the view itself
 must equal the output of the same call on plainly allocated tensors. The
 shapes are ragged on purpose: dim 37 (a partial channel tile), seqlen 1, 7 and
 257 (partial chunks and sub-chunks), dstate 3 and 13 (padded state slots),
-the TMA producer and the one without tensor maps (odd row lengths, outputs
-staged and written back by row), the one-lane-per-channel kernel (whole-row
-output stores, partial last chunks), and the split-sequence schedule with its
-workspace guarded too.
+the TMA producer and the one without tensor maps (odd row lengths: out rows
+stored as aligned blocks formed across each row's lanes, clipped at the
+segment's ends), out views at odd offsets on every forward variant, the
+one-lane-per-channel kernel (whole-row output stores, partial last chunks),
+and the split-sequence schedule with its workspace guarded too.
 """
 import ctypes
 
@@ -112,6 +113,57 @@ def test_forward_writes_nothing_outside_its_outputs(case):
     assert api.device_error() == 0
     assert go.untouched() and gl.untouched()
     assert torch.equal(go.view, ref_out) and torch.equal(gl.view, ref_last)
+
+
+def _guarded_matches_plain(w, opad, lpad, segmented=False):
+    """Run w into plainly allocated outputs and into guarded ones (out rows
+    padded by opad elements, last_state rows by lpad): margins untouched, the
+    same bits."""
+    lib = api.load_library()
+    stream = torch.cuda.current_stream().cuda_stream
+    nu = _inputs(w)
+    u = nu[0]
+    ref_out = torch.empty(u.shape, dtype=u.dtype, device="cuda")
+    ref_last = torch.empty((w.batch, w.dim, w.dstate), device="cuda")
+    p = api.make_params(*nu, w.delta_softplus, ref_out, ref_last)
+    ws = api.attach_workspace(p, u.device)
+    assert lib.ss_fwd(ctypes.byref(p), stream) == 0
+    go = Guarded(tuple(u.shape), u.dtype, opad)
+    gl = Guarded((w.batch, w.dim, w.dstate), torch.float32, lpad)
+    p = api.make_params(*nu, w.delta_softplus, go.view, gl.view)
+    ws2 = api.attach_workspace(p, u.device)
+    assert (ws2 is not None) or not segmented  # the schedule is split when asked
+    assert lib.ss_fwd(ctypes.byref(p), stream) == 0
+    torch.cuda.synchronize()
+    del ws, ws2
+    assert api.device_error() == 0
+    assert go.untouched() and gl.untouched()
+    assert torch.equal(go.view, ref_out) and torch.equal(gl.view, ref_last)
+
+
+@pytest.mark.parametrize("opad", [1, 3])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+def test_unaligned_out_rows_on_every_forward_variant(variant, opad, monkeypatch):
+    """Inputs TMA can describe, out rows that are not 16-byte aligned (296 + 1
+    or + 3 elements a row; ragged channel tiles, two groups): every forced
+    variant writes exactly out's bytes (element by element)."""
+    monkeypatch.setenv("SSFWD_VARIANT", str(variant))
+    _guarded_matches_plain(W("g_uout_bf16", 2, 2 * 40, 296, 16, groups=2, bc_4d=True, dtype="bf16",
+                             return_last_state=True, seed=313), opad, 1)
+
+
+@pytest.mark.parametrize("w", [
+    W("g_uout_seg_bf16", 1, 37, 8192, 16, dtype="bf16", return_last_state=True, seed=314),
+    W("g_uout_seg_fp32", 1, 40, 6000, 16, dtype="fp32", has_z=False, return_last_state=True, seed=315),
+    W("g_uout_seg_bf16_odd", 1, 37, 8191, 16, dtype="bf16", return_last_state=True, seed=316),
+    W("g_uout_seg_fp32_odd", 1, 40, 6001, 16, dtype="fp32", has_z=False, return_last_state=True, seed=317),
+], ids=lambda w: w.name)
+def test_unaligned_out_rows_on_the_split_sequence_schedule(w):
+    """Segments that start and end inside out's 16-byte blocks: each CTA
+    writes only its own steps, so neighbouring segments do not overwrite each
+    other's bytes (the instance without tensor maps, whose aligned blocks are
+    clipped at the segment's ends, runs the odd-length case below)."""
+    _guarded_matches_plain(w, 3, 2, segmented=True)
 
 
 @pytest.mark.parametrize("w", [

@@ -2,8 +2,9 @@
 multiples, views at odd offsets): the forward's producer copies the 16-byte
 blocks that cover each row (reading only inside the tensor, loading the ends of
 a tensor's first and last rows itself), the element warps read the rows at
-their byte offset, B/C rows are shifted into their tiles, and outputs whose
-rows are not 16-byte aligned are staged and written back by row. The plain-load
+their byte offset, B/C rows are shifted into their tiles, and out rows that
+are not 16-byte aligned are stored as aligned 16-byte blocks, each lane forming
+its blocks from its own piece and the 16 bytes before it. The plain-load
 producer (SSFWD_NO_BULK) builds the same tiles, so the two give identical
 results, and both match the oracle."""
 import ctypes
@@ -30,7 +31,7 @@ CASES = [
     (2, 40, 9, 16, 1, "variable", "bf16", None, True),       # pieces of 18 bytes: some without an interior
     (1, 24, 1, 16, 1, "variable", "bf16", None, True),
     (1, 64, 20001, 16, 1, "variable", "bf16", None, True),   # few CTAs: split sequence (summary pass too)
-    (2, 40, 1001, 16, 2, "variable", "bf16", None, True),    # staged outputs: a CTA's rows cross a group end
+    (2, 40, 1001, 16, 2, "variable", "bf16", None, True),    # odd out rows: a CTA's rows cross a group end
     (3, 72, 517, 16, 3, "variable", "bf16", None, False),    # the same, three groups, no gate
 ]
 
@@ -86,8 +87,8 @@ def test_views_at_every_alignment(offset, capfd, monkeypatch):
 @pytest.mark.parametrize("pitch", [2048, 2047 + 9])
 def test_odd_rows_into_other_out_pitches(pitch):
     """Rows TMA cannot describe written into an out tensor whose rows have
-    another pitch (16-byte aligned: vector stores; not: outputs staged and
-    written by the producer): the same bits as a contiguous out."""
+    another pitch (16-byte aligned: vector stores; not: aligned blocks formed
+    across each row's lanes): the same bits as a contiguous out."""
     w = workloads.Workload("pitch", 2, 48, 2047, 16, dtype="bf16", return_last_state=True, seed=77)
     x = workloads.make_inputs(w)
     dev = _to_dev(x)
